@@ -1,0 +1,421 @@
+"""Benchmark of the NVFP4 W4A4 linear layer on GB300.
+
+Headline workload: the prefill / training QLoRA linear
+  Y[8192,2048] = W4A4(X[8192,6144], W[2048,6144]) + (X A^T) B^T * 128/64,
+one step = one nvfp4_gemm call from bf16 X (dynamic per-tensor amax scale,
+in-call NVFP4 quantization of X, the bf16 LoRA down-projection, the tcgen05
+FP4 GEMM with the fused LoRA up-projection), bf16 out.  value = FP4 TFLOP/s
+(2*M*N*K per step; the LoRA's bf16 flops are not counted).
+
+Also measured in the same run (the "secondary" object): the expert-weight
+quantization sweep (32 x [2048,6144], row + column packings, GB/s), the decode
+projections (q_b_proj, o_proj at M = 1, 8, 32: weight GB/s) and the grouped MoE
+up-projection (4096 tokens, top-8 of 256 experts, LoRA r64: TFLOP/s and GB/s).
+
+Timing: CUDA events on the launching stream, after >= 3 warm-up steps;
+inputs rotate over buffers whose total exceeds L2, so no step reads its input
+from L2.  N > 1 (torchrun): every rank runs the same workload on its own GPU
+(replicas; the layer has no data-path exchange on one GPU per replica); the
+time is the max over ranks and value is the total over ranks.
+
+--impl reference: the CPU oracle on this host's cores, on a bounded row sample
+of the same workload, printed with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A4 GEMM FP4 TFLOP/s (prefill QLoRA linear X[8192,6144] x W[2048,6144] + LoRA r64)"
+UNIT = "TFLOP/s"
+PREFILL = dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0)
+L2_BYTES = 129 * 1024 * 1024
+FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"],
+                    bf16_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers --
+def ev_pairs(torch, n):
+    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(n)]
+
+
+def mean_ms(pairs):
+    return sum(a.elapsed_time(b) for a, b in pairs) / max(1, len(pairs))
+
+
+def time_loop(torch, fn, steps, warmup, prof=None):
+    """Run fn(i) warmup + steps times; return ms/step of the timed steps."""
+    for i in range(warmup):
+        fn(i, None)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        fn(warmup + i, None if prof is None else prof[i])
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
+# ---------------------------------------------------------- main workload --
+def prefill_setup(torch, nv, device, rotate):
+    from synth import torch_case
+    c = torch_case("prefill", seed=0, device=device)
+    M, N, K = c["M"], c["N"], c["K"]
+    wq = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
+    xs = [c["x"]] + [torch.empty_like(c["x"]).copy_(c["x"].roll(i * 977, dims=0))
+                     for i in range(1, rotate)]
+    lora = dict(a=c["lora_a"], b=c["lora_b"], alpha=c["alpha"])
+    calls = []
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    for x in xs:
+        call, _ = nv.prepare_gemm(wq["codes_row"], wq["sf_row"], wq["global_scale"], N, K,
+                                  a_bf16=x, lora=lora, out=out)
+        calls.append(call)
+    return c, wq, xs, calls, out
+
+
+def run_main(args, torch, nv, device, rank, world):
+    import ctypes as C
+    M, N, K = PREFILL["M"], PREFILL["N"], PREFILL["K"]
+    rotate = 4                                # 4 x 100.7 MB of X > L2
+    c, wq, xs, calls, out = prefill_setup(torch, nv, device, rotate)
+    prof = ev_pairs(torch, args.steps)
+
+    def step(i, pr):
+        call = calls[i % rotate]
+        if pr is not None:
+            call.args.prof_begin = C.c_void_p(pr[0].cuda_event)
+            call.args.prof_end = C.c_void_p(pr[1].cuda_event)
+        else:
+            call.args.prof_begin = None
+            call.args.prof_end = None
+        call()
+
+    for i in range(args.warmup):
+        step(i, None)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = time_loop(torch, step, args.steps, 0, prof)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        ms = float(t)
+    gemm_ms = mean_ms(prof)
+    flops = 2.0 * M * N * K
+    # end to end: pinned host X in, host Y out, through the same C-ABI call
+    e2e = run_e2e(args, torch, nv, device, wq, c, xs[0])
+    return dict(ms=ms, gemm_ms=gemm_ms, flops=flops, clocks=clk.summary(), e2e=e2e,
+                launches_per_step=4)
+
+
+def run_e2e(args, torch, nv, device, wq, c, x_dev):
+    M, N, K = PREFILL["M"], PREFILL["N"], PREFILL["K"]
+    x_host = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x_dev.cpu())
+    y_host = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=True)
+    x_in = torch.empty_like(x_dev)
+    lora = dict(a=c["lora_a"], b=c["lora_b"], alpha=c["alpha"])
+    call, y = nv.prepare_gemm(wq["codes_row"], wq["sf_row"], wq["global_scale"], N, K,
+                              a_bf16=x_in, lora=lora)
+
+    def step(i, pr):
+        x_in.copy_(x_host, non_blocking=True)
+        call()
+        y_host.copy_(y, non_blocking=True)
+
+    steps = max(3, args.steps // 2)
+    ms = time_loop(torch, step, steps, max(3, args.warmup))
+    return dict(ms=ms, h2d=M * K * 2, d2h=M * N * 2)
+
+
+# ------------------------------------------------------- secondary lines --
+def run_quantize_sweep(torch, nv, device, steps, warmup, pk):
+    import ctypes as C
+    from synth import torch_case
+    c = torch_case("quantize", seed=0, device=device)
+    E, N, K = c["E"], c["N"], c["K"]
+    call, out = nv.prepare_quantize(c["w"], pack="both", sf_layout="swizzled")
+    prof = ev_pairs(torch, steps)
+
+    def step(i, pr):
+        call.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
+        call.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+        call()
+    ms = time_loop(torch, step, steps, warmup, prof)
+    elems = E * N * K
+    alg = elems * (2 + 2 * 0.5625)             # one bf16 read, two NVFP4 packings written
+    kms = mean_ms(prof)
+    del c, out
+    return dict(workload="32 x W[2048,6144] bf16 -> row + column NVFP4 packings, swizzled scales, dynamic g",
+                ms=ms, elements_per_s=elems / (ms * 1e-3), gbs=alg / (ms * 1e-3) / 1e9,
+                kernel_gbs=alg / (kms * 1e-3) / 1e9, algorithmic_bytes=alg,
+                frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
+                note="amax pass + packing pass (2 reads of the 805 MB input); frac uses the packing kernel's time with the algorithmic one-read bytes")
+
+
+def run_decode(torch, nv, device, steps, warmup, pk):
+    import ctypes as C
+    from synth import torch_case
+    res = {}
+    for name in ("decode_q_b_proj", "decode_o_proj"):
+        c = torch_case(name, seed=0, device=device, M=32)
+        N, K = c["N"], c["K"]
+        wq0 = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
+        wbytes = N * K * 0.5625
+        copies = max(2, int(3 * L2_BYTES // wbytes) + 1)        # rotate > 3x L2 of weights
+        wqs = [wq0] + [{k: v.clone() for k, v in wq0.items()} for _ in range(copies - 1)]
+        gx = torch.tensor([16.0 / 2688.0], dtype=torch.float32, device=device)
+        for M in (1, 8, 32):
+            x = c["x"][:M].contiguous()
+            calls = [nv.prepare_gemm(w["codes_row"], w["sf_row"], w["global_scale"], N, K,
+                                     a_bf16=x, a_global_scale=gx)[0] for w in wqs]
+            prof = ev_pairs(torch, steps)
+
+            def step(i, pr, calls=calls):
+                cl = calls[i % len(calls)]
+                cl.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
+                cl.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+                cl()
+            ms = time_loop(torch, step, steps, warmup, prof)
+            kms = mean_ms(prof)
+            alg = wbytes + M * K * 2 + M * N * 2
+            res[f"{name[7:]}_M{M}"] = dict(
+                ms=ms, kernel_ms=kms, weight_gbs=wbytes / (ms * 1e-3) / 1e9,
+                kernel_gbs=alg / (kms * 1e-3) / 1e9, frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
+                path="cuda-core GEMV" if M <= 4 else "tcgen05 GEMM")
+        del wqs, c
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_grouped(torch, nv, device, steps, warmup, pk):
+    import ctypes as C
+    from synth import torch_case
+    c = torch_case("grouped", seed=0, device=device)
+    E, N, K, T, topk = c["E"], c["N"], c["K"], c["T"], c["topk"]
+    wq = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
+    del c["w"]
+    torch.cuda.empty_cache()
+    lora = dict(a=c["lora_a"], b=c["lora_b"], alpha=c["alpha"])
+    call, (d, perm, offs) = nv.prepare_grouped(c["expert_ids"], c["x"], wq["codes_row"],
+                                               wq["sf_row"], wq["global_scale"], N, K, E,
+                                               lora=lora)
+    prof = ev_pairs(torch, steps)
+
+    def step(i, pr):
+        call.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
+        call.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+        call()
+    ms = time_loop(torch, step, steps, warmup, prof)
+    kms = mean_ms(prof)
+    counts = torch.bincount(c["expert_ids"].reshape(-1).long(), minlength=E).cpu()
+    active = int((counts > 0).sum())
+    P = T * topk
+    flops = 2.0 * P * N * K
+    wbytes = active * N * K * 0.5625
+    lbytes = active * (c["rank"] * K + N * c["rank"]) * 2
+    alg = wbytes + lbytes + T * K * 2 + P * N * 2
+    return dict(workload=f"{T} tokens x top-{topk} of {E} experts W_e[{N},{K}] + LoRA r{c['rank']}",
+                ms=ms, tflops=flops / (ms * 1e-3) / 1e12, kernel_ms=kms,
+                kernel_tflops=flops / (kms * 1e-3) / 1e12,
+                kernel_gbs=alg / (kms * 1e-3) / 1e9, active_experts=active,
+                max_rows=int(counts.max()), hbm_frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
+                tensor_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16"] * FP4_PER_BF16))
+
+
+# ----------------------------------------------------------- CPU baseline --
+def cpu_baseline(rows: int = 96):
+    """The oracle on a row sample of the headline workload (host cores)."""
+    import numpy as np
+    from oracle import nvfp4_oracle as o
+    from synth import make_case
+    c = make_case("prefill", M=rows)
+    t0 = time.perf_counter()
+    xq = o.quantize(c["x"])
+    wq = o.quantize(c["w"])
+    o.linear_fp64(xq, wq, c["x"], (c["lora_a"], c["lora_b"], 128.0))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * PREFILL["N"] * PREFILL["K"]
+    return dict(value=flops / dt / 1e12, unit=UNIT, cores=1, kind="oracle",
+                sample=f"{rows} rows of X through quantize + dequantized fp64 GEMM + LoRA "
+                       f"(W quantized each call, as the oracle stands); {dt:.2f} s",
+                seconds=dt)
+
+
+def reference_arm(args):
+    steps, warm = args.steps, args.warmup
+    rows = 24
+    for _ in range(warm):
+        cpu_baseline(rows)
+    ts = [cpu_baseline(rows)["seconds"] for _ in range(steps)]
+    ms = 1e3 * sum(ts) / len(ts)
+    flops = 2.0 * rows * PREFILL["N"] * PREFILL["K"]
+    v = flops / (ms * 1e-3) / 1e12
+    line = dict(impl="reference", metric=METRIC, value=v, unit=UNIT, n_gpus=args.gpus,
+                steps=steps, warmup=warm, ms_per_step=ms, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+                config=dict(workload="prefill QLoRA linear, CPU oracle on a 24-row sample",
+                            M_sample=rows, N=PREFILL["N"], K=PREFILL["K"], rank=64),
+                cpu_baseline=dict(value=v, unit=UNIT, cores=1, kind="oracle",
+                                  sample=f"{rows} rows of X per step"),
+                e2e=dict(value=v, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------- main --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            os.environ.setdefault("OMP_NUM_THREADS", "1")
+            reference_arm(args)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    import nvfp4_block_scaled_06_gb300 as nv
+    nv.load()
+    pk = peaks()
+
+    main_res = run_main(args, torch, nv, device, rank, world)
+    sec = {}
+    if not args.only_main:
+        steps2 = max(10, min(args.steps, 30))
+        sec["quantize"] = run_quantize_sweep(torch, nv, device, steps2, max(3, args.warmup), pk)
+        torch.cuda.empty_cache()
+        sec["decode"] = run_decode(torch, nv, device, steps2, max(3, args.warmup), pk)
+        torch.cuda.empty_cache()
+        sec["grouped"] = run_grouped(torch, nv, device, steps2, max(3, args.warmup), pk)
+        torch.cuda.empty_cache()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    ms = main_res["ms"]
+    value = world * main_res["flops"] / (ms * 1e-3) / 1e12
+    fp4_peak = pk["bf16"] * FP4_PER_BF16
+    gemm_tflops = main_res["flops"] / (main_res["gemm_ms"] * 1e-3) / 1e12
+    e2e = main_res["e2e"]
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=ms, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="e2m1xe2m1->f32 (bf16 LoRA, bf16 out)", data="synthetic",
+        config=dict(workload="prefill QLoRA linear: X[8192,6144] bf16 ~N(0,1) -> NVFP4 (dynamic amax), "
+                             "frozen NVFP4 W[2048,6144] ~N(0,0.02), LoRA A[64,6144] B[2048,64] ~N(0,0.01), "
+                             "alpha 128, Y bf16",
+                    M=PREFILL["M"], N=PREFILL["N"], K=PREFILL["K"], rank=64, alpha=128.0,
+                    l2="X rotates over 4 buffers (403 MB > 129 MB L2)",
+                    parallelism=f"replicas x{world}"),
+        roofline=dict(bound="tensor", kernel="k_gemm_fp4<256>", achieved=gemm_tflops,
+                      peak=fp4_peak, unit="TFLOP/s", frac=gemm_tflops / fp4_peak,
+                      traffic=None,
+                      peak_note=f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x 6 (nominal fp4:bf16)"),
+        e2e=dict(value=world * main_res["flops"] / (e2e["ms"] * 1e-3) / 1e12, unit=UNIT,
+                 h2d_bytes_per_step=e2e["h2d"], d2h_bytes_per_step=e2e["d2h"]),
+        gpu_launches=main_res["launches_per_step"] * args.steps,
+        clocks=main_res["clocks"],
+        secondary=sec,
+    )
+    if not args.no_cpu:
+        cb = cpu_baseline()
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+"""NVFP4 W4A4 linear layer for sm_103a (GB300): Python binding of libnvfp4.
+
+The functions here carry the names of the C entry points in include/nvfp4.h
+and only marshal arguments: outputs and workspaces are allocated with torch on
+the input's device, pointers go into the C argument structs, and the library
+launches every kernel on the current (or given) torch stream.  A missing
+library raises; there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from ._binding import (EXPORTS, GemmArgs, GroupedArgs, LoraArgs, NVFP4Error, OUT_BF16,
+                       OUT_FP32, PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR,
+                       SF_SWIZZLED, check, load)
+
+__all__ = [
+    "load", "NVFP4Error", "nvfp4_quantize", "nvfp4_gemm", "nvfp4_grouped_gemm",
+    "nvfp4_lora_epilogue", "nvfp4_codes_bytes", "nvfp4_sf_bytes", "read_device_status",
+    "set_wait_timeout_ns", "Prepared", "prepare_gemm", "prepare_quantize", "prepare_grouped",
+    "SF_LINEAR", "SF_SWIZZLED", "PACK_ROW", "PACK_COL", "PACK_BOTH", "EXPORTS",
+]
+
+_PACK = {"row": PACK_ROW, "col": PACK_COL, "both": PACK_BOTH}
+_SF = {"linear": SF_LINEAR, "swizzled": SF_SWIZZLED}
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    # zero-filled: the first 4 bytes are the device status word
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def nvfp4_codes_bytes(rows: int, cols: int) -> int:
+    return int(load().nvfp4_codes_bytes(rows, cols))
+
+
+def nvfp4_sf_bytes(rows: int, cols: int, sf_layout: str = "swizzled") -> int:
+    return int(load().nvfp4_sf_bytes(rows, cols, _SF[sf_layout]))
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    return int(load().nvfp4_set_wait_timeout_ns(int(ns)))
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().nvfp4_read_device_status(_p(workspace), _stream(stream)))
+
+
+class Prepared:
+    """A filled argument struct and its C function: call() re-launches it.
+
+    Holds references to every tensor the struct points to."""
+
+    def __init__(self, fn, args, keep, where):
+        self.fn, self.args, self.keep, self.where = fn, args, keep, where
+        self._ref = C.byref(args)
+
+    def __call__(self, stream=None):
+        check(self.fn(self._ref, _stream(stream)), self.where)
+
+
+# ----------------------------------------------------------------- quantize --
+
+def prepare_quantize(src: torch.Tensor, pack: str = "row", sf_layout: str = "swizzled",
+                     global_scale: torch.Tensor | None = None) -> tuple[Prepared, dict]:
+    lib = load()
+    if src.dtype != torch.bfloat16 or not src.is_cuda:
+        raise TypeError("src must be a CUDA bf16 tensor")
+    batched = src.dim() == 3
+    s3 = src if batched else src.unsqueeze(0)
+    B, R, Cc = s3.shape
+    if s3.stride(2) != 1:
+        raise ValueError("src must have unit stride along columns")
+    dev = src.device
+    pk, sl = _PACK[pack], _SF[sf_layout]
+    out = {}
+    if pk & PACK_ROW:
+        out["codes_row"] = torch.empty((B, R, Cc // 2), dtype=torch.uint8, device=dev)
+        out["sf_row"] = torch.empty((B, lib.nvfp4_sf_bytes(R, Cc, sl)), dtype=torch.uint8, device=dev)
+    if pk & PACK_COL:
+        out["codes_col"] = torch.empty((B, Cc, R // 2), dtype=torch.uint8, device=dev)
+        out["sf_col"] = torch.empty((B, lib.nvfp4_sf_bytes(Cc, R, sl)), dtype=torch.uint8, device=dev)
+    gout = torch.empty(B, dtype=torch.float32, device=dev)
+    out["global_scale"] = global_scale if global_scale is not None else gout
+    a = QuantArgs(src=s3.data_ptr(), batch=B, rows=R, cols=Cc, ld=s3.stride(1),
+                  batch_stride=s3.stride(0), pack=pk, sf_layout=sl,
+                  global_scale_in=None if global_scale is None else global_scale.data_ptr(),
+                  global_scale_out=gout.data_ptr())
+    for k in ("codes_row", "sf_row", "codes_col", "sf_col"):
+        if k in out:
+            setattr(a, k, out[k].data_ptr())
+    ws = _ws(lib.nvfp4_quantize_workspace_bytes(C.byref(a)), dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    out["workspace"] = ws
+    if not batched:
+        out = {k: (v[0] if k in ("codes_row", "sf_row", "codes_col", "sf_col") else v)
+               for k, v in out.items()}
+    return Prepared(lib.nvfp4_quantize, a, (src, s3, out, gout, global_scale), "nvfp4_quantize"), out
+
+
+def nvfp4_quantize(src, pack="row", sf_layout="swizzled", global_scale=None, stream=None) -> dict:
+    """bf16 [rows, cols] (or [batch, rows, cols]) -> NVFP4 packings.
+
+    Returns codes_row/sf_row and/or codes_col/sf_col (uint8) and global_scale
+    (fp32 [batch])."""
+    call, out = prepare_quantize(src, pack, sf_layout, global_scale)
+    call(stream)
+    return out
+
+
+# --------------------------------------------------------------------- GEMM --
+
+def prepare_gemm(b_codes, b_sf, b_global_scale, N: int, K: int, *, a_codes=None, a_sf=None,
+                 a_global_scale=None, a_bf16=None, M: int | None = None, out_dtype=torch.bfloat16,
+                 lora=None, out=None) -> tuple[Prepared, torch.Tensor]:
+    """See nvfp4_gemm; returns (Prepared call, output tensor)."""
+    lib = load()
+    if M is None:
+        M = a_bf16.shape[0] if a_bf16 is not None else a_codes.shape[0]
+    dev = b_codes.device
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    a = GemmArgs(M=M, N=N, K=K, b_codes=b_codes.data_ptr(), b_sf=b_sf.data_ptr(),
+                 b_global_scale=b_global_scale.data_ptr(),
+                 out_dtype=OUT_FP32 if out.dtype == torch.float32 else OUT_BF16,
+                 d=out.data_ptr(), ldd=out.stride(0))
+    keep = [b_codes, b_sf, b_global_scale, out, a_codes, a_sf, a_global_scale, a_bf16]
+    if a_bf16 is not None:
+        a.a_bf16, a.lda = a_bf16.data_ptr(), a_bf16.stride(0)
+        if a_global_scale is not None:
+            a.a_global_scale = a_global_scale.data_ptr()
+    else:
+        a.a_codes, a.a_sf = a_codes.data_ptr(), a_sf.data_ptr()
+        a.a_global_scale = a_global_scale.data_ptr()
+    if lora is not None:
+        x = lora.get("x", a_bf16)
+        a.lora_x = lora["x"].data_ptr() if "x" in lora else None
+        if a_bf16 is None or "x" in lora:
+            a.lda = x.stride(0)
+        a.lora_a, a.lora_b = lora["a"].data_ptr(), lora["b"].data_ptr()
+        a.rank, a.alpha = lora["a"].shape[0], float(lora["alpha"])
+        keep += [x, lora["a"], lora["b"]]
+    ws = _ws(lib.nvfp4_gemm_workspace_bytes(C.byref(a)), dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    keep.append(ws)
+    call = Prepared(lib.nvfp4_gemm, a, keep, "nvfp4_gemm")
+    call.workspace = ws
+    return call, out
+
+
+def nvfp4_gemm(b_codes, b_sf, b_global_scale, N, K, *, a_codes=None, a_sf=None,
+               a_global_scale=None, a_bf16=None, out_dtype=torch.bfloat16, lora=None,
+               out=None, stream=None) -> torch.Tensor:
+    """D = W4A4(A, B) [+ (alpha/r) (X A_l^T) B_l^T].
+
+    A: packed (a_codes [M,K/2], a_sf swizzled, a_global_scale [1]) or bf16
+    a_bf16 [M,K] quantized in the call (a_global_scale = static scale, or None
+    = dynamic).  B: b_codes [N,K/2], b_sf swizzled, b_global_scale [1].
+    lora: dict(a=[r,K] bf16, b=[N,r] bf16, alpha=float[, x=[M,K] bf16])."""
+    call, out = prepare_gemm(b_codes, b_sf, b_global_scale, N, K, a_codes=a_codes, a_sf=a_sf,
+                             a_global_scale=a_global_scale, a_bf16=a_bf16,
+                             out_dtype=out_dtype, lora=lora, out=out)
+    call(stream)
+    return out
+
+
+# ------------------------------------------------------------------ grouped --
+
+def prepare_grouped(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N: int, K: int,
+                    num_experts: int, x_global_scale=None, lora=None):
+    lib = load()
+    dev = x_bf16.device
+    T, topk = expert_ids.shape
+    P = T * topk
+    d = torch.empty((P, N), dtype=torch.bfloat16, device=dev)
+    perm = torch.empty(P, dtype=torch.int32, device=dev)
+    offs = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    a = GroupedArgs(num_tokens=T, top_k=topk, num_experts=num_experts, N=N, K=K,
+                    expert_ids=expert_ids.data_ptr(), x_bf16=x_bf16.data_ptr(),
+                    x_global_scale=None if x_global_scale is None else x_global_scale.data_ptr(),
+                    w_codes=w_codes.data_ptr(), w_sf=w_sf.data_ptr(),
+                    w_global_scale=w_global_scale.data_ptr(), d=d.data_ptr(),
+                    perm_out=perm.data_ptr(), expert_offsets_out=offs.data_ptr())
+    keep = [expert_ids, x_bf16, w_codes, w_sf, w_global_scale, x_global_scale, d, perm, offs]
+    if lora is not None:
+        a.lora_a, a.lora_b = lora["a"].data_ptr(), lora["b"].data_ptr()
+        a.rank, a.alpha = lora["a"].shape[1], float(lora["alpha"])
+        keep += [lora["a"], lora["b"]]
+    ws = _ws(lib.nvfp4_grouped_workspace_bytes(C.byref(a)), dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    keep.append(ws)
+    call = Prepared(lib.nvfp4_grouped_gemm, a, keep, "nvfp4_grouped_gemm")
+    call.workspace = ws
+    return call, (d, perm, offs)
+
+
+def nvfp4_grouped_gemm(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N, K, num_experts,
+                       x_global_scale=None, lora=None, stream=None):
+    """Routed-expert W4A4 GEMM.  Returns (d [T*k, N] grouped by expert,
+    perm [T*k] grouped row -> pair index, offsets [E+1])."""
+    call, res = prepare_grouped(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N, K,
+                                num_experts, x_global_scale, lora)
+    call(stream)
+    return res
+
+
+# --------------------------------------------------------------------- LoRA --
+
+def nvfp4_lora_epilogue(y, x, lora_a, lora_b, alpha: float, want_norm: bool = False,
+                        stream=None):
+    """In place: y += (alpha/r) (x lora_a^T) lora_b^T.  Returns the sum of the
+    squared delta (fp32 tensor [1]) when want_norm, else None."""
+    lib = load()
+    M, K = x.shape
+    N = y.shape[1]
+    norm = torch.zeros(1, dtype=torch.float32, device=y.device) if want_norm else None
+    a = LoraArgs(M=M, N=N, K=K, x=x.data_ptr(), ldx=x.stride(0), lora_a=lora_a.data_ptr(),
+                 lora_b=lora_b.data_ptr(), rank=lora_a.shape[0], alpha=float(alpha),
+                 y_dtype=OUT_FP32 if y.dtype == torch.float32 else OUT_BF16, y=y.data_ptr(),
+                 ldy=y.stride(0), delta_sq_norm_out=None if norm is None else norm.data_ptr())
+    ws = _ws(lib.nvfp4_lora_workspace_bytes(C.byref(a)), y.device)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    check(lib.nvfp4_lora_epilogue(C.byref(a), _stream(stream)), "nvfp4_lora_epilogue")
+    return norm

@@ -1,0 +1,732 @@
+// api.cu -- the extern "C" entry points of libnvfp4 (declared in include/nvfp4.h).
+//
+// Host side only: argument validation, workspace carving, tensor-map encoding
+// and kernel sequencing on the caller's stream.  Nothing here allocates device
+// memory; scratch lives in the caller's workspace, whose first 256 bytes hold
+// the device status word written by bounded in-kernel waits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "internal.h"
+
+using namespace nvfp4;
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+  bool ok = false;
+};
+
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+nvfp4_status device_info(DevInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo &d = g_dev[dev];
+  if (!d.ok) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    d.ok = true;
+  }
+  *out = d;
+  if (d.major != 10 || d.minor != 3) return NVFP4_ERR_UNSUPPORTED_DEVICE;
+  return NVFP4_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t pad_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Bump allocator over the caller's workspace; offsets are 256-byte aligned.
+struct Carve {
+  uint8_t *base;
+  size_t off = 256;   // [0, 256): status word
+  explicit Carve(void *b) : base(static_cast<uint8_t *>(b)) {}
+  template <class T>
+  T *take(size_t bytes) {
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += (bytes + 255) / 256 * 256;
+    return p;
+  }
+};
+
+size_t sf_swizzled_bytes(int64_t rows, int64_t cols) {
+  return (size_t)pad_up(rows, 128) * (size_t)pad_up(cols / 16, 4);
+}
+
+nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+// Records an optional caller-owned cudaEvent_t on the stream (profiling hook).
+cudaError_t mark(void *ev, cudaStream_t st) {
+  return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), st) : cudaSuccess;
+}
+
+// ---------------------------------------------------------------- quantize --
+struct QuantPlan {
+  size_t ws = 0;
+  uint32_t *amax = nullptr;
+  int nparts = 0;
+};
+
+nvfp4_status plan_quantize(const nvfp4_quant_args *a, QuantPlan *pl) {
+  Carve c(a->workspace);
+  if (!a->global_scale_in) {
+    pl->nparts = amax_parts_for(a->rows);
+    pl->amax = c.take<uint32_t>((size_t)a->batch * pl->nparts * 4);
+  }
+  pl->ws = c.off;
+  return NVFP4_OK;
+}
+
+nvfp4_status validate_quantize(const nvfp4_quant_args *a) {
+  if (!a || !a->src) return NVFP4_ERR_INVALID_ARG;
+  if (a->batch < 1 || a->rows < 1 || a->cols < 1) return NVFP4_ERR_INVALID_ARG;
+  if (a->pack < NVFP4_PACK_ROW || a->pack > NVFP4_PACK_BOTH) return NVFP4_ERR_INVALID_ARG;
+  if (a->sf_layout != NVFP4_SF_LINEAR && a->sf_layout != NVFP4_SF_SWIZZLED) return NVFP4_ERR_INVALID_ARG;
+  const bool row = a->pack & NVFP4_PACK_ROW, col = a->pack & NVFP4_PACK_COL;
+  if (row && (!a->codes_row || !a->sf_row)) return NVFP4_ERR_INVALID_ARG;
+  if (col && (!a->codes_col || !a->sf_col)) return NVFP4_ERR_INVALID_ARG;
+  if (!a->global_scale_in && !a->global_scale_out) return NVFP4_ERR_INVALID_ARG;
+  if (a->ld < a->cols || (a->batch > 1 && a->batch_stride < a->rows * a->ld)) return NVFP4_ERR_INVALID_ARG;
+  if (a->cols % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (col && a->rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->rows > (1ll << 31) || a->cols > (1ll << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a->src, 16) || a->ld % 8 != 0 || (a->batch > 1 && a->batch_stride % 8 != 0))
+    return NVFP4_ERR_ALIGNMENT;
+  for (const void *p : {(const void *)a->codes_row, (const void *)a->sf_row, (const void *)a->codes_col,
+                        (const void *)a->sf_col})
+    if (p && !aligned(p, 16)) return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int sms, cudaStream_t st) {
+  QuantParams p{};
+  p.src = static_cast<const __nv_bfloat16 *>(a->src);
+  p.rows = a->rows;
+  p.cols = a->cols;
+  p.ld = a->ld;
+  p.bstride = a->batch > 1 ? a->batch_stride : 0;
+  p.batch = a->batch;
+  p.g_in = a->global_scale_in;
+  p.g_out = a->global_scale_out;
+  p.amax_part = pl.amax;
+  p.nparts = pl.nparts;
+  p.sf_swizzled = a->sf_layout == NVFP4_SF_SWIZZLED;
+  const bool row = a->pack & NVFP4_PACK_ROW, col = a->pack & NVFP4_PACK_COL;
+  if (row) {
+    p.codes_row = a->codes_row;
+    p.sf_row = a->sf_row;
+    p.codes_row_bstride = (int64_t)nvfp4_codes_bytes(a->rows, a->cols);
+    p.sf_row_bstride = (int64_t)nvfp4_sf_bytes(a->rows, a->cols, a->sf_layout);
+  }
+  if (col) {
+    p.codes_col = a->codes_col;
+    p.sf_col = a->sf_col;
+    p.codes_col_bstride = (int64_t)nvfp4_codes_bytes(a->cols, a->rows);
+    p.sf_col_bstride = (int64_t)nvfp4_sf_bytes(a->cols, a->rows, a->sf_layout);
+  }
+  p.dst_rows = a->rows;
+  if (!a->global_scale_in) {
+    cudaError_t e = launch_amax(p, st);
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
+  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaError_t e = col ? launch_quant_tiles(p, sms, st) : launch_quant_rows(p, sms, st);
+  if (e == cudaSuccess) e = mark(a->prof_end, st);
+  return cuda_status(e);
+}
+
+// -------------------------------------------------------------------- GEMM --
+bool map2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+           uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return make_map_2d(m, dt, base, inner, rows, pitch_bytes, box_inner, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int pick_bn(int64_t M, int64_t N, int sms) {
+  if (N <= 128) return 128;
+  const int64_t t256 = ceil_div(M, 128) * ceil_div(N, 256);
+  if (t256 < sms && N % 128 == 0) return 128;
+  return 256;
+}
+
+struct GemmPlan {
+  size_t ws = 0;
+  bool gemv = false;
+  float *gemv_partial = nullptr;
+  // in-call quantization of A
+  uint8_t *aq_codes = nullptr, *aq_sf = nullptr;
+  float *aq_g = nullptr;
+  uint32_t *aq_amax = nullptr;
+  int aq_nparts = 0;
+  __nv_bfloat16 *t = nullptr;   // T' [M][rank]
+};
+
+bool use_gemv(const nvfp4_gemm_args *a) {
+  return a->a_bf16 && a->a_global_scale && a->M <= 4 && a->K % 64 == 0 && !a->lora_a &&
+         aligned(a->b_codes, 32) && gemv_smem_bytes(a->M, a->K) <= 200 * 1024;
+}
+
+nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
+  Carve c(a->workspace);
+  if (use_gemv(a)) {
+    pl->gemv = true;
+    const size_t pb = gemv_workspace_bytes(a->M, a->N, a->K);
+    if (pb) pl->gemv_partial = c.take<float>(pb);
+    pl->ws = c.off;
+    return NVFP4_OK;
+  }
+  if (a->a_bf16) {
+    pl->aq_codes = c.take<uint8_t>((size_t)a->M * a->K / 2);
+    pl->aq_sf = c.take<uint8_t>(sf_swizzled_bytes(a->M, a->K));
+    pl->aq_g = c.take<float>(4);
+    if (!a->a_global_scale) {
+      pl->aq_nparts = amax_parts_for(a->M);
+      pl->aq_amax = c.take<uint32_t>((size_t)pl->aq_nparts * 4);
+    }
+  }
+  if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)a->M * a->rank * 2);
+  pl->ws = c.off;
+  return NVFP4_OK;
+}
+
+nvfp4_status validate_gemm(const nvfp4_gemm_args *a) {
+  if (!a || !a->b_codes || !a->b_sf || !a->b_global_scale || !a->d) return NVFP4_ERR_INVALID_ARG;
+  if (a->M < 1 || a->N < 1 || a->K < 1) return NVFP4_ERR_INVALID_ARG;
+  if (a->out_dtype != NVFP4_OUT_BF16 && a->out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+  if (a->ldd < a->N) return NVFP4_ERR_INVALID_ARG;
+  if (!a->a_bf16 && (!a->a_codes || !a->a_sf || !a->a_global_scale)) return NVFP4_ERR_INVALID_ARG;
+  if ((a->a_bf16 || a->lora_x) && a->lda < a->K) return NVFP4_ERR_INVALID_ARG;
+  if (a->K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->M > (1ll << 31) - 256 || a->N > (1ll << 31) - 256 || a->K > (1ll << 24))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->lora_a || a->lora_b) {
+    if (!a->lora_a || !a->lora_b || (!a->lora_x && !a->a_bf16)) return NVFP4_ERR_INVALID_ARG;
+    if (a->rank < 32 || a->rank > 256 || a->rank % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(a->lora_a, 16) || !aligned(a->lora_b, 16)) return NVFP4_ERR_ALIGNMENT;
+    if (a->lora_x && !aligned(a->lora_x, 16)) return NVFP4_ERR_ALIGNMENT;
+  }
+  const int64_t dalign = a->out_dtype == NVFP4_OUT_BF16 ? 8 : 4;
+  if (!aligned(a->d, 16) || a->ldd % dalign != 0) return NVFP4_ERR_ALIGNMENT;
+  if (!aligned(a->b_codes, 16) || !aligned(a->b_sf, 16)) return NVFP4_ERR_ALIGNMENT;
+  if (a->a_codes && (!aligned(a->a_codes, 16) || !aligned(a->a_sf, 16))) return NVFP4_ERR_ALIGNMENT;
+  if ((a->a_bf16 || a->lora_x) && a->lda % 8 != 0) return NVFP4_ERR_ALIGNMENT;
+  if (a->a_bf16 && !aligned(a->a_bf16, 16)) return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status check_workspace(void *ws, size_t have, size_t need) {
+  if (!ws || have < need || !aligned(ws, 256)) return NVFP4_ERR_WORKSPACE;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cudaStream_t st) {
+  int *status = static_cast<int *>(a->workspace);
+  const uint64_t tmo = g_timeout_ns.load();
+  if (pl.gemv) {
+    GemvParams g{};
+    g.M = a->M;
+    g.N = a->N;
+    g.K = a->K;
+    g.x = static_cast<const __nv_bfloat16 *>(a->a_bf16);
+    g.ldx = a->lda;
+    g.g_x = a->a_global_scale;
+    g.w_codes = a->b_codes;
+    g.w_sf = a->b_sf;
+    g.w_sf_katoms = pad_up(a->K / 16, 4) / 4;
+    g.g_w = a->b_global_scale;
+    g.d = a->d;
+    g.ldd = a->ldd;
+    g.out_fp32 = a->out_dtype == NVFP4_OUT_FP32;
+    if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    cudaError_t e = launch_gemv_ws(g, sms, st, pl.gemv_partial);
+    if (e == cudaSuccess) e = mark(a->prof_end, st);
+    return cuda_status(e);
+  }
+  const uint8_t *a_codes = a->a_codes, *a_sf = a->a_sf;
+  const float *g_a = a->a_global_scale;
+  const void *xb = a->lora_x ? a->lora_x : a->a_bf16;
+  if (a->a_bf16) {
+    QuantParams q{};
+    q.src = static_cast<const __nv_bfloat16 *>(a->a_bf16);
+    q.rows = a->M;
+    q.cols = a->K;
+    q.ld = a->lda;
+    q.batch = 1;
+    q.g_in = a->a_global_scale;
+    q.g_out = pl.aq_g;
+    q.amax_part = pl.aq_amax;
+    q.nparts = pl.aq_nparts;
+    q.codes_row = pl.aq_codes;
+    q.sf_row = pl.aq_sf;
+    q.sf_swizzled = 1;
+    q.dst_rows = a->M;
+    if (!a->a_global_scale && launch_amax(q, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    a_codes = pl.aq_codes;
+    a_sf = pl.aq_sf;
+    g_a = pl.aq_g;
+  }
+  GemmMaps maps;
+  const int bn = pick_bn(a->M, a->N, sms);
+  if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, a->K / 2, a->M, a->K / 2, 128, 128) ||
+      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, bn))
+    return NVFP4_ERR_CUDA;
+  maps.t = maps.a;
+  maps.lb = maps.b;
+  int lora_steps = 0;
+  if (a->lora_a) {
+    LoraDownMaps lm;
+    if (!map2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a->K, a->M, a->lda * 2, 64, 128) ||
+        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->rank, a->K * 2, 64, a->rank) ||
+        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, a->M, a->rank * 2, 64, 128) ||
+        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, bn))
+      return NVFP4_ERR_CUDA;
+    LoraDownParams lp{};
+    lp.M = a->M;
+    lp.K = a->K;
+    lp.rank = a->rank;
+    lp.num_k64 = (int)ceil_div(a->K, 64);
+    lp.lora_scale = a->alpha / (float)a->rank;
+    lp.g_a = g_a;
+    lp.g_b = a->b_global_scale;
+    lp.t_out = pl.t;
+    lp.tiles_m = (int)ceil_div(a->M, 128);
+    lp.status = status;
+    lp.timeout_ns = tmo;
+    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+  }
+  GemmParams p{};
+  p.M = a->M;
+  p.N = a->N;
+  p.K = a->K;
+  p.num_kt = (int)ceil_div(a->K, 256);
+  p.nk64 = (int)ceil_div(a->K, 64);
+  p.a_sf = a_sf;
+  p.b_sf = a->b_sf;
+  p.a_sf_katoms = pad_up(a->K / 16, 4) / 4;
+  p.b_sf_katoms = p.a_sf_katoms;
+  p.b_sf_row_chunks = ceil_div(a->N, 128);
+  p.g_a = g_a;
+  p.g_b = a->b_global_scale;
+  p.d = a->d;
+  p.ldd = a->ldd;
+  p.out_fp32 = a->out_dtype == NVFP4_OUT_FP32;
+  p.lora_steps = lora_steps;
+  p.tiles_m = (int)ceil_div(a->M, 128);
+  p.tiles_n = (int)ceil_div(a->N, bn);
+  p.status = status;
+  p.timeout_ns = tmo;
+  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  if (e == cudaSuccess) e = mark(a->prof_end, st);
+  return cuda_status(e);
+}
+
+// ------------------------------------------------------------------ grouped --
+struct GroupedPlan {
+  size_t ws = 0;
+  int nchunks = 0;
+  int64_t prow_max = 0;
+  int32_t *hist = nullptr, *counts = nullptr, *offsets = nullptr, *poffsets = nullptr;
+  int32_t *row_map = nullptr, *nmt = nullptr;
+  GroupTile *gtiles = nullptr;
+  uint32_t *amax = nullptr;
+  int nparts = 0;
+  float *g_x = nullptr;
+  uint8_t *xq = nullptr, *xsf = nullptr;
+  __nv_bfloat16 *t = nullptr;
+};
+
+nvfp4_status plan_grouped(const nvfp4_grouped_args *a, GroupedPlan *pl) {
+  Carve c(a->workspace);
+  const int64_t P = a->num_tokens * a->top_k;
+  pl->nchunks = (int)ceil_div(P, 1024);
+  pl->prow_max = pad_up(P + a->num_experts * 127, 128);
+  pl->hist = c.take<int32_t>((size_t)pl->nchunks * a->num_experts * 4);
+  pl->counts = c.take<int32_t>((size_t)a->num_experts * 4);
+  pl->offsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  pl->poffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  pl->row_map = c.take<int32_t>((size_t)pl->prow_max * 4);
+  pl->gtiles = c.take<GroupTile>((size_t)(pl->prow_max / 128) * sizeof(GroupTile));
+  pl->nmt = c.take<int32_t>(4);
+  if (!a->x_global_scale) {
+    pl->nparts = amax_parts_for(a->num_tokens);
+    pl->amax = c.take<uint32_t>((size_t)pl->nparts * 4);
+  }
+  pl->g_x = c.take<float>(4);
+  pl->xq = c.take<uint8_t>((size_t)pl->prow_max * a->K / 2);
+  pl->xsf = c.take<uint8_t>(sf_swizzled_bytes(pl->prow_max, a->K));
+  if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)pl->prow_max * a->rank * 2);
+  pl->ws = c.off;
+  return NVFP4_OK;
+}
+
+nvfp4_status validate_grouped(const nvfp4_grouped_args *a) {
+  if (!a || !a->expert_ids || !a->x_bf16 || !a->w_codes || !a->w_sf || !a->w_global_scale || !a->d ||
+      !a->perm_out)
+    return NVFP4_ERR_INVALID_ARG;
+  if (a->num_tokens < 1 || a->top_k < 1 || a->num_experts < 1 || a->N < 1 || a->K < 1)
+    return NVFP4_ERR_INVALID_ARG;
+  if (a->num_experts > 1024 || a->top_k > a->num_experts) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->N % 256 != 0 || a->K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->num_tokens * a->top_k > (1ll << 30) || a->num_experts * a->N > (1ll << 31) - 256)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->lora_a || a->lora_b) {
+    if (!a->lora_a || !a->lora_b) return NVFP4_ERR_INVALID_ARG;
+    if (a->rank < 32 || a->rank > 256 || a->rank % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(a->lora_a, 16) || !aligned(a->lora_b, 16)) return NVFP4_ERR_ALIGNMENT;
+  }
+  if (!aligned(a->x_bf16, 16) || !aligned(a->w_codes, 16) || !aligned(a->w_sf, 16) || !aligned(a->d, 16))
+    return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int sms, cudaStream_t st) {
+  int *status = static_cast<int *>(a->workspace);
+  const uint64_t tmo = g_timeout_ns.load();
+  const int64_t P = a->num_tokens * a->top_k;
+  RouteParams r{};
+  r.expert_ids = a->expert_ids;
+  r.pairs = P;
+  r.top_k = (int)a->top_k;
+  r.num_experts = (int)a->num_experts;
+  r.chunk = 1024;
+  r.nchunks = pl.nchunks;
+  r.hist = pl.hist;
+  r.counts = pl.counts;
+  r.offsets = pl.offsets;
+  r.poffsets = pl.poffsets;
+  r.perm = a->perm_out;
+  r.row_map = pl.row_map;
+  r.padded_rows_max = pl.prow_max;
+  r.gtiles = pl.gtiles;
+  r.gnum_mtiles = pl.nmt;
+  r.offsets_out = a->expert_offsets_out;
+  if (launch_route(r, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+
+  QuantParams q{};
+  q.src = static_cast<const __nv_bfloat16 *>(a->x_bf16);
+  q.rows = a->num_tokens;
+  q.cols = a->K;
+  q.ld = a->K;
+  q.batch = 1;
+  q.g_in = a->x_global_scale;
+  q.g_out = pl.g_x;
+  q.amax_part = pl.amax;
+  q.nparts = pl.nparts;
+  q.codes_row = pl.xq;
+  q.sf_row = pl.xsf;
+  q.sf_swizzled = 1;
+  q.row_map = pl.row_map;
+  q.dst_rows = pl.prow_max;
+  if (!a->x_global_scale && launch_amax(q, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  const float *g_x = a->x_global_scale ? a->x_global_scale : pl.g_x;
+
+  const int bn = 256;
+  GemmMaps maps;
+  if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, pl.xq, a->K / 2, pl.prow_max, a->K / 2, 128, 128) ||
+      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->w_codes, a->K / 2, a->num_experts * a->N, a->K / 2,
+             128, bn))
+    return NVFP4_ERR_CUDA;
+  maps.t = maps.a;
+  maps.lb = maps.b;
+  int lora_steps = 0;
+  if (a->lora_a) {
+    LoraDownMaps lm;
+    if (!make_map_2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->x_bf16, a->K, a->num_tokens, a->K * 2, 64,
+                     1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->num_experts * a->rank, a->K * 2, 64,
+               a->rank) ||
+        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, pl.prow_max, a->rank * 2, 64, 128) ||
+        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->num_experts * a->N,
+               a->rank * 2, 64, bn))
+      return NVFP4_ERR_CUDA;
+    LoraDownParams lp{};
+    lp.M = pl.prow_max;
+    lp.K = a->K;
+    lp.rank = a->rank;
+    lp.num_k64 = (int)ceil_div(a->K, 64);
+    lp.lora_scale = a->alpha / (float)a->rank;
+    lp.g_a = g_x;
+    lp.g_b = a->w_global_scale;
+    lp.t_out = pl.t;
+    lp.gtiles = pl.gtiles;
+    lp.gnum_mtiles = pl.nmt;
+    lp.row_map = pl.row_map;
+    lp.status = status;
+    lp.timeout_ns = tmo;
+    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+  }
+  GemmParams p{};
+  p.M = pl.prow_max;
+  p.N = a->N;
+  p.K = a->K;
+  p.num_kt = (int)ceil_div(a->K, 256);
+  p.nk64 = (int)ceil_div(a->K, 64);
+  p.a_sf = pl.xsf;
+  p.b_sf = a->w_sf;
+  p.a_sf_katoms = pad_up(a->K / 16, 4) / 4;
+  p.b_sf_katoms = p.a_sf_katoms;
+  p.b_sf_row_chunks = a->num_experts * a->N / 128;
+  p.g_a = g_x;
+  p.g_b = a->w_global_scale;
+  p.d = a->d;
+  p.ldd = a->N;
+  p.out_fp32 = 0;
+  p.lora_steps = lora_steps;
+  p.tiles_n = (int)(a->N / bn);
+  p.gtiles = pl.gtiles;
+  p.gnum_mtiles = pl.nmt;
+  p.status = status;
+  p.timeout_ns = tmo;
+  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  if (e == cudaSuccess) e = mark(a->prof_end, st);
+  return cuda_status(e);
+}
+
+// --------------------------------------------------------------------- LoRA --
+struct LoraPlan {
+  size_t ws = 0;
+  __nv_bfloat16 *t = nullptr;
+};
+
+nvfp4_status plan_lora(const nvfp4_lora_args *a, LoraPlan *pl) {
+  Carve c(a->workspace);
+  pl->t = c.take<__nv_bfloat16>((size_t)a->M * a->rank * 2);
+  pl->ws = c.off;
+  return NVFP4_OK;
+}
+
+nvfp4_status validate_lora(const nvfp4_lora_args *a) {
+  if (!a || !a->x || !a->lora_a || !a->lora_b || !a->y) return NVFP4_ERR_INVALID_ARG;
+  if (a->M < 1 || a->N < 1 || a->K < 1 || a->ldx < a->K || a->ldy < a->N) return NVFP4_ERR_INVALID_ARG;
+  if (a->y_dtype != NVFP4_OUT_BF16 && a->y_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+  if (a->rank < 32 || a->rank > 256 || a->rank % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->K % 8 != 0 || a->M > (1ll << 31) - 256 || a->N > (1ll << 31) - 256) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a->x, 16) || !aligned(a->lora_a, 16) || !aligned(a->lora_b, 16) || !aligned(a->y, 16) ||
+      a->ldx % 8 != 0)
+    return NVFP4_ERR_ALIGNMENT;
+  if (a->y_dtype == NVFP4_OUT_FP32 ? a->ldy % 4 != 0 : a->ldy % 8 != 0) return NVFP4_ERR_ALIGNMENT;
+  if (a->delta_sq_norm_out && !aligned(a->delta_sq_norm_out, 4)) return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_lora(const nvfp4_lora_args *a, const LoraPlan &pl, int sms, cudaStream_t st) {
+  int *status = static_cast<int *>(a->workspace);
+  const uint64_t tmo = g_timeout_ns.load();
+  const int bn = a->N <= 128 ? 128 : 256;
+  LoraDownMaps lm;
+  GemmMaps maps;
+  if (!map2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->x, a->K, a->M, a->ldx * 2, 64, 128) ||
+      !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->rank, a->K * 2, 64, a->rank) ||
+      !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, a->M, a->rank * 2, 64, 128) ||
+      !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, bn))
+    return NVFP4_ERR_CUDA;
+  maps.a = maps.t;
+  maps.b = maps.lb;
+  LoraDownParams lp{};
+  lp.M = a->M;
+  lp.K = a->K;
+  lp.rank = a->rank;
+  lp.num_k64 = (int)ceil_div(a->K, 64);
+  lp.lora_scale = a->alpha / (float)a->rank;
+  lp.t_out = pl.t;
+  lp.tiles_m = (int)ceil_div(a->M, 128);
+  lp.status = status;
+  lp.timeout_ns = tmo;
+  if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (a->delta_sq_norm_out && cudaMemsetAsync(a->delta_sq_norm_out, 0, 4, st) != cudaSuccess)
+    return NVFP4_ERR_CUDA;
+  GemmParams p{};
+  p.M = a->M;
+  p.N = a->N;
+  p.K = 0;
+  p.num_kt = 0;
+  p.nk64 = 0;
+  p.d = a->y;
+  p.ldd = a->ldy;
+  p.out_fp32 = a->y_dtype == NVFP4_OUT_FP32;
+  p.accumulate_d = 1;
+  p.sqnorm = a->delta_sq_norm_out;
+  p.lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+  p.tiles_m = (int)ceil_div(a->M, 128);
+  p.tiles_n = (int)ceil_div(a->N, bn);
+  p.status = status;
+  p.timeout_ns = tmo;
+  return cuda_status(launch_gemm_fp4(p, maps, bn, sms, st));
+}
+
+}  // namespace
+
+namespace nvfp4 {
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                 uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace nvfp4
+
+// =============================================================== C ABI ==
+extern "C" {
+
+size_t nvfp4_codes_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return (size_t)rows * (size_t)cols / 2;
+}
+
+size_t nvfp4_sf_bytes(int64_t rows, int64_t cols, int32_t sf_layout) {
+  if (rows < 0 || cols < 0) return 0;
+  if (sf_layout == NVFP4_SF_SWIZZLED) return sf_swizzled_bytes(rows, cols);
+  return (size_t)rows * (size_t)(cols / 16);
+}
+
+const char *nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case NVFP4_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case NVFP4_ERR_CUDA: return "CUDA runtime error";
+    case NVFP4_ERR_TIMEOUT: return "an in-kernel wait timed out";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+  }
+  return "unknown status";
+}
+
+int32_t nvfp4_version(void) { return 0x000100; }
+
+uint64_t nvfp4_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
+
+nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream) {
+  if (!workspace) return NVFP4_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (v != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  return static_cast<nvfp4_status>(v);
+}
+
+size_t nvfp4_quantize_workspace_bytes(const nvfp4_quant_args *a) {
+  if (!a) return 0;
+  nvfp4_quant_args c = *a;
+  c.workspace = nullptr;
+  QuantPlan pl;
+  plan_quantize(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_quantize(const nvfp4_quant_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_quantize(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  QuantPlan pl;
+  plan_quantize(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_quantize(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_gemm_workspace_bytes(const nvfp4_gemm_args *a) {
+  if (!a) return 0;
+  nvfp4_gemm_args c = *a;
+  c.workspace = nullptr;
+  GemmPlan pl;
+  plan_gemm(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_gemm_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_gemm(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  GemmPlan pl;
+  plan_gemm(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_gemm(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_grouped_workspace_bytes(const nvfp4_grouped_args *a) {
+  if (!a) return 0;
+  nvfp4_grouped_args c = *a;
+  c.workspace = nullptr;
+  GroupedPlan pl;
+  plan_grouped(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_grouped_gemm(const nvfp4_grouped_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_grouped(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  GroupedPlan pl;
+  plan_grouped(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_grouped(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_lora_workspace_bytes(const nvfp4_lora_args *a) {
+  if (!a) return 0;
+  nvfp4_lora_args c = *a;
+  c.workspace = nullptr;
+  LoraPlan pl;
+  plan_lora(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_lora_epilogue(const nvfp4_lora_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_lora(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  LoraPlan pl;
+  plan_lora(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_lora(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,207 @@
+// gemv.cu -- batch-1 decode: y = (g_x g_w) sum_b sx_b sw_b sum_{k in b} e2m1(x_k) e2m1(w_nk)
+//
+// At batch size 1 the W4A4 projection is a GEMV whose time is the weight
+// bandwidth ("vroomfondel/glm-5.2-reap-504B-v2-W4A4" card, "What this variant
+// changes": o_proj 6144x16384 and q_b_proj 16384x2048 at bs 1), with the
+// activation quantized per call under the static per-tensor input_scale
+// ("How it was produced").  The CUDA-core path streams W once:
+//   * every CTA quantizes the (tiny) X into shared memory with the static
+//     scale, keeping the E2M1 values as exact fp16 pairs and the E4M3 block
+//     scales as fp32;
+//   * a warp reads 32 x 32 contiguous bytes of W codes (64 elements per lane)
+//     and the matching 4-byte group of swizzled scales;
+//   * a 16-element block dot product of E2M1 values is exact in fp16x2 (every
+//     partial sum is a multiple of 1/4 below 512), sx_b*sw_b is exact in fp32
+//     (two 4-bit significands) and so is their product with the block dot;
+//     only the fp32 sum over blocks rounds.
+// Long rows (K > 4096) are split into 2048-element chunks written as fp32
+// partials and summed in order by a second kernel (no atomics, deterministic).
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+constexpr int kGemvThreads = 256;
+constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lanes x 64
+
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+  uint32_t r;
+  const uint16_t b = (uint16_t)(byte & 0xFF);
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "h"(b));
+  return r;
+}
+
+// Same block quantizer as the row packing (kept local: tiny X, static scale).
+__device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g, float t6g,
+                                              uint32_t (&h2)[8], float &sx) {
+  uint32_t w[8];
+  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
+  const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+  const float bamax = __uint_as_float(max(m2 & 0xFFFFu, m2 >> 16) << 16);
+  uint32_t sb = 0;
+  if (g > 0.0f) sb = cvt_e4m3(__fdiv_rn(bamax, t6g));
+  sx = e4m3_to_f32(sb);
+  if (sb == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h2[i] = 0;
+    return;
+  }
+  const float senc = fminf(__frcp_rn(__fmul_rn(sx, g)), 3.402823466e38f);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    h2[i] = e2m1x2_to_h2(cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc)));
+}
+
+template <int MX>
+__global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int64_t K = p.K, nblk = K / 16;
+  uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // [MX][K/2] half2
+  float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // [MX][K/16]
+
+  const float g = *p.g_x;
+  const float t6g = __fmul_rn(6.0f, g);
+  for (int64_t i = threadIdx.x; i < MX * nblk; i += blockDim.x) {
+    const int m = (int)(i / nblk);
+    const int64_t b = i % nblk;
+    uint32_t h2[8];
+    float sx;
+    quant_x_block(p.x + m * p.ldx + b * 16, g, t6g, h2, sx);
+    uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2) + b * 8);
+    dst[0] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+    dst[1] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+    sxs[m * nblk + b] = sx;
+  }
+  __syncthreads();
+
+  const float alpha = __fmul_rn(g, *p.g_w);
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * (kGemvThreads / 32) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (kGemvThreads / 32);
+  const int64_t units = p.N * nchunks;
+  const int64_t row_bytes = K / 2;
+  for (int64_t u = warp; u < units; u += nwarps) {
+    // consecutive warps take consecutive rows of one chunk (shared scale atoms)
+    const int64_t kc = u / p.N, n = u % p.N;
+    float acc[MX];
+#pragma unroll
+    for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
+    const int64_t g4_begin = kc * (kGemvChunk / 64);
+    const int64_t g4_end = (K / 64 < g4_begin + kGemvChunk / 64) ? K / 64 : g4_begin + kGemvChunk / 64;
+    for (int64_t g4 = g4_begin + lane; g4 < g4_end; g4 += 32) {
+      uint32_t c[8];
+      asm volatile(
+          "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3]), "=r"(c[4]), "=r"(c[5]), "=r"(c[6]),
+            "=r"(c[7])
+          : "l"(p.w_codes + n * row_bytes + g4 * 32));
+      const uint32_t sf4 = __ldg(reinterpret_cast<const uint32_t *>(
+          p.w_sf + 512 * ((n >> 7) * p.w_sf_katoms + g4) + 16 * (n & 31) + 4 * ((n & 127) >> 5)));
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const float sw = e4m3_to_f32((sf4 >> (8 * bb)) & 0xFF);
+        uint32_t wh[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          wh[2 * j] = e2m1x2_to_h2(c[2 * bb] >> (8 * j));
+          wh[2 * j + 1] = e2m1x2_to_h2(c[2 * bb + 1] >> (8 * j));
+        }
+        const int64_t b = g4 * 4 + bb;
+#pragma unroll
+        for (int m = 0; m < MX; ++m) {
+          const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2) + b * 8);
+          const uint4 x0 = xp[0], x1 = xp[1];
+          const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          __half2 s = __float2half2_rn(0.0f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            s = __hfma2(*reinterpret_cast<const __half2 *>(&wh[j]),
+                        *reinterpret_cast<const __half2 *>(&xv[j]), s);
+          const float dot = __fadd_rn(__low2float(s), __high2float(s));
+          acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + b]), acc[m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MX; ++m)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+    if (lane < MX) {
+      float v = acc[0];
+#pragma unroll
+      for (int m = 1; m < MX; ++m)
+        if (lane == m) v = acc[m];
+      if (nchunks == 1) {
+        const float y = __fmul_rn(v, alpha);
+        if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n] = y;
+        else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n] = __float2bfloat16_rn(y);
+      } else {
+        partial[(kc * MX + lane) * p.N + n] = v;
+      }
+    }
+  }
+}
+
+__global__ void k_gemv_reduce(const GemvParams p, int nchunks, int mx, const float *partial) {
+  const float alpha = __fmul_rn(*p.g_x, *p.g_w);
+  const int64_t total = (int64_t)mx * p.N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / p.N, n = i % p.N;
+    float s = 0.0f;
+    for (int kc = 0; kc < nchunks; ++kc) s = __fadd_rn(s, partial[(kc * mx + m) * p.N + n]);
+    const float y = __fmul_rn(s, alpha);
+    if (p.out_fp32) reinterpret_cast<float *>(p.d)[m * p.ldd + n] = y;
+    else reinterpret_cast<__nv_bfloat16 *>(p.d)[m * p.ldd + n] = __float2bfloat16_rn(y);
+  }
+}
+
+size_t gemv_smem_bytes(int64_t M, int64_t K) { return (size_t)M * (K / 2) * 4 + (size_t)M * (K / 16) * 4; }
+int gemv_chunks(int64_t K) { return K > 4096 ? (int)((K + kGemvChunk - 1) / kGemvChunk) : 1; }
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const int c = gemv_chunks(K);
+  return c > 1 ? (size_t)c * M * N * sizeof(float) : 0;
+}
+
+template <int MX>
+static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {
+  const size_t smem = gemv_smem_bytes(MX, p.K);
+  static size_t configured = 48 * 1024;
+  if (smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  const int nchunks = gemv_chunks(p.K);
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX>, kGemvThreads, smem);
+  per_sm = std::max(1, std::min(per_sm, 4));
+  const int64_t warps_needed = (p.N * nchunks + 7) / 8;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, warps_needed));
+  k_gemv<MX><<<grid, kGemvThreads, smem, st>>>(p, nchunks, partial);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || nchunks == 1) return e;
+  k_gemv_reduce<<<num_sms, 256, 0, st>>>(p, nchunks, MX, partial);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_ws(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {
+  switch (p.M) {
+    case 1: return launch_mx<1>(p, num_sms, st, partial);
+    case 2: return launch_mx<2>(p, num_sms, st, partial);
+    case 3: return launch_mx<3>(p, num_sms, st, partial);
+    case 4: return launch_mx<4>(p, num_sms, st, partial);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,139 @@
+// internal.h -- host/device structures shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------- quantization --
+struct QuantParams {
+  const __nv_bfloat16 *src;
+  int64_t rows, cols, ld, bstride;    // per matrix; strides in elements
+  int64_t batch;
+  const float *g_in;                  // static scales [batch] or null
+  float *g_out;                       // receives g [batch] (may be null)
+  uint32_t *amax_part;                // [batch][nparts] magnitude bits (dynamic)
+  int nparts;
+  uint8_t *codes_row, *sf_row, *codes_col, *sf_col;
+  int64_t codes_row_bstride, sf_row_bstride, codes_col_bstride, sf_col_bstride;
+  int sf_swizzled;
+  const int32_t *row_map;             // optional gather: dst row -> src row (<0: skip)
+  int64_t dst_rows;                   // rows written by the row packing
+};
+
+int amax_parts_for(int64_t rows);
+cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
+cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
+cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
+
+// --------------------------------------------------------------------- GEMM --
+// One grouped m-tile: expert, first A row (padded grouped order), valid rows,
+// first output row (unpadded grouped order).
+struct GroupTile {
+  int32_t expert, a_row0, valid_rows, out_row0;
+};
+
+struct GemmParams {
+  int64_t M, N, K;            // N = rows of one expert's B (dense: all of B)
+  int num_kt;                 // 256-element K tiles of the FP4 product (0: LoRA only)
+  int nk64;                   // 64-element K steps in total: ceil(K/64)
+  const uint8_t *a_sf, *b_sf;
+  int64_t a_sf_katoms, b_sf_katoms;   // 128x4 atoms per 128-row group
+  int64_t b_sf_row_chunks;            // 128-row chunks present in b_sf (all experts)
+  const float *g_a;           // scalar
+  const float *g_b;           // [experts] (dense: 1)
+  void *d;
+  int64_t ldd;
+  int out_fp32;
+  int accumulate_d;           // D += result (the standalone LoRA path)
+  float *sqnorm;              // optional sum of squares of the written result
+  int lora_steps;             // 64-wide bf16 K steps of the LoRA up-projection
+  int tiles_m, tiles_n;
+  const GroupTile *gtiles;    // grouped mode: m-tile table
+  const int32_t *gnum_mtiles; // grouped mode: number of m-tiles (device)
+  int *status;
+  uint64_t timeout_ns;
+};
+
+struct GemmMaps {
+  CUtensorMap a, b, t, lb;
+};
+
+cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, int num_sms,
+                            cudaStream_t st);
+
+// LoRA down-projection: T' = bf16(scale_row * X A^T), X gathered for grouped.
+struct LoraDownParams {
+  int64_t M, K;
+  int rank;
+  int num_k64;                // ceil(K/64)
+  float lora_scale;           // alpha / rank
+  const float *g_a;           // null: T' = bf16(scale * T); else divide by g_a * g_b[e]
+  const float *g_b;
+  __nv_bfloat16 *t_out;       // [rows][rank]
+  int tiles_m;
+  const GroupTile *gtiles;
+  const int32_t *gnum_mtiles;
+  const int32_t *row_map;     // grouped: padded row -> token (gather)
+  int *status;
+  uint64_t timeout_ns;
+};
+
+struct LoraDownMaps {
+  CUtensorMap x, a;
+};
+
+cudaError_t launch_lora_down(const LoraDownParams &p, const LoraDownMaps &maps, int num_sms,
+                             cudaStream_t st);
+
+// -------------------------------------------------------------------- GEMV --
+struct GemvParams {
+  int64_t M, N, K;
+  const __nv_bfloat16 *x;
+  int64_t ldx;
+  const float *g_x;           // static input scale
+  const uint8_t *w_codes, *w_sf;
+  int64_t w_sf_katoms;
+  const float *g_w;
+  void *d;
+  int64_t ldd;
+  int out_fp32;
+};
+// partial: fp32 [chunks][M][N] scratch when gemv_workspace_bytes() > 0.
+cudaError_t launch_gemv_ws(const GemvParams &p, int num_sms, cudaStream_t st, float *partial);
+size_t gemv_smem_bytes(int64_t M, int64_t K);
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+// ------------------------------------------------------------------ routing --
+struct RouteParams {
+  const int32_t *expert_ids;
+  int64_t pairs;              // tokens * top_k
+  int top_k;
+  int num_experts;
+  int chunk;                  // pairs per chunk
+  int nchunks;
+  int32_t *hist;              // [nchunks][E] -> chunk bases after the scan
+  int32_t *counts;            // [E]
+  int32_t *offsets;           // [E+1]
+  int32_t *poffsets;          // [E+1] padded (multiples of 128)
+  int32_t *perm;              // [pairs]
+  int32_t *row_map;           // [padded_rows_max]
+  int64_t padded_rows_max;
+  GroupTile *gtiles;          // [max m-tiles]
+  int32_t *gnum_mtiles;
+  int32_t *offsets_out;       // optional copy of offsets for the caller
+};
+cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
+
+// ------------------------------------------------------------- tensor maps --
+// Encodes a 2-D row-major tensor map; returns false on failure.
+bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                 uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner,
+                 uint32_t box_rows, CUtensorMapSwizzle sw);
+
+}  // namespace nvfp4

@@ -1,0 +1,385 @@
+// quantize.cu -- bf16 -> NVFP4 (E2M1 codes, E4M3 per-16 scales, fp32 global).
+//
+// Operation order (one IEEE fp32 rounding per step, no contraction):
+//   g = amax / 2688            (weight_scale_2 = amax/(6*448): the
+//                               "vroomfondel/glm-5.2-reap-504B-v2-W4A4" card,
+//                               "How it was produced")
+//   q = bamax / (6*g);  sb = E4M3_rn_satfinite(q)
+//   s_dec = sb * g;  s_enc = min(1/s_dec, FLT_MAX);  v = x * s_enc
+//   code = sign(x) | E2M1_rn_satfinite(|v|);  sb == 0 => all codes +0
+// Blocks are 16 consecutive elements along the contraction axis ("GLM-5.2-
+// NVFP4" card, "Quantization recipe"); the column packing quantizes the
+// transpose from the same bf16 values, with the same g ("Getting GLM-5.2
+// NVFP4 Post-Training off the ground", "Why can't we just transpose the one
+// copy?").  All kernels here are HBM-bound: one pass over bf16 input, packed
+// codes and scales written once.
+#include <cfloat>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------------ helpers --
+
+__device__ __forceinline__ int64_t sf_swz_offset(int64_t r, int64_t c, int64_t sf_cols_pad) {
+  return 512 * ((r >> 7) * (sf_cols_pad >> 2) + (c >> 2)) + 16 * (r & 31) +
+         4 * ((r & 127) >> 5) + (c & 3);
+}
+
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Max over the block; every thread must call it.  `scratch` holds >= 32 words.
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t *scratch) {
+  v = warp_max_u32(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) scratch[w] = v;
+  __syncthreads();
+  const int nw = (blockDim.x + 31) >> 5;
+  v = (l < nw) ? scratch[l] : 0u;
+  return warp_max_u32(v);
+}
+
+// Global scale of matrix b: static, or amax/2688 from the per-part maxima of
+// |bf16| bit patterns (for non-NaN bf16, the order of |x| is the order of its
+// magnitude bits, so the integer max is the exact amax).
+__device__ __forceinline__ float resolve_global_scale(const QuantParams &p, int b,
+                                                      uint32_t *scratch) {
+  if (p.g_in) return p.g_in[b];
+  uint32_t m = 0;
+  for (int i = threadIdx.x; i < p.nparts; i += blockDim.x)
+    m = max(m, p.amax_part[(int64_t)b * p.nparts + i]);
+  m = block_max_u32(m, scratch);
+  const float amax = __uint_as_float(m << 16);
+  return __fdiv_rn(amax, 2688.0f);
+}
+
+struct BlockScale {
+  float t6g, g;
+  bool gzero;
+};
+
+__device__ __forceinline__ BlockScale make_block_scale(float g) {
+  BlockScale s;
+  s.g = g;
+  s.t6g = __fmul_rn(6.0f, g);
+  s.gzero = !(g > 0.0f);
+  return s;
+}
+
+// Quantize 16 bf16 values held as 8 words (element 2i in the low half of w[i]).
+// Returns the 8 code bytes (element 2i in the low nibble of byte i) and the
+// E4M3 scale byte.
+__device__ __forceinline__ uint64_t quant16(const uint32_t (&w)[8], const BlockScale &s,
+                                            uint32_t &sf_out) {
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+  const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
+  const float bamax = __uint_as_float(mb << 16);
+  uint32_t sb = 0;
+  if (!s.gzero) sb = cvt_e4m3(__fdiv_rn(bamax, s.t6g));
+  sf_out = sb;
+  if (sb == 0) return 0ull;
+  const float sdec = __fmul_rn(e4m3_to_f32(sb), s.g);
+  const float senc = fminf(__frcp_rn(sdec), FLT_MAX);
+  uint32_t lo = 0, hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    lo |= cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc)) << (8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    hi |= cvt_e2m1x2(__fmul_rn(bf16lo(w[4 + i]), senc), __fmul_rn(bf16hi(w[4 + i]), senc))
+          << (8 * i);
+  return (uint64_t)lo | ((uint64_t)hi << 32);
+}
+
+template <bool kV8>
+__device__ __forceinline__ void load16(const __nv_bfloat16 *src, uint32_t (&w)[8]) {
+  if (kV8) {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7])
+        : "l"(src));
+  } else {
+    const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
+    const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+}
+
+// -------------------------------------------------------------------- amax --
+// Grid (nparts, batch).  Part i of matrix b reduces rows i, i+nparts, ... and
+// writes max |bf16| magnitude bits to amax_part[b*nparts + i].
+__global__ void __launch_bounds__(256) k_amax_partial(QuantParams p) {
+  __shared__ uint32_t scratch[32];
+  const int b = blockIdx.y;
+  const __nv_bfloat16 *base = p.src + (int64_t)b * p.bstride;
+  const int64_t vec_per_row = p.cols / 8;
+  uint32_t m2 = 0;
+  for (int64_t r = blockIdx.x; r < p.rows; r += gridDim.x) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(base + r * p.ld);
+    int64_t v = threadIdx.x;
+    for (; v + 3 * 256 < vec_per_row; v += 4 * 256) {
+      uint4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) a[u] = __ldg(row + v + u * 256);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        m2 = __vmaxu2(m2, a[u].x & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, a[u].y & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, a[u].z & 0x7FFF7FFFu);
+        m2 = __vmaxu2(m2, a[u].w & 0x7FFF7FFFu);
+      }
+    }
+    for (; v < vec_per_row; v += 256) {
+      const uint4 a = __ldg(row + v);
+      m2 = __vmaxu2(m2, a.x & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, a.y & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, a.z & 0x7FFF7FFFu);
+      m2 = __vmaxu2(m2, a.w & 0x7FFF7FFFu);
+    }
+  }
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  m = block_max_u32(m, scratch);
+  if (threadIdx.x == 0) p.amax_part[(int64_t)b * p.nparts + blockIdx.x] = m;
+}
+
+// ------------------------------------------------------------- row packing --
+// One warp per destination row, one lane per 16-element block.  Grid
+// (ctas, batch); rows are striped over the warps of the grid.  Destination row
+// r reads source row row_map[r] (gather) or r; row_map < 0 rows are skipped.
+// With the swizzled layout, rows up to pad128 and scale columns up to pad4 are
+// written (zeros outside the matrix).
+template <bool kV8>
+__global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
+  __shared__ uint32_t scratch[32];
+  const int b = blockIdx.y;
+  const float g = resolve_global_scale(p, b, scratch);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) p.g_out[b] = g;
+  const BlockScale s = make_block_scale(g);
+
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nblk = p.cols / 16;
+  const int64_t sfc_pad = (nblk + 3) & ~int64_t(3);
+  const int64_t rows_out = p.sf_swizzled ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  const __nv_bfloat16 *src = p.src + (int64_t)b * p.bstride;
+  uint8_t *codes = p.codes_row + (int64_t)b * p.codes_row_bstride;
+  uint8_t *sf = p.sf_row + (int64_t)b * p.sf_row_bstride;
+  const int64_t row_bytes = p.cols / 2;
+
+  for (int64_t r = warp; r < rows_out; r += nwarps) {
+    int64_t sr = -1;
+    if (r < p.dst_rows) sr = p.row_map ? (int64_t)p.row_map[r] : r;
+    if (p.row_map && sr < 0) continue;   // unmapped (padding) rows are left untouched
+    const __nv_bfloat16 *srow = src + sr * p.ld;
+    for (int64_t blk0 = 0; blk0 < sfc_pad; blk0 += 128) {
+      uint32_t w[4][8];
+      uint64_t c[4];
+      uint32_t sb[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t blk = blk0 + u * 32 + lane;
+        if (sr >= 0 && blk < nblk) load16<kV8>(srow + blk * 16, w[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t blk = blk0 + u * 32 + lane;
+        c[u] = 0;
+        sb[u] = 0;
+        if (sr >= 0 && blk < nblk) c[u] = quant16(w[u], s, sb[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t blk = blk0 + u * 32 + lane;
+        if (blk0 + u * 32 >= sfc_pad) break;
+        if (sr >= 0 && blk < nblk)
+          *reinterpret_cast<uint2 *>(codes + r * row_bytes + blk * 8) =
+              make_uint2((uint32_t)c[u], (uint32_t)(c[u] >> 32));
+        if (p.sf_swizzled) {
+          uint32_t v = sb[u];
+          v |= __shfl_down_sync(0xffffffffu, sb[u], 1) << 8;
+          v |= __shfl_down_sync(0xffffffffu, sb[u], 2) << 16;
+          v |= __shfl_down_sync(0xffffffffu, sb[u], 3) << 24;
+          if ((lane & 3) == 0 && blk < sfc_pad)
+            *reinterpret_cast<uint32_t *>(sf + sf_swz_offset(r, blk, sfc_pad)) = v;
+        } else if (sr >= 0 && blk < nblk) {
+          sf[r * nblk + blk] = (uint8_t)sb[u];
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------- tiled col (+row) packing --
+// A CTA quantizes 64x64 tiles of one matrix: the tile is staged in shared
+// memory; each thread quantizes one 16-element row block from registers (row
+// packing) and one 16-element column block from shared memory (column
+// packing).  Requires rows % 16 == 0 for the column packing.
+constexpr int kTile = 64;
+
+__global__ void __launch_bounds__(256) k_quant_tiles(QuantParams p) {
+  __shared__ uint32_t scratch[32];
+  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTile];
+  __shared__ uint8_t sfcol[kTile][4];
+  const int b = blockIdx.y;
+  const float g = resolve_global_scale(p, b, scratch);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) p.g_out[b] = g;
+  const BlockScale s = make_block_scale(g);
+
+  const int t = threadIdx.x, lane = t & 31;
+  const int64_t tiles_r = (p.rows + kTile - 1) / kTile, tiles_c = (p.cols + kTile - 1) / kTile;
+  const __nv_bfloat16 *src = p.src + (int64_t)b * p.bstride;
+  const bool do_row = p.codes_row != nullptr, do_col = p.codes_col != nullptr;
+  // row packing geometry
+  const int64_t nblk_r = p.cols / 16, sfc_pad_r = (nblk_r + 3) & ~int64_t(3);
+  // column packing: output matrix is [cols][rows]
+  const int64_t nblk_c = p.rows / 16, sfc_pad_c = (nblk_c + 3) & ~int64_t(3);
+  uint8_t *codes_r = do_row ? p.codes_row + (int64_t)b * p.codes_row_bstride : nullptr;
+  uint8_t *sf_r = do_row ? p.sf_row + (int64_t)b * p.sf_row_bstride : nullptr;
+  uint8_t *codes_c = do_col ? p.codes_col + (int64_t)b * p.codes_col_bstride : nullptr;
+  uint8_t *sf_c = do_col ? p.sf_col + (int64_t)b * p.sf_col_bstride : nullptr;
+
+  for (int64_t tix = blockIdx.x; tix < tiles_r * tiles_c; tix += gridDim.x) {
+    const int64_t r0 = (tix / tiles_c) * kTile, c0 = (tix % tiles_c) * kTile;
+    // load: thread t holds tile row t/4, 16-column block t%4
+    const int tr = t >> 2, tb = t & 3;
+    const int64_t gr = r0 + tr, gc = c0 + tb * 16;
+    uint32_t w[8];
+    const bool in = gr < p.rows && gc < p.cols;
+    if (in) load16<false>(src + gr * p.ld + gc, w);
+    else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = 0;
+    }
+    __syncthreads();   // previous tile's column readers are done
+    *reinterpret_cast<uint4 *>(&tile[tr][tb * 16]) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(&tile[tr][tb * 16 + 8]) = make_uint4(w[4], w[5], w[6], w[7]);
+
+    if (do_row) {
+      uint32_t sb = 0;
+      uint64_t c = in ? quant16(w, s, sb) : 0ull;
+      if (in)
+        *reinterpret_cast<uint2 *>(codes_r + gr * (p.cols / 2) + gc / 2) =
+            make_uint2((uint32_t)c, (uint32_t)(c >> 32));
+      const int64_t blk = gc / 16;
+      if (p.sf_swizzled) {
+        uint32_t v = sb;
+        v |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
+        v |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
+        v |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
+        if (tb == 0 && gr < p.rows && blk < sfc_pad_r)
+          *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = v;
+      } else if (in) {
+        sf_r[gr * nblk_r + blk] = (uint8_t)sb;
+      }
+    }
+    __syncthreads();
+    if (do_col) {
+      // thread t: tile column t%64, row block t/64 (16 rows)
+      const int cc = t & 63, rb = t >> 6;
+      const int64_t oc = c0 + cc;                 // output row (= input column)
+      const int64_t orow_blk = (r0 + rb * 16) / 16;
+      const bool cin = oc < p.cols && r0 + rb * 16 < p.rows;
+      uint32_t cw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = __bfloat16_as_ushort(tile[rb * 16 + 2 * i][cc]);
+        const uint32_t hi = __bfloat16_as_ushort(tile[rb * 16 + 2 * i + 1][cc]);
+        cw[i] = lo | (hi << 16);
+      }
+      uint32_t sb = 0;
+      const uint64_t c = cin ? quant16(cw, s, sb) : 0ull;
+      if (cin)
+        *reinterpret_cast<uint2 *>(codes_c + oc * (p.rows / 2) + (r0 + rb * 16) / 2) =
+            make_uint2((uint32_t)c, (uint32_t)(c >> 32));
+      if (p.sf_swizzled) {
+        sfcol[cc][rb] = (uint8_t)sb;
+      } else if (cin) {
+        sf_c[oc * nblk_c + orow_blk] = (uint8_t)sb;
+      }
+      __syncthreads();
+      if (p.sf_swizzled && t < kTile) {
+        const int64_t oc2 = c0 + t;
+        const int64_t blk = r0 / 16;    // first of 4 column blocks of this tile
+        if (oc2 < p.cols && blk < sfc_pad_c) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (r0 + k * 16 < p.rows) v |= (uint32_t)sfcol[t][k] << (8 * k);
+          *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc2, blk, sfc_pad_c)) = v;
+        }
+      }
+    }
+  }
+  (void)lane;
+}
+
+// Zero the swizzled padding of a scale buffer that the tile kernel does not
+// reach: rows in [rows, pad128(rows)) of every matrix.  Columns beyond the
+// matrix inside a reached row are written by the kernels themselves.
+__global__ void k_zero_sf_pad_rows(uint8_t *sf, int64_t bstride, int64_t rows, int64_t sf_cols) {
+  const int b = blockIdx.y;
+  const int64_t sfc_pad = (sf_cols + 3) & ~int64_t(3);
+  const int64_t prow = (rows + 127) & ~int64_t(127);
+  const int64_t n = (prow - rows) * sfc_pad;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = rows + i / sfc_pad, c = i % sfc_pad;
+    sf[(int64_t)b * bstride + sf_swz_offset(r, c, sfc_pad)] = 0;
+  }
+}
+
+// ---------------------------------------------------------------- launchers --
+
+int amax_parts_for(int64_t rows) { return (int)std::min<int64_t>(rows, 512); }
+
+cudaError_t launch_amax(const QuantParams &p, cudaStream_t st) {
+  dim3 grid(p.nparts, (unsigned)p.batch);
+  k_amax_partial<<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st) {
+  const int64_t rows_out = p.sf_swizzled ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  int64_t ctas = (rows_out + 7) / 8;      // 8 warps per CTA, one row each per pass
+  const int64_t cap = (int64_t)num_sms * 8 / std::max<int64_t>(1, p.batch);
+  ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, std::max<int64_t>(cap, 1)));
+  dim3 grid((unsigned)ctas, (unsigned)p.batch);
+  const bool v8 = ((reinterpret_cast<uintptr_t>(p.src) & 31) == 0) && (p.ld % 16 == 0) &&
+                  (p.bstride % 16 == 0);
+  if (v8) k_quant_rows<true><<<grid, 256, 0, st>>>(p);
+  else k_quant_rows<false><<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
+  const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kTile - 1) / kTile);
+  int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * 8 / std::max<int64_t>(1, p.batch));
+  ctas = std::max<int64_t>(ctas, 1);
+  dim3 grid((unsigned)ctas, (unsigned)p.batch);
+  k_quant_tiles<<<grid, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !p.sf_swizzled) return e;
+  // rows beyond the matrix inside the last 128-row atom
+  if (p.codes_row && (p.rows % 128) != 0) {
+    k_zero_sf_pad_rows<<<dim3(4, (unsigned)p.batch), 256, 0, st>>>(p.sf_row, p.sf_row_bstride,
+                                                                  p.rows, p.cols / 16);
+  }
+  if (p.codes_col && (p.cols % 128) != 0) {
+    k_zero_sf_pad_rows<<<dim3(4, (unsigned)p.batch), 256, 0, st>>>(p.sf_col, p.sf_col_bstride,
+                                                                  p.cols, p.rows / 16);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

@@ -235,3 +235,41 @@ def ceil_div(a: int, b: int) -> int:
 
 def log2_int(v: int) -> int:
     return int(math.log2(v))
+
+
+def torch_case(name: str, seed: int = 0, device="cuda", **over) -> dict:
+    """The named workload drawn on ``device`` (same recipe, torch Philox streams).
+
+    Returns torch tensors (bf16 / int32).  Used for full-size benchmark inputs."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(seed)
+    if name == "prefill":
+        c = dict(CONFIGS["prefill"], **over)
+        return dict(x=torch_normal_bf16((c["M"], c["K"]), 1.0, gen, device),
+                    w=torch_normal_bf16((c["N"], c["K"]), 0.02, gen, device),
+                    lora_a=torch_normal_bf16((c["rank"], c["K"]), 0.01, gen, device),
+                    lora_b=torch_normal_bf16((c["N"], c["rank"]), 0.01, gen, device), **c)
+    if name == "grouped":
+        c = dict(CONFIGS["grouped"], **over)
+        return dict(x=torch_normal_bf16((c["T"], c["K"]), 1.0, gen, device),
+                    w=torch_normal_bf16((c["E"], c["N"], c["K"]), 0.02, gen, device),
+                    lora_a=torch_normal_bf16((c["E"], c["rank"], c["K"]), 0.01, gen, device),
+                    lora_b=torch_normal_bf16((c["E"], c["N"], c["rank"]), 0.01, gen, device),
+                    expert_ids=torch_route_top_k(c["T"], c["E"], c["topk"], gen, device), **c)
+    if name == "quantize":
+        c = dict(CONFIGS["quantize"], **over)
+        w = torch_normal_bf16((c["E"], c["N"], c["K"]), 0.02, gen, device)
+        torch_outliers_per_row(w, int(round(0.001 * c["K"])), 50.0, gen)
+        return dict(w=w, **c)
+    if name in ("decode_q_b_proj", "decode_o_proj"):
+        c = dict(CONFIGS[name], **over)
+        M = over.get("M", 1)
+        return dict(w=torch_normal_bf16((c["N"], c["K"]), 0.02, gen, device),
+                    x=torch_normal_bf16((M, c["K"]), 1.0, gen, device), M=M, N=c["N"], K=c["K"])
+    if name == "tiny":
+        c = dict(CONFIGS["tiny"], **over)
+        w = torch_normal_bf16((c["N"], c["K"]), 0.02, gen, device)
+        x = torch_normal_bf16((c["M"], c["K"]), 1.0, gen, device)
+        torch_outliers_global(x, 0.01, 20.0, gen)
+        return dict(x=x, w=w, **c)
+    raise KeyError(name)

@@ -1,0 +1,181 @@
+"""nvfp4_gemm / nvfp4_lora_epilogue on the GPU against the oracle.
+
+Tolerances (fp64 oracle Y_or, S = sum_k |x_hat w_hat| per output):
+  fp32 out: |Y - Y_or| <= 2e-5 S;  bf16 out: |Y - bf16(Y_or)| <= ulp(max(|Y_or|, 2e-5 S));
+  with the LoRA branch both add 2^-8 (alpha/r) sum_j |T_j||B_nj| (bf16 rounding of
+  the scaled T before the tensor-core step)."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_block_scaled_06_gb300 as nv
+from helpers import (assert_bits_equal, assert_gemm_close, dev_bf16, host_bits,
+                     lora_bf16_term, u8)
+from oracle import nvfp4_oracle as o
+from synth import f32_to_bf16_bits, make_case
+
+pytestmark = pytest.mark.gpu
+
+
+def quant_dev(bits, static=None):
+    gs = None if static is None else torch.tensor([static], dtype=torch.float32, device="cuda")
+    out = nv.nvfp4_quantize(dev_bf16(bits), pack="row", sf_layout="swizzled", global_scale=gs)
+    return out["codes_row"], out["sf_row"], out["global_scale"]
+
+
+def oracle_linear(x_bits, w_bits, lora=None, xg=None):
+    xq = o.quantize(x_bits, xg)
+    wq = o.quantize(w_bits)
+    y = o.linear_fp64(xq, wq, x_bits, lora)
+    s = o.error_scale(xq, wq)
+    term = None if lora is None else lora_bf16_term(x_bits, *lora)
+    return y, s, term
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_tiny_config_packed_operands(out_dtype):
+    c = make_case("tiny")                          # X[32,512] with outliers, W[256,512]
+    xc, xs, xg = quant_dev(c["x"])
+    wc, ws, wg = quant_dev(c["w"])
+    y = nv.nvfp4_gemm(wc, ws, wg, 256, 512, a_codes=xc, a_sf=xs, a_global_scale=xg,
+                      out_dtype=out_dtype)
+    y_or, S, _ = oracle_linear(c["x"], c["w"])
+    assert_gemm_close(y, y_or, S, what="tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 320, 544), (128, 256, 256), (1, 128, 32),
+                                   (513, 1024, 2048), (200, 640, 1056)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_ragged_gemm(M, N, K, out_dtype):
+    rng = np.random.default_rng(M + N + K)
+    xb = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wb = f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    xc, xs, xg = quant_dev(xb)
+    wc, ws, wg = quant_dev(wb)
+    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg,
+                      out_dtype=out_dtype)
+    y_or, S, _ = oracle_linear(xb, wb)
+    assert_gemm_close(y, y_or, S, what=f"gemm {M}x{N}x{K}")
+
+
+def test_bf16_input_dynamic_matches_packed_path():
+    c = make_case("prefill", M=384, N=512, K=1024)
+    wc, ws, wg = quant_dev(c["w"])
+    x = dev_bf16(c["x"])
+    y1 = nv.nvfp4_gemm(wc, ws, wg, 512, 1024, a_bf16=x)
+    xc, xs, xg = quant_dev(c["x"])
+    y2 = nv.nvfp4_gemm(wc, ws, wg, 512, 1024, a_codes=xc, a_sf=xs, a_global_scale=xg)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.parametrize("rank", [64, 32, 128])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_prefill_lora_small(rank, out_dtype):
+    M, N, K = 320, 512, 1024
+    c = make_case("prefill", M=M, N=N, K=K, rank=rank)
+    wc, ws, wg = quant_dev(c["w"])
+    lora = dict(a=dev_bf16(c["lora_a"]), b=dev_bf16(c["lora_b"]), alpha=128.0)
+    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), lora=lora, out_dtype=out_dtype)
+    y_or, S, term = oracle_linear(c["x"], c["w"], (c["lora_a"], c["lora_b"], 128.0))
+    assert_gemm_close(y, y_or, S, term, what=f"lora r{rank}")
+
+
+def test_prefill_full_size_sampled_rows():
+    """X[8192,6144], W[2048,6144], LoRA r64 alpha 128, bf16 out: 96 sampled rows."""
+    c = make_case("prefill")
+    wc, ws, wg = quant_dev(c["w"])
+    lora = dict(a=dev_bf16(c["lora_a"]), b=dev_bf16(c["lora_b"]), alpha=128.0)
+    y = nv.nvfp4_gemm(wc, ws, wg, 2048, 6144, a_bf16=dev_bf16(c["x"]), lora=lora)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 127, 128, 8191],
+                                     np.random.default_rng(1).choice(8192, 92, replace=False)]))
+    gx = o.global_scale(c["x"])
+    xq = o.quantize(c["x"][rows], gx)
+    wq = o.quantize(c["w"])
+    lo = (c["lora_a"], c["lora_b"], 128.0)
+    y_or = o.linear_fp64(xq, wq, c["x"][rows], lo)
+    S = o.error_scale(xq, wq)
+    term = lora_bf16_term(c["x"][rows], *lo)
+    assert_gemm_close(y[torch.from_numpy(rows).cuda()], y_or, S, term, what="prefill full")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 32])
+def test_decode_static_scale(M):
+    """Decode: X quantized per call with a static input_scale (GEMV for M <= 4)."""
+    N, K = 1024, 2048
+    c = make_case("decode_q_b_proj", M=M, N=N, K=K)
+    static = 16.0 / 2688.0
+    wc, ws, wg = quant_dev(c["w"])
+    gx = torch.tensor([static], dtype=torch.float32, device="cuda")
+    for od in (torch.bfloat16, torch.float32):
+        y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx,
+                          out_dtype=od)
+        y_or, S, _ = oracle_linear(c["x"], c["w"], xg=np.float32(static))
+        assert_gemm_close(y, y_or, S, what=f"decode M{M}")
+
+
+@pytest.mark.parametrize("name", ["decode_q_b_proj", "decode_o_proj"])
+def test_decode_full_weights_sampled(name):
+    c = make_case(name, M=1)
+    N, K = c["N"], c["K"]
+    static = np.float32(16.0 / 2688.0)
+    wc, ws, wg = quant_dev(c["w"])
+    gx = torch.tensor([float(static)], dtype=torch.float32, device="cuda")
+    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx,
+                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    cols = np.random.default_rng(2).choice(N, 256, replace=False)
+    xq = o.quantize(c["x"], static)
+    wq = o.quantize(c["w"][cols])
+    wq = (wq[0], wq[1], o.global_scale(c["w"]))
+    # the sampled rows of W quantized with the tensor-wide scale
+    wq = o.quantize(c["w"][cols], o.global_scale(c["w"]))
+    y_or = o.linear_fp64(xq, wq)
+    S = o.error_scale(xq, wq)
+    assert_gemm_close(y[:, torch.from_numpy(cols).cuda()], y_or, S, what=name)
+
+
+@pytest.mark.parametrize("ydtype", [torch.bfloat16, torch.float32])
+def test_lora_epilogue_in_place_and_norm(ydtype):
+    M, N, K, r = 300, 384, 512, 64
+    c = make_case("prefill", M=M, N=N, K=K, rank=r)
+    rng = np.random.default_rng(9)
+    y0 = rng.standard_normal((M, N)).astype(np.float32)
+    y = torch.from_numpy(y0).to("cuda", ydtype)
+    ybase = y.double().cpu().numpy()
+    norm = nv.nvfp4_lora_epilogue(y, dev_bf16(c["x"]), dev_bf16(c["lora_a"]),
+                                  dev_bf16(c["lora_b"]), 128.0, want_norm=True)
+    torch.cuda.synchronize()
+    d, _ = o.lora_delta_fp64(c["x"], c["lora_a"], c["lora_b"], 128.0)
+    term = lora_bf16_term(c["x"], c["lora_a"], c["lora_b"], 128.0)
+    got = y.double().cpu().numpy()
+    tol = term + 2e-5 * np.abs(d) + 1e-30
+    if ydtype == torch.bfloat16:
+        tol = tol + o.bf16_ulp(np.abs(ybase + d) + 1e-30)
+    assert np.all(np.abs(got - (ybase + d)) <= tol)
+    want = float(np.sum(d * d))
+    assert abs(float(norm) - want) <= 2e-2 * want
+
+
+def test_timeout_path_reports_and_recovers():
+    """A zero wait budget makes in-kernel waits expire: the call must report
+    NVFP4_ERR_TIMEOUT through the status word and leave the context usable."""
+    M, N, K = 1024, 2048, 8192
+    rng = np.random.default_rng(11)
+    xb = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wb = f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    xc, xs, xg = quant_dev(xb)
+    wc, ws, wg = quant_dev(wb)
+    call, y = nv.prepare_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg)
+    old = nv.set_wait_timeout_ns(0)
+    try:
+        call()
+        st = nv.read_device_status(call.workspace)
+    finally:
+        nv.set_wait_timeout_ns(old)
+    assert st == 6, st
+    call()
+    assert nv.read_device_status(call.workspace) == 0
+    y_or, S, _ = oracle_linear(xb[:64], wb)
+    assert_gemm_close(y[:64], y_or, S, what="after timeout")

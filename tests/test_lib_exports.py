@@ -1,0 +1,90 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/nvfp4.h declares, and rejects bad arguments on the host before any
+device work (status codes only; no compute call is made here)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def clib():
+    from nvfp4_block_scaled_06_gb300 import build as b
+    b.build()
+    from nvfp4_block_scaled_06_gb300 import _binding
+    return _binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(clib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(clib, n), n
+    from nvfp4_block_scaled_06_gb300._binding import EXPORTS
+    assert sorted(EXPORTS) == names
+
+
+def test_size_queries(clib):
+    assert clib.nvfp4_codes_bytes(2048, 6144) == 2048 * 3072
+    assert clib.nvfp4_sf_bytes(2048, 6144, 0) == 2048 * 384
+    # swizzled: rows padded to 128, scale columns padded to 4
+    assert clib.nvfp4_sf_bytes(37, 80, 1) == 128 * 8
+    assert clib.nvfp4_status_string(4).decode().startswith("workspace")
+    assert clib.nvfp4_version() == 0x000100
+
+
+def test_host_validation_without_device(clib):
+    from nvfp4_block_scaled_06_gb300._binding import (ERR_ALIGNMENT, ERR_INVALID_ARG,
+                                                       ERR_UNSUPPORTED_SHAPE, GemmArgs,
+                                                       GroupedArgs, LoraArgs, QuantArgs)
+    nullq = C.cast(None, C.POINTER(QuantArgs))
+    assert clib.nvfp4_quantize(nullq, None) == ERR_INVALID_ARG
+    q = QuantArgs(src=4096, batch=1, rows=16, cols=24, ld=24, pack=1, sf_layout=1,
+                  global_scale_out=4096, codes_row=4096, sf_row=4096)
+    assert clib.nvfp4_quantize(C.byref(q), None) == ERR_UNSUPPORTED_SHAPE      # cols % 16
+    q.cols, q.ld = 32, 32
+    q.src = 4104                                                              # not 16-aligned
+    assert clib.nvfp4_quantize(C.byref(q), None) == ERR_ALIGNMENT
+    g = GemmArgs(M=8, N=8, K=48, a_codes=4096, a_sf=4096, a_global_scale=4096, b_codes=4096,
+                 b_sf=4096, b_global_scale=4096, d=4096, ldd=8)
+    assert clib.nvfp4_gemm(C.byref(g), None) == ERR_UNSUPPORTED_SHAPE          # K % 32
+    g.K = 64
+    g.lora_a, g.lora_b, g.lora_x, g.lda, g.rank = 4096, 4096, 4096, 64, 48
+    assert clib.nvfp4_gemm(C.byref(g), None) == ERR_UNSUPPORTED_SHAPE          # rank % 32
+    gr = GroupedArgs(num_tokens=4, top_k=2, num_experts=8, N=200, K=64, expert_ids=4096,
+                     x_bf16=4096, w_codes=4096, w_sf=4096, w_global_scale=4096, d=4096,
+                     perm_out=4096)
+    assert clib.nvfp4_grouped_gemm(C.byref(gr), None) == ERR_UNSUPPORTED_SHAPE  # N % 256
+    lo = LoraArgs(M=4, N=8, K=64, x=4096, ldx=64, lora_a=4096, lora_b=4096, rank=64,
+                  y=4096, ldy=8, y_dtype=3)
+    assert clib.nvfp4_lora_epilogue(C.byref(lo), None) == ERR_INVALID_ARG      # bad dtype
+
+
+def test_workspace_queries_need_no_device(clib):
+    from nvfp4_block_scaled_06_gb300._binding import GemmArgs, GroupedArgs
+    g = GemmArgs(M=8192, N=2048, K=6144, a_bf16=4096, lda=6144, b_codes=4096, b_sf=4096,
+                 b_global_scale=4096, d=4096, ldd=2048, lora_a=4096, lora_b=4096, rank=64,
+                 alpha=128.0)
+    ws = clib.nvfp4_gemm_workspace_bytes(C.byref(g))
+    # X codes + swizzled scales + T' (bf16 [M, r]) + small scalars
+    assert ws >= 8192 * 3072 + 8192 * 384 + 8192 * 64 * 2
+    gr = GroupedArgs(num_tokens=4096, top_k=8, num_experts=256, N=2048, K=6144)
+    assert clib.nvfp4_grouped_workspace_bytes(C.byref(gr)) > 32768 * 3072
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "nvfp4_block_scaled_06_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.replace("the oracle", ""), f
