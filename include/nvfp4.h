@@ -238,8 +238,10 @@ const char *nvfp4_status_string(nvfp4_status s);
  * start of `workspace` and returns it (NVFP4_OK when no wait expired). */
 nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream);
 /* Bound, in nanoseconds, of every in-kernel wait launched afterwards by this
- * process (default 2e9).  Tests set a tiny bound to exercise the timeout path
- * without a hang.  Returns the previous value. */
+ * process (default 2e9).  Returns the previous value.  0 is a test hook: each
+ * GEMM kernel launched afterwards first waits on a barrier that nothing
+ * arrives at, so its expiry path (status word NVFP4_ERR_TIMEOUT, drain of its
+ * own copies and MMAs, TMEM freed, early return) runs without any hang. */
 uint64_t nvfp4_set_wait_timeout_ns(uint64_t ns);
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t nvfp4_version(void);

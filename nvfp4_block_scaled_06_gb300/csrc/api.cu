@@ -190,7 +190,29 @@ struct GemmPlan {
   uint32_t *aq_amax = nullptr;
   int aq_nparts = 0;
   __nv_bfloat16 *t = nullptr;   // T' [M][rank]
+  float *t32 = nullptr;         // T [M][rank] fp32 (dynamic X with LoRA: amax in the same pass)
+  int bn = 256, ksplit = 1;
+  float *partial = nullptr;     // split-K partials [ksplit][M][N]
 };
+
+// K is split when the output has too few tiles to occupy the SMs (small-M
+// decode); the caller's SM count is taken from the device at plan time.
+int pick_ksplit(int64_t M, int64_t N, int64_t K, int bn, int sms, bool lora) {
+  if (lora) return 1;
+  const int64_t tiles = ceil_div(M, 128) * ceil_div(N, bn);
+  const int64_t nkt = ceil_div(K, 256);
+  if (tiles * 2 > sms || nkt < 8) return 1;
+  int64_t ks = std::max<int64_t>(1, (sms + tiles / 2) / tiles);
+  ks = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(ks, nkt / 4), 16));
+  const int64_t per = ceil_div(nkt, ks);   // every K range non-empty
+  return (int)ceil_div(nkt, per);
+}
+
+int plan_sms() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms > 0 ? sms : 148;
+}
 
 bool use_gemv(const nvfp4_gemm_args *a) {
   return a->a_bf16 && a->a_global_scale && a->M <= 4 && a->K % 64 == 0 && !a->lora_a &&
@@ -212,10 +234,17 @@ nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
     pl->aq_g = c.take<float>(4);
     if (!a->a_global_scale) {
       pl->aq_nparts = amax_parts_for(a->M);
-      pl->aq_amax = c.take<uint32_t>((size_t)pl->aq_nparts * 4);
+      // sized for either producer of the partials: the amax kernel or the LoRA pass's grid
+      pl->aq_amax = c.take<uint32_t>((size_t)std::max(pl->aq_nparts, 1024) * 4);
     }
   }
   if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)a->M * a->rank * 2);
+  if (a->lora_a && a->a_bf16 && !a->a_global_scale && !a->lora_x)
+    pl->t32 = c.take<float>((size_t)a->M * a->rank * 4);
+  const int sms = plan_sms();
+  pl->bn = pick_bn(a->M, a->N, sms);
+  pl->ksplit = pick_ksplit(a->M, a->N, a->K, pl->bn, sms, a->lora_a != nullptr);
+  if (pl->ksplit > 1) pl->partial = c.take<float>((size_t)pl->ksplit * a->M * a->N * 4);
   pl->ws = c.off;
   return NVFP4_OK;
 }
@@ -276,6 +305,29 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   const uint8_t *a_codes = a->a_codes, *a_sf = a->a_sf;
   const float *g_a = a->a_global_scale;
   const void *xb = a->lora_x ? a->lora_x : a->a_bf16;
+  const int bn = pl.bn;
+  GemmMaps maps;
+  int lora_steps = 0;
+  LoraDownMaps lm;
+  LoraDownParams lp{};
+  if (a->lora_a) {
+    if (!map2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a->K, a->M, a->lda * 2, 64, 128) ||
+        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->rank, a->K * 2, 64, a->rank) ||
+        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, a->M, a->rank * 2, 64, 128) ||
+        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, bn))
+      return NVFP4_ERR_CUDA;
+    lp.M = a->M;
+    lp.K = a->K;
+    lp.rank = a->rank;
+    lp.num_k64 = (int)ceil_div(a->K, 64);
+    lp.lora_scale = a->alpha / (float)a->rank;
+    lp.g_b = a->b_global_scale;
+    lp.t_out = pl.t;
+    lp.tiles_m = (int)ceil_div(a->M, 128);
+    lp.status = status;
+    lp.timeout_ns = tmo;
+    lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+  }
   if (a->a_bf16) {
     QuantParams q{};
     q.src = static_cast<const __nv_bfloat16 *>(a->a_bf16);
@@ -291,41 +343,36 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     q.sf_row = pl.aq_sf;
     q.sf_swizzled = 1;
     q.dst_rows = a->M;
-    if (!a->a_global_scale && launch_amax(q, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (pl.t32) {
+      // one pass over X forms T = X A^T (fp32) and the amax partials; the
+      // packing pass then derives g, quantizes X and rounds T' = bf16(T s)
+      lp.amax_part = pl.aq_amax;
+      lp.t_f32 = pl.t32;
+      if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+      q.nparts = std::min(lp.tiles_m, sms);
+      q.t_f32 = pl.t32;
+      q.t_out = pl.t;
+      q.rank = a->rank;
+      q.lora_scale = lp.lora_scale;
+      q.g_b = a->b_global_scale;
+    } else if (!a->a_global_scale && launch_amax(q, st) != cudaSuccess) {
+      return NVFP4_ERR_CUDA;
+    }
     if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
     a_codes = pl.aq_codes;
     a_sf = pl.aq_sf;
     g_a = pl.aq_g;
   }
-  GemmMaps maps;
-  const int bn = pick_bn(a->M, a->N, sms);
+  if (a->lora_a && !pl.t32) {
+    lp.g_a = g_a;
+    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
   if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, a->K / 2, a->M, a->K / 2, 128, 128) ||
       !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, bn))
     return NVFP4_ERR_CUDA;
-  maps.t = maps.a;
-  maps.lb = maps.b;
-  int lora_steps = 0;
-  if (a->lora_a) {
-    LoraDownMaps lm;
-    if (!map2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a->K, a->M, a->lda * 2, 64, 128) ||
-        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->rank, a->K * 2, 64, a->rank) ||
-        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, a->M, a->rank * 2, 64, 128) ||
-        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, bn))
-      return NVFP4_ERR_CUDA;
-    LoraDownParams lp{};
-    lp.M = a->M;
-    lp.K = a->K;
-    lp.rank = a->rank;
-    lp.num_k64 = (int)ceil_div(a->K, 64);
-    lp.lora_scale = a->alpha / (float)a->rank;
-    lp.g_a = g_a;
-    lp.g_b = a->b_global_scale;
-    lp.t_out = pl.t;
-    lp.tiles_m = (int)ceil_div(a->M, 128);
-    lp.status = status;
-    lp.timeout_ns = tmo;
-    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
-    lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+  if (!a->lora_a) {
+    maps.t = maps.a;
+    maps.lb = maps.b;
   }
   GemmParams p{};
   p.M = a->M;
@@ -346,10 +393,14 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   p.lora_steps = lora_steps;
   p.tiles_m = (int)ceil_div(a->M, 128);
   p.tiles_n = (int)ceil_div(a->N, bn);
+  p.ksplit = pl.ksplit;
+  p.partial = pl.partial;
   p.status = status;
   p.timeout_ns = tmo;
+  p.stall_probe = tmo == 0;
   if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  if (e == cudaSuccess && pl.ksplit > 1) e = launch_splitk_reduce(p, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
   return cuda_status(e);
 }
@@ -513,6 +564,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   p.gnum_mtiles = pl.nmt;
   p.status = status;
   p.timeout_ns = tmo;
+  p.stall_probe = tmo == 0;
   if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
@@ -588,6 +640,7 @@ nvfp4_status run_lora(const nvfp4_lora_args *a, const LoraPlan &pl, int sms, cud
   p.tiles_n = (int)ceil_div(a->N, bn);
   p.status = status;
   p.timeout_ns = tmo;
+  p.stall_probe = tmo == 0;
   return cuda_status(launch_gemm_fp4(p, maps, bn, sms, st));
 }
 

@@ -26,7 +26,8 @@
 namespace nvfp4 {
 
 constexpr int kBM = 128;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
 constexpr uint64_t kDrainNs = 200000000ull;
 
 template <int BN>
@@ -53,10 +54,14 @@ struct TileInfo {
   int64_t a_row0, out_row0, b_row0, n0;
 };
 
+// Dense: n-tile major (concurrent CTAs share B tiles; all of A stays in L2).
+// Grouped: m-tile major (the 8 n-tiles of one expert's m-tile run together, so
+// its gathered A tile is read from L2 and each expert's weights stream once).
 template <int BN>
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, int nmt) {
   TileInfo ti;
-  const int nt = t / nmt, j = t % nmt;
+  const int nt = p.gtiles ? t % p.tiles_n : t / nmt;
+  const int j = p.gtiles ? t / p.tiles_n : t % nmt;
   ti.n0 = (int64_t)nt * BN;
   if (p.gtiles) {
     const GroupTile g = p.gtiles[j];
@@ -79,8 +84,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, int 
 // LoRA pre-scaling so that (alpha/r)/(g_a g_b) * (g_a g_b) cancels.  A zero
 // product means the FP4 operand is all zero codes; 1 keeps the LoRA exact.
 __device__ __forceinline__ float acc_scale(const float *g_a, const float *g_b, int e) {
-  const float ab = __fmul_rn(g_a ? *g_a : 1.0f, g_b ? g_b[e] : 1.0f);
-  return ab > 0.0f ? ab : 1.0f;
+  return acc_scale_of(g_a ? *g_a : 1.0f, g_b ? g_b[e] : 1.0f);
 }
 
 __device__ __forceinline__ void signal_abort(volatile int *abort_flag, int *status) {
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 1, *drain = acc_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  uint64_t *never = acc_full + 4;          // test hook: a barrier nothing arrives at
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -115,8 +120,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, kEpiWarps);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -138,8 +144,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int nmt = p.gtiles ? *p.gnum_mtiles : p.tiles_m;
-  const int num_tiles = nmt * p.tiles_n;
-  const int ksteps = p.num_kt + p.lora_steps;
+  const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
+  const int num_tiles = nmt * p.tiles_n * ksplit;     // work units: (tile, K range)
+  const int kt_per = (p.num_kt + ksplit - 1) / ksplit;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -148,9 +155,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;   // bit s: stage s has an outstanding fill
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile<BN>(p, t, nmt);
-        for (int kt = 0; kt < ksteps; ++kt) {
+      for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+        const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
+        const int kt0 = (u % ksplit) * kt_per;
+        const int kt1 = min(p.num_kt, kt0 + kt_per);
+        for (int kk = kt0; kk < kt1 + p.lora_steps; ++kk) {
+          const int kt = kk < kt1 ? kk : p.num_kt + (kk - kt1);   // LoRA steps follow the FP4 range
           if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns)) {
             signal_abort(abort_flag, p.status);
             ok = false;
@@ -200,8 +210,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile<BN>(p, t, nmt);
+      if (p.stall_probe && !mbar_wait(never, 0, p.timeout_ns)) {
+        signal_abort(abort_flag, p.status);   // expected: the expiry path under test
+        ok = false;
+      }
+      for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+        const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
+        const int kt0 = (u % ksplit) * kt_per;
+        const int kt1 = min(p.num_kt, kt0 + kt_per);
         if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1, p.timeout_ns)) {
           signal_abort(abort_flag, p.status);
           break;
@@ -209,7 +225,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         uint32_t accumulate = 0;
         const uint32_t sfb_lane_col = (uint32_t)((ti.b_row0 & 127) >> 5);
-        for (int kt = 0; kt < ksteps; ++kt) {
+        for (int kk = kt0; kk < kt1 + p.lora_steps; ++kk) {
+          const int kt = kk < kt1 ? kk : p.num_kt + (kk - kt1);
           if (*abort_flag || !mbar_wait(&full[stage], phase, p.timeout_ns)) {
             signal_abort(abort_flag, p.status);
             ok = false;
@@ -259,44 +276,58 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    // Warp w reads TMEM lane quarter (w % 4) and half (w - 2) / 4 of the BN
+    // columns: all of its accumulator columns are loaded into registers, the
+    // accumulator is released to the MMA warp, then the values are scaled,
+    // converted and stored while the next tile's MMAs run.
+    constexpr int kCh = BN / 64;            // 32-column chunks per thread
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;            // accumulator row owned by this thread
     uint32_t acc_phase = 0;
     float sq = 0.0f;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile<BN>(p, t, nmt);
+    for (int u = blockIdx.x; u < num_tiles; u += gridDim.x) {
+      const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
+      const int ks = u % ksplit;
       // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(acc_full, acc_phase, p.timeout_ns))) {
         if (lane == 0) signal_abort(abort_flag, p.status);
         break;
       }
       tc_fence_after();
+      uint32_t v[kCh][32];
+#pragma unroll
+      for (int c = 0; c < kCh; ++c)
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (half * kCh + c) * 32, v[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+      acc_phase ^= 1;
+
       const float alpha = p.accumulate_d ? 1.0f : acc_scale(p.g_a, p.g_b, ti.e);
-      const bool row_ok = r < ti.valid_rows;
+      if (r >= ti.valid_rows) continue;
       const int64_t orow = ti.out_row0 + r;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
-        tmem_ld_wait();
-        if (c == BN / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
-        }
-        const int64_t n = ti.n0 + c * 32;
-        if (!row_ok || n >= p.N) continue;
+#pragma unroll
+      for (int c = 0; c < kCh; ++c) {
+        const int64_t n = ti.n0 + (half * kCh + c) * 32;
+        if (n >= p.N) break;
         float f[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+        for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[c][i]), alpha);
         const bool full_chunk = n + 32 <= p.N;
-        if (p.out_fp32) {
+        const int nvalid = full_chunk ? 32 : (int)(p.N - n);
+        if (p.partial) {
+          float *dst = p.partial + ((int64_t)ks * p.M + orow) * p.N + n;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < nvalid) dst[i] = f[i];
+        } else if (p.out_fp32) {
           float *dst = reinterpret_cast<float *>(p.d) + orow * p.ldd + n;
           if (p.accumulate_d) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (full_chunk || n + i < p.N) {
+              if (i < nvalid) {
                 sq += f[i] * f[i];
                 dst[i] = dst[i] + f[i];
               }
@@ -308,16 +339,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) sq += f[i] * f[i];
           } else {
-            for (int i = 0; n + i < p.N; ++i) {
-              dst[i] = f[i];
-              sq += f[i] * f[i];
-            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) {
+                dst[i] = f[i];
+                sq += f[i] * f[i];
+              }
           }
         } else {
           __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.d) + orow * p.ldd + n;
           if (p.accumulate_d) {
+#pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (full_chunk || n + i < p.N) {
+              if (i < nvalid) {
                 sq += f[i] * f[i];
                 dst[i] = __float2bfloat16_rn(__fadd_rn(__bfloat162float(dst[i]), f[i]));
               }
@@ -335,14 +369,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) sq += f[i] * f[i];
           } else {
-            for (int i = 0; n + i < p.N; ++i) {
-              dst[i] = __float2bfloat16_rn(f[i]);
-              sq += f[i] * f[i];
-            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) {
+                dst[i] = __float2bfloat16_rn(f[i]);
+                sq += f[i] * f[i];
+              }
           }
         }
       }
-      acc_phase ^= 1;
     }
     if (p.sqnorm) {
 #pragma unroll
@@ -389,18 +424,21 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
   uint64_t *acc_full = bars + 2 * stages, *acc_empty = acc_full + 1, *drain = acc_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  uint32_t *amax_smem = tmem_slot + 2;
   const uint32_t tcols = tmem_cols_for(p.rank);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool scan = p.amax_part != nullptr;   // epilogue warps also scan X for amax
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], scan ? 5 : 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *amax_smem = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -502,9 +540,39 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t m2 = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
       int64_t row0;
       int e = 0;
+      if (scan) {
+        // max |x| over this warp's 32 rows of every X tile, read from shared memory
+        for (int kt = 0; kt < p.num_k64; ++kt) {
+          if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(&full[stage], phase, p.timeout_ns))) {
+            if (lane == 0) signal_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + r * 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = row[i];
+            m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+            m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[stage]);
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
       if (p.gtiles) {
         row0 = p.gtiles[t].a_row0;
         e = p.gtiles[t].expert;
@@ -520,6 +588,27 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       if (p.g_a) s = __fdiv_rn(p.lora_scale, acc_scale(p.g_a, p.g_b, e));
       const int64_t row = row0 + r;
       const bool row_ok = p.gtiles ? true : row < p.M;
+      if (p.t_f32) {
+        for (int c = 0; c < p.rank / 32; ++c) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
+          tmem_ld_wait();
+          if (c == p.rank / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+          }
+          if (!row_ok) continue;
+          float4 *dst = reinterpret_cast<float4 *>(p.t_f32 + row * p.rank + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        }
+        acc_phase ^= 1;
+        continue;
+      }
       for (int c = 0; c < p.rank / 32; ++c) {
         uint32_t v[32];
         __syncwarp();
@@ -545,12 +634,39 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       }
       acc_phase ^= 1;
     }
+    if (scan) {
+      uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) atomicMax(amax_smem, m);
+    }
   }
   __syncthreads();
+  if (scan && threadIdx.x == 0) p.amax_part[blockIdx.x] = *amax_smem;
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, tcols);
   }
+}
+
+// ----------------------------------------------------------- split-K sum --
+__global__ void k_splitk_reduce(const GemmParams p) {
+  const int64_t total = p.M * p.N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / p.N, n = i % p.N;
+    float s = p.partial[i];
+    for (int k = 1; k < p.ksplit; ++k) s = __fadd_rn(s, p.partial[k * total + i]);
+    if (p.out_fp32) reinterpret_cast<float *>(p.d)[m * p.ldd + n] = s;
+    else reinterpret_cast<__nv_bfloat16 *>(p.d)[m * p.ldd + n] = __float2bfloat16_rn(s);
+  }
+}
+
+cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st) {
+  const int64_t total = p.M * p.N;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 4));
+  k_splitk_reduce<<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------- launch --
@@ -565,7 +681,7 @@ static cudaError_t launch_bn(const GemmParams &p, const GemmMaps &m, int num_sms
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  int64_t tiles = (int64_t)p.tiles_n * (p.gtiles ? 0 : p.tiles_m);
+  int64_t tiles = (int64_t)p.tiles_n * (p.gtiles ? 0 : p.tiles_m) * std::max(1, p.ksplit);
   int grid = num_sms;
   if (!p.gtiles) grid = (int)std::min<int64_t>(tiles, num_sms);
   if (grid <= 0) return cudaSuccess;

@@ -109,11 +109,11 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
         const float sw = e4m3_to_f32((sf4 >> (8 * bb)) & 0xFF);
-        uint32_t wh[8];
+        uint32_t wh[8];   // wh[j] = elements 2j, 2j+1 of the block (same order as X)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          wh[2 * j] = e2m1x2_to_h2(c[2 * bb] >> (8 * j));
-          wh[2 * j + 1] = e2m1x2_to_h2(c[2 * bb + 1] >> (8 * j));
+          wh[j] = e2m1x2_to_h2(c[2 * bb] >> (8 * j));
+          wh[4 + j] = e2m1x2_to_h2(c[2 * bb + 1] >> (8 * j));
         }
         const int64_t b = g4 * 4 + bb;
 #pragma unroll

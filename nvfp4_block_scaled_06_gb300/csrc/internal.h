@@ -24,6 +24,12 @@ struct QuantParams {
   int sf_swizzled;
   const int32_t *row_map;             // optional gather: dst row -> src row (<0: skip)
   int64_t dst_rows;                   // rows written by the row packing
+  // optional LoRA hand-off: T' = bf16(T * (lora_scale / (g * g_b))) per row
+  const float *t_f32;                 // [dst_rows][rank]
+  __nv_bfloat16 *t_out;               // [dst_rows][rank]
+  int rank;
+  float lora_scale;
+  const float *g_b;
 };
 
 int amax_parts_for(int64_t rows);
@@ -56,8 +62,11 @@ struct GemmParams {
   int tiles_m, tiles_n;
   const GroupTile *gtiles;    // grouped mode: m-tile table
   const int32_t *gnum_mtiles; // grouped mode: number of m-tiles (device)
+  int ksplit;                 // >1: K split into ranges, fp32 partials [ksplit][M][N]
+  float *partial;
   int *status;
   uint64_t timeout_ns;
+  int stall_probe;            // test hook: first wait on a barrier nothing arrives at
 };
 
 struct GemmMaps {
@@ -66,6 +75,8 @@ struct GemmMaps {
 
 cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, int num_sms,
                             cudaStream_t st);
+// Sums split-K partials in order: D = sum_s partial[s] (bf16 or fp32 out).
+cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st);
 
 // LoRA down-projection: T' = bf16(scale_row * X A^T), X gathered for grouped.
 struct LoraDownParams {
@@ -80,6 +91,8 @@ struct LoraDownParams {
   const GroupTile *gtiles;
   const int32_t *gnum_mtiles;
   const int32_t *row_map;     // grouped: padded row -> token (gather)
+  uint32_t *amax_part;        // optional: per-CTA max |x| magnitude bits of the X tiles read
+  float *t_f32;               // optional: write T in fp32 (unscaled) instead of T'
   int *status;
   uint64_t timeout_ns;
 };

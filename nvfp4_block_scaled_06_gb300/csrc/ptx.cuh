@@ -236,6 +236,15 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
 }
 
+// The scale applied to the FP4 accumulator, g_a * g_b; a zero product means
+// the FP4 operand holds only zero codes, and 1 keeps the LoRA term exact.  The
+// LoRA operand is pre-scaled by (alpha/r) / acc_scale so that the product
+// cancels; both sides must compute it bit for bit the same way.
+__device__ __forceinline__ float acc_scale_of(float g_a, float g_b) {
+  const float ab = __fmul_rn(g_a, g_b);
+  return ab > 0.0f ? ab : 1.0f;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -177,10 +177,16 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   uint8_t *sf = p.sf_row + (int64_t)b * p.sf_row_bstride;
   const int64_t row_bytes = p.cols / 2;
 
+  const float t_scale = p.t_f32 ? __fdiv_rn(p.lora_scale, acc_scale_of(g, *p.g_b)) : 0.0f;
   for (int64_t r = warp; r < rows_out; r += nwarps) {
     int64_t sr = -1;
     if (r < p.dst_rows) sr = p.row_map ? (int64_t)p.row_map[r] : r;
     if (p.row_map && sr < 0) continue;   // unmapped (padding) rows are left untouched
+    if (p.t_f32 && r < p.dst_rows) {
+      // LoRA hand-off: the down-projection's fp32 row, scaled and rounded once to bf16
+      for (int j = lane; j < p.rank; j += 32)
+        p.t_out[r * p.rank + j] = __float2bfloat16_rn(__fmul_rn(p.t_f32[r * p.rank + j], t_scale));
+    }
     const __nv_bfloat16 *srow = src + sr * p.ld;
     for (int64_t blk0 = 0; blk0 < sfc_pad; blk0 += 128) {
       uint32_t w[4][8];
