@@ -112,6 +112,22 @@ def ev_pairs(torch, n):
             for _ in range(n)]
 
 
+def arm(C, args, pr):
+    """Point the library's profiling hook at an event pair (or disarm it).
+
+    The library records the events around its kernel with cudaEventRecord;
+    torch records them once first so that it accepts them in elapsed_time()
+    (the library's later record on the same stream sets the timestamps)."""
+    if pr is None:
+        args.prof_begin = None
+        args.prof_end = None
+    else:
+        pr[0].record()
+        pr[1].record()
+        args.prof_begin = C.c_void_p(pr[0].cuda_event)
+        args.prof_end = C.c_void_p(pr[1].cuda_event)
+
+
 def mean_ms(pairs):
     return sum(a.elapsed_time(b) for a, b in pairs) / max(1, len(pairs))
 
@@ -157,12 +173,7 @@ def run_main(args, torch, nv, device, rank, world):
 
     def step(i, pr):
         call = calls[i % rotate]
-        if pr is not None:
-            call.args.prof_begin = C.c_void_p(pr[0].cuda_event)
-            call.args.prof_end = C.c_void_p(pr[1].cuda_event)
-        else:
-            call.args.prof_begin = None
-            call.args.prof_end = None
+        arm(C, call.args, pr)
         call()
 
     for i in range(args.warmup):
@@ -215,8 +226,7 @@ def run_quantize_sweep(torch, nv, device, steps, warmup, pk):
     prof = ev_pairs(torch, steps)
 
     def step(i, pr):
-        call.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
-        call.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+        arm(C, call.args, pr)
         call()
     ms = time_loop(torch, step, steps, warmup, prof)
     elems = E * N * K
@@ -250,8 +260,7 @@ def run_decode(torch, nv, device, steps, warmup, pk):
 
             def step(i, pr, calls=calls):
                 cl = calls[i % len(calls)]
-                cl.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
-                cl.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+                arm(C, cl.args, pr)
                 cl()
             ms = time_loop(torch, step, steps, warmup, prof)
             kms = mean_ms(prof)
@@ -280,8 +289,7 @@ def run_grouped(torch, nv, device, steps, warmup, pk):
     prof = ev_pairs(torch, steps)
 
     def step(i, pr):
-        call.args.prof_begin = None if pr is None else C.c_void_p(pr[0].cuda_event)
-        call.args.prof_end = None if pr is None else C.c_void_p(pr[1].cuda_event)
+        arm(C, call.args, pr)
         call()
     ms = time_loop(torch, step, steps, warmup, prof)
     kms = mean_ms(prof)

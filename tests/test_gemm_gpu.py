@@ -127,9 +127,7 @@ def test_decode_full_weights_sampled(name):
     torch.cuda.synchronize()
     cols = np.random.default_rng(2).choice(N, 256, replace=False)
     xq = o.quantize(c["x"], static)
-    wq = o.quantize(c["w"][cols])
-    wq = (wq[0], wq[1], o.global_scale(c["w"]))
-    # the sampled rows of W quantized with the tensor-wide scale
+    # the sampled rows of W, quantized with the whole tensor's global scale
     wq = o.quantize(c["w"][cols], o.global_scale(c["w"]))
     y_or = o.linear_fp64(xq, wq)
     S = o.error_scale(xq, wq)
@@ -177,5 +175,6 @@ def test_timeout_path_reports_and_recovers():
     assert st == 6, st
     call()
     assert nv.read_device_status(call.workspace) == 0
-    y_or, S, _ = oracle_linear(xb[:64], wb)
+    # first 64 rows, quantized with the whole tensor's global scale
+    y_or, S, _ = oracle_linear(xb[:64], wb, xg=o.global_scale(xb))
     assert_gemm_close(y[:64], y_or, S, what="after timeout")
