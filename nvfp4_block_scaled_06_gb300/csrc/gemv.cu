@@ -25,6 +25,7 @@ namespace nvfp4 {
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lanes x 64
+constexpr int kRows = 4;           // units (rows) a warp has in flight
 
 __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
   uint32_t r;
@@ -89,63 +90,82 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   const int64_t nwarps = (int64_t)gridDim.x * (kGemvThreads / 32);
   const int64_t units = p.N * nchunks;
   const int64_t row_bytes = K / 2;
-  for (int64_t u = warp; u < units; u += nwarps) {
-    // consecutive warps take consecutive rows of one chunk (shared scale atoms)
-    const int64_t kc = u / p.N, n = u % p.N;
-    float acc[MX];
+  const int64_t g4_total = K / 64;
+  // A warp takes kRows consecutive units (consecutive rows of one K chunk) and
+  // issues all of their loads before any arithmetic, so every lane keeps
+  // kRows x 32 bytes of weights in flight.
+  for (int64_t u0 = warp * kRows; u0 < units; u0 += nwarps * kRows) {
+    uint32_t c[kRows][8];
+    uint32_t sf4[kRows];
+    int64_t n[kRows], g4v[kRows];
 #pragma unroll
-    for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
-    const int64_t g4_begin = kc * (kGemvChunk / 64);
-    const int64_t g4_end = (K / 64 < g4_begin + kGemvChunk / 64) ? K / 64 : g4_begin + kGemvChunk / 64;
-    for (int64_t g4 = g4_begin + lane; g4 < g4_end; g4 += 32) {
-      uint32_t c[8];
-      asm volatile(
-          "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-          : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3]), "=r"(c[4]), "=r"(c[5]), "=r"(c[6]),
-            "=r"(c[7])
-          : "l"(p.w_codes + n * row_bytes + g4 * 32));
-      const uint32_t sf4 = __ldg(reinterpret_cast<const uint32_t *>(
-          p.w_sf + 512 * ((n >> 7) * p.w_sf_katoms + g4) + 16 * (n & 31) + 4 * ((n & 127) >> 5)));
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        const float sw = e4m3_to_f32((sf4 >> (8 * bb)) & 0xFF);
-        uint32_t wh[8];   // wh[j] = elements 2j, 2j+1 of the block (same order as X)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          wh[j] = e2m1x2_to_h2(c[2 * bb] >> (8 * j));
-          wh[4 + j] = e2m1x2_to_h2(c[2 * bb + 1] >> (8 * j));
-        }
-        const int64_t b = g4 * 4 + bb;
-#pragma unroll
-        for (int m = 0; m < MX; ++m) {
-          const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2) + b * 8);
-          const uint4 x0 = xp[0], x1 = xp[1];
-          const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          __half2 s = __float2half2_rn(0.0f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            s = __hfma2(*reinterpret_cast<const __half2 *>(&wh[j]),
-                        *reinterpret_cast<const __half2 *>(&xv[j]), s);
-          const float dot = __fadd_rn(__low2float(s), __high2float(s));
-          acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + b]), acc[m]);
-        }
+    for (int j = 0; j < kRows; ++j) {
+      const int64_t u = u0 + j;
+      const int64_t kc = u / p.N;
+      n[j] = u % p.N;
+      g4v[j] = kc * (kGemvChunk / 64) + lane;
+      const bool live = u < units && g4v[j] < g4_total && g4v[j] < (kc + 1) * (kGemvChunk / 64);
+      if (!live) g4v[j] = -1;
+      if (live) {
+        asm volatile(
+            "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+            : "=r"(c[j][0]), "=r"(c[j][1]), "=r"(c[j][2]), "=r"(c[j][3]), "=r"(c[j][4]),
+              "=r"(c[j][5]), "=r"(c[j][6]), "=r"(c[j][7])
+            : "l"(p.w_codes + n[j] * row_bytes + g4v[j] * 32));
+        sf4[j] = __ldg(reinterpret_cast<const uint32_t *>(
+            p.w_sf + 512 * ((n[j] >> 7) * p.w_sf_katoms + g4v[j]) + 16 * (n[j] & 31) +
+            4 * ((n[j] & 127) >> 5)));
       }
     }
 #pragma unroll
-    for (int m = 0; m < MX; ++m)
+    for (int j = 0; j < kRows; ++j) {
+      float acc[MX];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-    if (lane < MX) {
-      float v = acc[0];
+      for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
+      if (g4v[j] >= 0) {
 #pragma unroll
-      for (int m = 1; m < MX; ++m)
-        if (lane == m) v = acc[m];
-      if (nchunks == 1) {
-        const float y = __fmul_rn(v, alpha);
-        if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n] = y;
-        else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n] = __float2bfloat16_rn(y);
-      } else {
-        partial[(kc * MX + lane) * p.N + n] = v;
+        for (int bb = 0; bb < 4; ++bb) {
+          const float sw = e4m3_to_f32((sf4[j] >> (8 * bb)) & 0xFF);
+          uint32_t wh[8];   // wh[i] = elements 2i, 2i+1 of the block (same order as X)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            wh[i] = e2m1x2_to_h2(c[j][2 * bb] >> (8 * i));
+            wh[4 + i] = e2m1x2_to_h2(c[j][2 * bb + 1] >> (8 * i));
+          }
+          const int64_t b = g4v[j] * 4 + bb;
+#pragma unroll
+          for (int m = 0; m < MX; ++m) {
+            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2) + b * 8);
+            const uint4 x0 = xp[0], x1 = xp[1];
+            const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            __half2 s2 = __float2half2_rn(0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              s2 = __hfma2(*reinterpret_cast<const __half2 *>(&wh[i]),
+                           *reinterpret_cast<const __half2 *>(&xv[i]), s2);
+            const float dot = __fadd_rn(__low2float(s2), __high2float(s2));
+            acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + b]), acc[m]);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < MX; ++m)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+      const int64_t u = u0 + j;
+      if (u < units && lane < MX) {
+        float v = acc[0];
+#pragma unroll
+        for (int m = 1; m < MX; ++m)
+          if (lane == m) v = acc[m];
+        const int64_t kc = u / p.N;
+        if (nchunks == 1) {
+          const float y = __fmul_rn(v, alpha);
+          if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n[j]] = y;
+          else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n[j]] = __float2bfloat16_rn(y);
+        } else {
+          partial[(kc * MX + lane) * p.N + n[j]] = v;
+        }
       }
     }
   }
@@ -184,8 +204,8 @@ static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, 
   const int nchunks = gemv_chunks(p.K);
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX>, kGemvThreads, smem);
-  per_sm = std::max(1, std::min(per_sm, 4));
-  const int64_t warps_needed = (p.N * nchunks + 7) / 8;
+  per_sm = std::max(1, std::min(per_sm, 8));
+  const int64_t warps_needed = (p.N * nchunks + 8 * kRows - 1) / (8 * kRows);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, warps_needed));
   k_gemv<MX><<<grid, kGemvThreads, smem, st>>>(p, nchunks, partial);
   cudaError_t e = cudaGetLastError();

@@ -17,12 +17,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ void record_timeout(int *status) {
   if (status) atomicExch(status, kStatusTimeout);
 }
@@ -54,15 +48,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete.  The budget
+// is counted on the SM's cycle counter (cheap to read, unlike %globaltimer):
+// two cycles per nanosecond, an upper bound of the SM clock, so the wait
+// lasts at most about timeout_ns at full clock and proportionally longer at
+// lower clocks -- bounded either way.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const uint64_t limit = timeout_ns > (1ull << 62) ? (1ull << 63) : timeout_ns * 2;
+  const uint64_t t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 16; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > timeout_ns) return false;
+    if ((uint64_t)(clock64() - t0) > limit) return false;
   }
 }
 
