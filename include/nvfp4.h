@@ -111,6 +111,32 @@ nvfp4_status nvfp4_quantize(const nvfp4_quant_args *args, nvfp4_stream stream);
 size_t nvfp4_quantize_workspace_bytes(const nvfp4_quant_args *args);
 
 /* ------------------------------------------------------------------------ *
+ * nvfp4_quantize_noalloc -- nvfp4_quantize for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this entry point; it serves callers that
+ * hold no device allocator at the point of the call -- for example a plugin or
+ * custom-op hook that receives only its input and output pointers and must not
+ * allocate there (an allocation could synchronize the device or fall outside
+ * the host framework's memory accounting), or a statically planned memory
+ * layout with no slot for per-call scratch.
+ *
+ * Same arguments, results and requirements as nvfp4_quantize, except that
+ * `workspace` and `workspace_bytes` are ignored and nothing is allocated: the
+ * scratch the dynamic global scale needs (one 32-bit word per (matrix, part),
+ * min(rows, 512) parts per matrix) lives in a 64 KiB array inside the library
+ * (16384 words), present on every GPU that loads the library until the
+ * process exits.  Returns NVFP4_ERR_WORKSPACE, before any device work, when
+ * batch * min(rows, 512) exceeds 16384 (static global scales need none).
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * on a device share the array and it keeps the last call's contents (every
+ * word a call reads is first written by that call, so nothing needs
+ * clearing); calls that overlap on the GPU (different streams, no ordering)
+ * race on it.
+ * ------------------------------------------------------------------------ */
+nvfp4_status nvfp4_quantize_noalloc(const nvfp4_quant_args *args, nvfp4_stream stream);
+
+/* ------------------------------------------------------------------------ *
  * nvfp4_gemm -- D = (g_a*g_b) * sum_k (a_k*sfa)(b_k*sfb)  [+ LoRA]
  *
  * The W4A4 product of "Kernel choice" on tcgen05 block-scaled MMA

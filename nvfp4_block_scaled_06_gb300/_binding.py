@@ -25,7 +25,7 @@ EXPORTS = [
     "nvfp4_gemm_workspace_bytes", "nvfp4_grouped_gemm", "nvfp4_grouped_workspace_bytes",
     "nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", "nvfp4_codes_bytes",
     "nvfp4_sf_bytes", "nvfp4_status_string", "nvfp4_read_device_status",
-    "nvfp4_set_wait_timeout_ns", "nvfp4_version",
+    "nvfp4_set_wait_timeout_ns", "nvfp4_version", "nvfp4_quantize_noalloc",
 ]
 
 
@@ -112,6 +112,8 @@ def load(path: str | None = None):
         w = getattr(lib, wsq)
         w.argtypes = [C.POINTER(st)]
         w.restype = C.c_size_t
+    lib.nvfp4_quantize_noalloc.argtypes = [C.POINTER(QuantArgs), vp]
+    lib.nvfp4_quantize_noalloc.restype = C.c_int
     lib.nvfp4_codes_bytes.argtypes = [C.c_int64, C.c_int64]
     lib.nvfp4_codes_bytes.restype = C.c_size_t
     lib.nvfp4_sf_bytes.argtypes = [C.c_int64, C.c_int64, C.c_int32]

@@ -660,6 +660,25 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 }
 }  // namespace nvfp4
 
+namespace nvfp4 {
+// nvfp4_quantize with the amax scratch supplied by the caller of this function
+// (the workspace-free entry point); `words` is the scratch capacity.
+nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scratch, size_t words,
+                                        cudaStream_t st) {
+  nvfp4_status s = validate_quantize(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  QuantPlan pl;
+  if (!a->global_scale_in) {
+    pl.nparts = amax_parts_for(a->rows);
+    if ((size_t)a->batch * (size_t)pl.nparts > words) return NVFP4_ERR_WORKSPACE;
+    pl.amax = scratch;
+  }
+  return run_quantize(a, pl, d.sms, st);
+}
+}  // namespace nvfp4
+
 // =============================================================== C ABI ==
 extern "C" {
 

@@ -8,6 +8,8 @@
 
 #include <algorithm>
 
+#include "../../include/nvfp4.h"
+
 namespace nvfp4 {
 
 // ------------------------------------------------------------- quantization --
@@ -33,6 +35,9 @@ struct QuantParams {
 };
 
 int amax_parts_for(int64_t rows);
+// The quantize path with caller-supplied amax scratch of `words` 32-bit words.
+nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scratch, size_t words,
+                                        cudaStream_t st);
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
