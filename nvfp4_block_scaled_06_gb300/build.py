@@ -37,17 +37,24 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int = 8) -> str:
-    """Compile (if stale) and return the path of libnvfp4.so."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int = 8,
+          defines=(), lib_path: str | None = None, build_dir: str | None = None) -> str:
+    """Compile (if stale) and return the path of libnvfp4.so.
+
+    ``defines`` adds -D flags (e.g. NVFP4_WAIT_STATS for the wait-statistics
+    build); such variants go to their own ``lib_path`` / ``build_dir``."""
+    lib_out = lib_path or LIB
+    bdir = build_dir or BUILD
+    os.makedirs(bdir, exist_ok=True)
+    dflags = [f"-D{d}" for d in defines]
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "nvfp4.h")]
     cc = nvcc()
 
     def compile_one(src):
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if _stale(o, [s] + hdrs):
-            cmd = [cc, *ARCH, *FLAGS, "-c", s, "-o", o]
+            cmd = [cc, *ARCH, *FLAGS, *dflags, "-c", s, "-o", o]
             if ptxas_verbose:
                 cmd += ["-Xptxas", "-v"]
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,12 +66,12 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int = 8) -> 
 
     with ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if _stale(LIB, objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-Xcompiler", "-fPIC"]
+    if _stale(lib_out, objs):
+        cmd = [cc, *ARCH, "-shared", "-o", lib_out, *objs, "-Xcompiler", "-fPIC"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    return LIB
+    return lib_out
 
 
 if __name__ == "__main__":  # pragma: no cover

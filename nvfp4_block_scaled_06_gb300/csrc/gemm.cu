@@ -20,14 +20,17 @@
 //   warps 2..5  epilogue: tcgen05.ld -> * g_a g_b -> bf16/fp32 -> global.
 // Every mbarrier wait is bounded; on expiry the CTA records a timeout, waits
 // for its own copies and MMAs in flight, frees TMEM and exits.
+#include <cstdlib>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace nvfp4 {
 
 constexpr int kBM = 128;
-constexpr int kEpiWarps = 8;                       // two per TMEM lane quarter
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
+constexpr int kSfWarps = 4;                        // scale-factor writers, one per lane quarter
+constexpr int kEpiWarps = 4;                       // accumulator drain, one per lane quarter
+constexpr int kGemmThreads = 64 + 32 * (kSfWarps + kEpiWarps);
 constexpr uint64_t kDrainNs = 200000000ull;
 
 template <int BN>
@@ -87,6 +90,19 @@ __device__ __forceinline__ float acc_scale(const float *g_a, const float *g_b, i
   return acc_scale_of(g_a ? *g_a : 1.0f, g_b ? g_b[e] : 1.0f);
 }
 
+// Optional wait statistics (compile with -DNVFP4_WAIT_STATS): cycles each role
+// spends in waits, summed over CTAs into 64-bit counters at byte 64 of the
+// workspace (the status word's reserved block).  Off in normal builds.
+#ifdef NVFP4_WAIT_STATS
+#define WSTAT_T0() const long long _ws_t0 = clock64()
+#define WSTAT_ADD(p, i) \
+  atomicAdd(reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>((p).status) + 64) + (i), \
+            (unsigned long long)(clock64() - _ws_t0))
+#else
+#define WSTAT_T0() (void)0
+#define WSTAT_ADD(p, i) (void)0
+#endif
+
 __device__ __forceinline__ void signal_abort(volatile int *abort_flag, int *status) {
   *abort_flag = 1;
   record_timeout(status);
@@ -99,6 +115,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                const GemmParams p) {
   using C = GemmCfg<BN>;
   constexpr int S = C::kStages;
+#ifdef NVFP4_WAIT_STATS
+  const long long kernel_t0 = clock64();
+#endif
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -107,17 +126,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t *sSFA = sB + S * C::kBBytes;
   uint8_t *sSFB = sSFA + S * C::kSfaBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + S * C::kSfbBytes);
-  uint64_t *full = bars, *empty = bars + S;
-  uint64_t *acc_full = bars + 2 * S, *acc_empty = acc_full + 1, *drain = acc_full + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 3);
+  uint64_t *full = bars, *empty = bars + S, *sfready = bars + 2 * S;
+  uint64_t *acc_full = bars + 3 * S, *acc_empty = acc_full + 1, *drain = acc_full + 2;
+  uint64_t *never = acc_full + 3;          // test hook: a barrier nothing arrives at
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 4);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  uint64_t *never = acc_full + 4;          // test hook: a barrier nothing arrives at
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sfready[s], kSfWarps);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiWarps);
@@ -151,6 +171,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
+      // Every per-stage address is a precomputed base plus a constant: this
+      // single thread issues ~6 operations per 256-wide K step.
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      const uint32_t sfa_base = smem_u32(sSFA), sfb_base = smem_u32(sSFB);
+      const uint32_t full_base = smem_u32(full), empty_base = smem_u32(empty);
+      const int last_nk = p.nk64 - (p.num_kt - 1) * 4;    // K steps of the last K tile
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;   // bit s: stage s has an outstanding fill
@@ -159,36 +185,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
         const int kt0 = (u % ksplit) * kt_per;
         const int kt1 = min(p.num_kt, kt0 + kt_per);
-        for (int kk = kt0; kk < kt1 + p.lora_steps; ++kk) {
-          const int kt = kk < kt1 ? kk : p.num_kt + (kk - kt1);   // LoRA steps follow the FP4 range
-          if (*abort_flag || !mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns)) {
+        const int64_t chunk0 = ti.b_row0 >> 7;
+        int chunks = 0;
+#pragma unroll
+        for (int c = 0; c < C::kSfbChunks; ++c)
+          if (chunk0 + c < p.b_sf_row_chunks) chunks = c + 1;
+        const int a_row = (int)ti.a_row0, b_row = (int)ti.b_row0;
+        const uint8_t *sfa_src = p.a_sf + 512 * ((ti.a_row0 >> 7) * p.a_sf_katoms + (int64_t)kt0 * 4);
+        const uint8_t *sfb_src = p.b_sf + 512 * (chunk0 * p.b_sf_katoms + (int64_t)kt0 * 4);
+        const int64_t sfb_chunk_stride = 512 * p.b_sf_katoms;
+        const int nsteps = (kt1 - kt0) + p.lora_steps;
+        for (int i = 0; i < nsteps; ++i) {
+          const int kt = kt0 + i;
+          const uint32_t fb = full_base + 8 * stage;
+          WSTAT_T0();
+          const bool got = !*abort_flag && mbar_wait_u(empty_base + 8 * stage, phase ^ 1, p.timeout_ns);
+          WSTAT_ADD(p, 0);
+          if (!got) {
             signal_abort(abort_flag, p.status);
             ok = false;
             break;
           }
-          if (kt < p.num_kt) {
-            const int nk = min(4, p.nk64 - kt * 4);
-            int chunks = 0;
-            const int64_t chunk0 = ti.b_row0 >> 7;
-#pragma unroll
-            for (int c = 0; c < C::kSfbChunks; ++c)
-              if (chunk0 + c < p.b_sf_row_chunks) chunks = c + 1;
-            const uint32_t bytes = C::kABytes + C::kBBytes + nk * 512 + chunks * nk * 512;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kt * 128, (int)ti.a_row0);
-            tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kt * 128, (int)ti.b_row0);
-            bulk_load(sSFA + stage * C::kSfaBytes,
-                      p.a_sf + 512 * ((ti.a_row0 >> 7) * p.a_sf_katoms + kt * 4), nk * 512,
-                      &full[stage]);
-            for (int c = 0; c < chunks; ++c)
-              bulk_load(sSFB + stage * C::kSfbBytes + c * 2048,
-                        p.b_sf + 512 * ((chunk0 + c) * p.b_sf_katoms + kt * 4), nk * 512,
-                        &full[stage]);
+          const uint32_t a_dst = a_base + stage * C::kABytes, b_dst = b_base + stage * C::kBBytes;
+          if (kt < kt1) {
+            const int nk = kt == p.num_kt - 1 ? last_nk : 4;
+            const uint32_t sfb = nk * 512;
+            mbar_arrive_expect_tx_u(fb, C::kABytes + C::kBBytes + sfb * (1 + chunks));
+            tma_load_2d_u(a_dst, &tmA, fb, kt * 128, a_row);
+            tma_load_2d_u(b_dst, &tmB, fb, kt * 128, b_row);
+            bulk_load_u(sfa_base + stage * C::kSfaBytes, sfa_src, sfb, fb);
+            bulk_load_u(sfb_base + stage * C::kSfbBytes, sfb_src, sfb, fb);
+            if (C::kSfbChunks > 1 && chunks > 1)
+              bulk_load_u(sfb_base + stage * C::kSfbBytes + 2048, sfb_src + sfb_chunk_stride, sfb, fb);
+            sfa_src += 2048;
+            sfb_src += 2048;
           } else {
-            const int ls = kt - p.num_kt;
-            mbar_arrive_expect_tx(&full[stage], C::kABytes + C::kBBytes);
-            tma_load_2d(sA + stage * C::kABytes, &tmT, &full[stage], ls * 64, (int)ti.a_row0);
-            tma_load_2d(sB + stage * C::kBBytes, &tmLB, &full[stage], ls * 64, (int)ti.b_row0);
+            const int ls = kt - kt1;
+            mbar_arrive_expect_tx_u(fb, C::kABytes + C::kBBytes);
+            tma_load_2d_u(a_dst, &tmT, fb, ls * 64, a_row);
+            tma_load_2d_u(b_dst, &tmLB, fb, ls * 64, b_row);
           }
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -207,6 +242,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_nvfp4(kBM, BN);
       const uint32_t idesc_l = idesc_bf16(kBM, BN);
+      // stage-0 descriptors; a stage adds its byte offset / 16 to the address field
+      const uint64_t adesc0 = sdesc_k_sw128(sA), bdesc0 = sdesc_k_sw128(sB);
+      const uint32_t sfr_base = smem_u32(sfready), empty_base = smem_u32(empty);
+      const uint32_t accf = smem_u32(acc_full), acce = smem_u32(acc_empty);
+      const int last_nk = p.nk64 - (p.num_kt - 1) * 4;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -218,40 +258,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
         const int kt0 = (u % ksplit) * kt_per;
         const int kt1 = min(p.num_kt, kt0 + kt_per);
-        if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1, p.timeout_ns)) {
+        WSTAT_T0();
+        const bool got_acc = !*abort_flag && mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns);
+        WSTAT_ADD(p, 2);
+        if (!got_acc) {
           signal_abort(abort_flag, p.status);
           break;
         }
         tc_fence_after();
         uint32_t accumulate = 0;
         const uint32_t sfb_lane_col = (uint32_t)((ti.b_row0 & 127) >> 5);
-        for (int kk = kt0; kk < kt1 + p.lora_steps; ++kk) {
-          const int kt = kk < kt1 ? kk : p.num_kt + (kk - kt1);
-          if (*abort_flag || !mbar_wait(&full[stage], phase, p.timeout_ns)) {
+        const int nsteps = (kt1 - kt0) + p.lora_steps;
+        for (int i = 0; i < nsteps; ++i) {
+          const int kt = kt0 + i;
+          WSTAT_T0();
+          // the stage's operands have landed and its scales are in tensor memory
+          const bool got = !*abort_flag && mbar_wait_u(sfr_base + 8 * stage, phase, p.timeout_ns);
+          WSTAT_ADD(p, 1);
+          if (!got) {
             signal_abort(abort_flag, p.status);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_k_sw128(sA + stage * C::kABytes);
-          const uint64_t bdesc = sdesc_k_sw128(sB + stage * C::kBBytes);
-          if (kt < p.num_kt) {
-            const int nk = min(4, p.nk64 - kt * 4);
+          const uint64_t adesc = adesc0 + (uint64_t)((stage * C::kABytes) >> 4);
+          const uint64_t bdesc = bdesc0 + (uint64_t)((stage * C::kBBytes) >> 4);
+          if (kt < kt1) {
+            const int nk = kt == p.num_kt - 1 ? last_nk : 4;
             const uint32_t sfa_col = tmem + BN + stage * C::kSfColsPerStage;
             const uint32_t sfb_col = sfa_col + 16;
-            const int64_t chunk0 = ti.b_row0 >> 7;
-            for (int j = 0; j < nk; ++j) {
-              tc_cp_32x128b_x4(sfa_col + 4 * j, sdesc_sf_atom(sSFA + stage * C::kSfaBytes + 512 * j));
 #pragma unroll
-              for (int c = 0; c < C::kSfbChunks; ++c)
-                if (chunk0 + c < p.b_sf_row_chunks)
-                  tc_cp_32x128b_x4(sfb_col + j * C::kSfbColsPerK + 4 * c,
-                                   sdesc_sf_atom(sSFB + stage * C::kSfbBytes + c * 2048 + 512 * j));
-            }
-            for (int j = 0; j < nk; ++j) {
-              tc_mma_nvfp4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col + 4 * j,
-                           sfb_col + j * C::kSfbColsPerK + sfb_lane_col, accumulate);
-              accumulate = 1;
+            for (int j = 0; j < 4; ++j) {
+              if (j < nk) {
+                tc_mma_nvfp4(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col + 4 * j,
+                             sfb_col + j * C::kSfbColsPerK + sfb_lane_col, accumulate);
+                accumulate = 1;
+              }
             }
           } else {
 #pragma unroll
@@ -260,124 +302,186 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               accumulate = 1;
             }
           }
-          tc_commit(&empty[stage]);
+          tc_commit_u(empty_base + 8 * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit_u(accf);
         acc_phase ^= 1;
       }
-      // all MMAs and copies issued by this thread complete before TMEM is freed
+      // all MMAs issued by this thread complete before TMEM is freed
       tc_commit(drain);
       mbar_wait(drain, 0, kDrainNs);
     }
+  } else if (warp < 2 + kSfWarps) {
+    // --------------------------------------------------- scales -> tensor memory --
+    // Warp w writes TMEM lane quarter (w % 4).  Lane i of every quarter gets
+    // line i of each 128x4 scale atom (rows i, i+32, i+64, i+96), so each
+    // quarter holds the whole atom: per k-step, the A scales in 4 columns and
+    // the B scales in 4 columns per 128-row chunk -- the layout the block-scaled
+    // MMA reads (the same one tcgen05.cp .32x128b.warpx4 produces).
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + BN;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+      const int kt0 = (u % ksplit) * kt_per;
+      const int kt1 = min(p.num_kt, kt0 + kt_per);
+      const int nsteps = (kt1 - kt0) + p.lora_steps;
+      for (int i = 0; i < nsteps; ++i) {
+        if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(&full[stage], phase, p.timeout_ns))) {
+          if (lane == 0) signal_abort(abort_flag, p.status);
+          ok = false;
+          break;
+        }
+        if (kt0 + i < kt1) {
+          const uint4 *fa = reinterpret_cast<const uint4 *>(sSFA + stage * C::kSfaBytes) + lane;
+          const uint4 *fb = reinterpret_cast<const uint4 *>(sSFB + stage * C::kSfbBytes) + lane;
+          uint32_t v[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 w = fa[32 * j];              // atom j, line `lane`
+            v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+          }
+          tmem_st_32x32b_x16(tq + stage * C::kSfColsPerStage, v);
+#pragma unroll
+          for (int h = 0; h < C::kSfbChunks; ++h) {
+            // columns 16 + 16h .. : k-steps 2h', 2h'+1 for BN=256 (8 columns per k-step)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int col = 16 * h + 4 * t;        // column offset inside the B region
+              const int j = col / C::kSfbColsPerK, c = (col % C::kSfbColsPerK) / 4;
+              const uint4 w = fb[128 * c + 32 * j];  // chunk c (2048 B), atom j (512 B)
+              v[4 * t] = w.x; v[4 * t + 1] = w.y; v[4 * t + 2] = w.z; v[4 * t + 3] = w.w;
+            }
+            tmem_st_32x32b_x16(tq + stage * C::kSfColsPerStage + 16 + 16 * h, v);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[stage]);
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue --
-    // Warp w reads TMEM lane quarter (w % 4) and half (w - 2) / 4 of the BN
-    // columns: all of its accumulator columns are loaded into registers, the
-    // accumulator is released to the MMA warp, then the values are scaled,
-    // converted and stored while the next tile's MMAs run.
-    constexpr int kCh = BN / 64;            // 32-column chunks per thread
+    // Warp w drains TMEM lane quarter (w % 4): each thread owns one accumulator
+    // row, loads it in two halves and releases the accumulator after the second
+    // half's loads, so the next tile's MMAs overlap the remaining stores.
+    constexpr int kCh = BN / 64;            // 32-column chunks per half
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;            // accumulator row owned by this thread
     uint32_t acc_phase = 0;
     float sq = 0.0f;
     for (int u = blockIdx.x; u < num_tiles; u += gridDim.x) {
       const TileInfo ti = decode_tile<BN>(p, u / ksplit, nmt);
       const int ks = u % ksplit;
+      WSTAT_T0();
       // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
-      if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(acc_full, acc_phase, p.timeout_ns))) {
+      const bool got_full = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(acc_full, acc_phase, p.timeout_ns));
+      if (warp == 2 + kSfWarps && lane == 0) WSTAT_ADD(p, 3);
+      if (!got_full) {
         if (lane == 0) signal_abort(abort_flag, p.status);
         break;
       }
       tc_fence_after();
-      uint32_t v[kCh][32];
-#pragma unroll
-      for (int c = 0; c < kCh; ++c)
-        tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (half * kCh + c) * 32, v[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
-      acc_phase ^= 1;
-
       const float alpha = p.accumulate_d ? 1.0f : acc_scale(p.g_a, p.g_b, ti.e);
-      if (r >= ti.valid_rows) continue;
+      const bool row_ok = r < ti.valid_rows;
       const int64_t orow = ti.out_row0 + r;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[kCh][32];
+        __syncwarp();
 #pragma unroll
-      for (int c = 0; c < kCh; ++c) {
-        const int64_t n = ti.n0 + (half * kCh + c) * 32;
-        if (n >= p.N) break;
-        float f[32];
+        for (int c = 0; c < kCh; ++c)
+          tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (half * kCh + c) * 32, v[c]);
+        tmem_ld_wait();
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (!row_ok) continue;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(__uint_as_float(v[c][i]), alpha);
-        const bool full_chunk = n + 32 <= p.N;
-        const int nvalid = full_chunk ? 32 : (int)(p.N - n);
-        if (p.partial) {
-          float *dst = p.partial + ((int64_t)ks * p.M + orow) * p.N + n;
+        for (int c = 0; c < kCh; ++c) {
+          const int64_t n = ti.n0 + (half * kCh + c) * 32;
+          if (n >= p.N) break;
+          float f[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < nvalid) dst[i] = f[i];
-        } else if (p.out_fp32) {
-          float *dst = reinterpret_cast<float *>(p.d) + orow * p.ldd + n;
-          if (p.accumulate_d) {
+          for (int i2 = 0; i2 < 32; ++i2) f[i2] = __fmul_rn(__uint_as_float(v[c][i2]), alpha);
+          const bool full_chunk = n + 32 <= p.N;
+          const int nvalid = full_chunk ? 32 : (int)(p.N - n);
+          if (p.partial) {
+            float *dst = p.partial + ((int64_t)ks * p.M + orow) * p.N + n;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                sq += f[i] * f[i];
-                dst[i] = dst[i] + f[i];
-              }
-          } else if (full_chunk) {
+            for (int i2 = 0; i2 < 32; ++i2)
+              if (i2 < nvalid) dst[i2] = f[i2];
+          } else if (p.out_fp32) {
+            float *dst = reinterpret_cast<float *>(p.d) + orow * p.ldd + n;
+            if (p.accumulate_d) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4 *>(dst + i) = make_float4(f[i], f[i + 1], f[i + 2], f[i + 3]);
-            if (p.sqnorm)
+              for (int i2 = 0; i2 < 32; ++i2)
+                if (i2 < nvalid) {
+                  sq += f[i2] * f[i2];
+                  dst[i2] = dst[i2] + f[i2];
+                }
+            } else if (full_chunk) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) sq += f[i] * f[i];
-          } else {
+              for (int i2 = 0; i2 < 32; i2 += 4)
+                *reinterpret_cast<float4 *>(dst + i2) = make_float4(f[i2], f[i2 + 1], f[i2 + 2], f[i2 + 3]);
+              if (p.sqnorm)
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                dst[i] = f[i];
-                sq += f[i] * f[i];
-              }
-          }
-        } else {
-          __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.d) + orow * p.ldd + n;
-          if (p.accumulate_d) {
+                for (int i2 = 0; i2 < 32; ++i2) sq += f[i2] * f[i2];
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                sq += f[i] * f[i];
-                dst[i] = __float2bfloat16_rn(__fadd_rn(__bfloat162float(dst[i]), f[i]));
-              }
-          } else if (full_chunk) {
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-              w[i] = *reinterpret_cast<const uint32_t *>(&h);
+              for (int i2 = 0; i2 < 32; ++i2)
+                if (i2 < nvalid) {
+                  dst[i2] = f[i2];
+                  sq += f[i2] * f[i2];
+                }
             }
-#pragma unroll
-            for (int i = 0; i < 16; i += 4)
-              *reinterpret_cast<uint4 *>(dst + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
-            if (p.sqnorm)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) sq += f[i] * f[i];
           } else {
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.d) + orow * p.ldd + n;
+            if (p.accumulate_d) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                dst[i] = __float2bfloat16_rn(f[i]);
-                sq += f[i] * f[i];
+              for (int i2 = 0; i2 < 32; ++i2)
+                if (i2 < nvalid) {
+                  sq += f[i2] * f[i2];
+                  dst[i2] = __float2bfloat16_rn(__fadd_rn(__bfloat162float(dst[i2]), f[i2]));
+                }
+            } else if (full_chunk) {
+              uint32_t w[16];
+#pragma unroll
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * i2], f[2 * i2 + 1]);
+                w[i2] = *reinterpret_cast<const uint32_t *>(&h2);
               }
+#pragma unroll
+              for (int i2 = 0; i2 < 16; i2 += 4)
+                *reinterpret_cast<uint4 *>(dst + 2 * i2) = make_uint4(w[i2], w[i2 + 1], w[i2 + 2], w[i2 + 3]);
+              if (p.sqnorm)
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) sq += f[i2] * f[i2];
+            } else {
+#pragma unroll
+              for (int i2 = 0; i2 < 32; ++i2)
+                if (i2 < nvalid) {
+                  dst[i2] = __float2bfloat16_rn(f[i2]);
+                  sq += f[i2] * f[i2];
+                }
+            }
           }
         }
       }
+      acc_phase ^= 1;
     }
     if (p.sqnorm) {
 #pragma unroll
@@ -386,6 +490,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   __syncthreads();
+#ifdef NVFP4_WAIT_STATS
+  if (threadIdx.x == 0) {
+    unsigned long long *c = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(p.status) + 64);
+    atomicAdd(c + 4, (unsigned long long)(clock64() - kernel_t0));
+    atomicAdd(c + 5, 1ull);
+  }
+#endif
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -400,7 +511,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 constexpr int kLoraStages = 6;
 constexpr int kLoraThreads = 192;
 
-__host__ __device__ constexpr int lora_stage_bytes(int rank) { return kBM * 128 + rank * 128; }
+// A stage holds two 64-wide K sub-tiles: [X0 | X1 | A0 | A1], X tiles 128 rows x 128 B.
+constexpr int kLoraSub = 2;
+__host__ __device__ constexpr int lora_stage_bytes(int rank) { return kLoraSub * (kBM * 128 + rank * 128); }
 __host__ __device__ constexpr int lora_smem_bytes(int rank, int stages) {
   return stages * lora_stage_bytes(rank) + 256 + 1024;
 }
@@ -451,7 +564,11 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = p.gtiles ? *p.gnum_mtiles : p.tiles_m;
 
+  const int nsteps = (p.num_k64 + kLoraSub - 1) / kLoraSub;   // pipeline stages per tile
+  const uint32_t x_sub = kBM * 128, a_sub = (uint32_t)p.rank * 128;
   if (warp == 0) {
+    const uint32_t sbase = smem_u32(base);
+    const uint32_t full_base = smem_u32(full), empty_base = smem_u32(empty);
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
@@ -462,31 +579,36 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       if (p.row_map) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int32_t s = p.row_map[row0 + lane * 4 + i];
-          src[i] = s < 0 ? 0 : s;
+          const int32_t sr = p.row_map[row0 + lane * 4 + i];
+          src[i] = sr < 0 ? 0 : sr;
         }
       }
-      for (int kt = 0; kt < p.num_k64; ++kt) {
+      for (int st = 0; st < nsteps; ++st) {
         bool good = true;
         if (lane == 0)
-          good = !*abort_flag && mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns);
+          good = !*abort_flag && mbar_wait_u(empty_base + 8 * stage, phase ^ 1, p.timeout_ns);
         good = __shfl_sync(0xffffffffu, good ? 1 : 0, 0) != 0;
         if (!good) {
           if (lane == 0) signal_abort(abort_flag, p.status);
           ok = false;
           break;
         }
-        uint8_t *sx = base + stage * sbytes;
-        uint8_t *sa = sx + kBM * 128;
+        const uint32_t fb = full_base + 8 * stage;
+        const uint32_t sx = sbase + stage * sbytes, sa = sx + kLoraSub * x_sub;
+        const int k64 = st * kLoraSub;
+        const int nsub = min(kLoraSub, p.num_k64 - k64);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], kBM * 128 + p.rank * 128);
-          tma_load_2d(sa, &tmA, &full[stage], kt * 64, a_row);
-          if (!p.row_map) tma_load_2d(sx, &tmX, &full[stage], kt * 64, (int)row0);
+          mbar_arrive_expect_tx_u(fb, nsub * (x_sub + a_sub));
+          for (int j = 0; j < nsub; ++j) {
+            tma_load_2d_u(sa + j * a_sub, &tmA, fb, (k64 + j) * 64, a_row);
+            if (!p.row_map) tma_load_2d_u(sx + j * x_sub, &tmX, fb, (k64 + j) * 64, (int)row0);
+          }
         }
         __syncwarp();
         if (p.row_map)
-          tma_gather4(sx + lane * 4 * 128, &tmX, &full[stage], kt * 64, src[0], src[1], src[2],
-                      src[3]);
+          for (int j = 0; j < nsub; ++j)
+            tma_gather4(base + stage * sbytes + j * x_sub + lane * 4 * 128, &tmX, &full[stage],
+                        (k64 + j) * 64, src[0], src[1], src[2], src[3]);
         if (lane == 0) {
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -498,39 +620,47 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       }
     }
     if (lane == 0)
-      for (int s = 0; s < stages; ++s)
-        if (armed & (1u << s)) mbar_wait(&full[s], (armed_par >> s) & 1, kDrainNs);
+      for (int s2 = 0; s2 < stages; ++s2)
+        if (armed & (1u << s2)) mbar_wait(&full[s2], (armed_par >> s2) & 1, kDrainNs);
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kBM, p.rank);
+      const uint64_t desc0 = sdesc_k_sw128(base);
+      const uint32_t full_base = smem_u32(full), empty_base = smem_u32(empty);
+      const uint32_t accf = smem_u32(acc_full), acce = smem_u32(acc_empty);
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        if (*abort_flag || !mbar_wait(acc_empty, acc_phase ^ 1, p.timeout_ns)) {
+        if (*abort_flag || !mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns)) {
           signal_abort(abort_flag, p.status);
           break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < p.num_k64; ++kt) {
-          if (*abort_flag || !mbar_wait(&full[stage], phase, p.timeout_ns)) {
+        for (int st = 0; st < nsteps; ++st) {
+          if (*abort_flag || !mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns)) {
             signal_abort(abort_flag, p.status);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_k_sw128(base + stage * sbytes);
-          const uint64_t bdesc = sdesc_k_sw128(base + stage * sbytes + kBM * 128);
+          const int nsub = min(kLoraSub, p.num_k64 - st * kLoraSub);
+          const uint64_t sdesc = desc0 + (uint64_t)((stage * sbytes) >> 4);
+          for (int j = 0; j < nsub; ++j) {
+            const uint64_t adesc = sdesc + ((j * x_sub) >> 4);
+            const uint64_t bdesc = sdesc + ((kLoraSub * x_sub + j * a_sub) >> 4);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) tc_mma_bf16(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, (kt | j) != 0);
-          tc_commit(&empty[stage]);
+            for (int q = 0; q < 4; ++q)
+              tc_mma_bf16(tmem, adesc + 2 * q, bdesc + 2 * q, idesc, (st | j | q) != 0);
+          }
+          tc_commit_u(empty_base + 8 * stage);
           if (++stage == stages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc_commit(acc_full);
+        tc_commit_u(accf);
         acc_phase ^= 1;
       }
       tc_commit(drain);
@@ -549,20 +679,23 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       int e = 0;
       if (scan) {
         // max |x| over this warp's 32 rows of every X tile, read from shared memory
-        for (int kt = 0; kt < p.num_k64; ++kt) {
+        for (int st = 0; st < nsteps; ++st) {
           if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(&full[stage], phase, p.timeout_ns))) {
             if (lane == 0) signal_abort(abort_flag, p.status);
             ok = false;
             break;
           }
-          const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + r * 128);
+          const int nsub = min(kLoraSub, p.num_k64 - st * kLoraSub);
+          for (int j = 0; j < nsub; ++j) {
+            const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + j * x_sub + r * 128);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = row[i];
-            m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+            for (int i = 0; i < 8; ++i) {
+              const uint4 v = row[i];
+              m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+              m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+              m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+              m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+            }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
@@ -683,7 +816,10 @@ static cudaError_t launch_bn(const GemmParams &p, const GemmMaps &m, int num_sms
   }
   int64_t tiles = (int64_t)p.tiles_n * (p.gtiles ? 0 : p.tiles_m) * std::max(1, p.ksplit);
   int grid = num_sms;
-  if (!p.gtiles) grid = (int)std::min<int64_t>(tiles, num_sms);
+#ifdef NVFP4_WAIT_STATS
+  if (const char *cap = getenv("NVFP4_GRID_CAP")) grid = std::max(1, std::min(grid, atoi(cap)));
+#endif
+  if (!p.gtiles) grid = (int)std::min<int64_t>(tiles, grid);
   if (grid <= 0) return cudaSuccess;
   k_gemm_fp4<BN><<<grid, kGemmThreads, C::kSmemBytes, st>>>(m.a, m.b, m.t, m.lb, p);
   return cudaGetLastError();
