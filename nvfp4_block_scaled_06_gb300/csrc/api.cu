@@ -86,6 +86,11 @@ size_t sf_swizzled_bytes(int64_t rows, int64_t cols) {
 
 nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
 
+// K ranges of the fused LoRA-down + amax pass (fp32 partials, summed in order
+// by the packing kernel): two ranges put 2x as many SMs on the pass over X.
+// Every range must hold at least one 128-wide stage, so short K uses one.
+int lora_split_for(int64_t K) { return ceil_div(K, 64) >= 8 ? 2 : 1; }
+
 // Records an optional caller-owned cudaEvent_t on the stream (profiling hook).
 cudaError_t mark(void *ev, cudaStream_t st) {
   return ev ? cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), st) : cudaSuccess;
@@ -190,7 +195,8 @@ struct GemmPlan {
   uint32_t *aq_amax = nullptr;
   int aq_nparts = 0;
   __nv_bfloat16 *t = nullptr;   // T' [M][rank]
-  float *t32 = nullptr;         // T [M][rank] fp32 (dynamic X with LoRA: amax in the same pass)
+  float *t32 = nullptr;         // T [lsplit][M][rank] fp32 (dynamic X with LoRA: amax in the same pass)
+  int lsplit = 1;
   int bn = 256, ksplit = 1;
   float *partial = nullptr;     // split-K partials [ksplit][M][N]
 };
@@ -239,8 +245,10 @@ nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
     }
   }
   if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)a->M * a->rank * 2);
-  if (a->lora_a && a->a_bf16 && !a->a_global_scale && !a->lora_x)
-    pl->t32 = c.take<float>((size_t)a->M * a->rank * 4);
+  if (a->lora_a && a->a_bf16 && !a->a_global_scale && !a->lora_x) {
+    pl->lsplit = lora_split_for(a->K);
+    pl->t32 = c.take<float>((size_t)pl->lsplit * a->M * a->rank * 4);
+  }
   const int sms = plan_sms();
   pl->bn = pick_bn(a->M, a->N, sms);
   pl->ksplit = pick_ksplit(a->M, a->N, a->K, pl->bn, sms, a->lora_a != nullptr);
@@ -348,9 +356,11 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
       // packing pass then derives g, quantizes X and rounds T' = bf16(T s)
       lp.amax_part = pl.aq_amax;
       lp.t_f32 = pl.t32;
+      lp.ksplit = pl.lsplit;
       if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
-      q.nparts = std::min(lp.tiles_m, sms);
+      q.nparts = std::min(lp.tiles_m * pl.lsplit, sms);
       q.t_f32 = pl.t32;
+      q.t_splits = pl.lsplit;
       q.t_out = pl.t;
       q.rank = a->rank;
       q.lora_scale = lp.lora_scale;

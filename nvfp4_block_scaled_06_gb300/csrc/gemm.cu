@@ -562,9 +562,11 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int num_tiles = p.gtiles ? *p.gnum_mtiles : p.tiles_m;
+  const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
+  const int num_tiles = (p.gtiles ? *p.gnum_mtiles : p.tiles_m) * ksplit;   // (tile, K range)
+  // K range of a unit, in 64-wide steps, a multiple of the stage width
+  const int k64_per = ((p.num_k64 + ksplit - 1) / ksplit + kLoraSub - 1) / kLoraSub * kLoraSub;
 
-  const int nsteps = (p.num_k64 + kLoraSub - 1) / kLoraSub;   // pipeline stages per tile
   const uint32_t x_sub = kBM * 128, a_sub = (uint32_t)p.rank * 128;
   if (warp == 0) {
     const uint32_t sbase = smem_u32(base);
@@ -572,7 +574,10 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+      const int t = u / ksplit;
+      const int kb = (u % ksplit) * k64_per, ke = min(p.num_k64, kb + k64_per);
+      const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
       const int64_t row0 = p.gtiles ? (int64_t)p.gtiles[t].a_row0 : (int64_t)t * kBM;
       const int a_row = p.gtiles ? p.gtiles[t].expert * p.rank : 0;   // this expert's A
       int32_t src[4] = {0, 0, 0, 0};
@@ -595,8 +600,8 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
         }
         const uint32_t fb = full_base + 8 * stage;
         const uint32_t sx = sbase + stage * sbytes, sa = sx + kLoraSub * x_sub;
-        const int k64 = st * kLoraSub;
-        const int nsub = min(kLoraSub, p.num_k64 - k64);
+        const int k64 = kb + st * kLoraSub;
+        const int nsub = min(kLoraSub, ke - k64);
         if (lane == 0) {
           mbar_arrive_expect_tx_u(fb, nsub * (x_sub + a_sub));
           for (int j = 0; j < nsub; ++j) {
@@ -631,7 +636,9 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+        const int kb = (u % ksplit) * k64_per, ke = min(p.num_k64, kb + k64_per);
+        const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
         if (*abort_flag || !mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns)) {
           signal_abort(abort_flag, p.status);
           break;
@@ -644,7 +651,7 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
             break;
           }
           tc_fence_after();
-          const int nsub = min(kLoraSub, p.num_k64 - st * kLoraSub);
+          const int nsub = min(kLoraSub, ke - (kb + st * kLoraSub));
           const uint64_t sdesc = desc0 + (uint64_t)((stage * sbytes) >> 4);
           for (int j = 0; j < nsub; ++j) {
             const uint64_t adesc = sdesc + ((j * x_sub) >> 4);
@@ -674,7 +681,10 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
     uint32_t phase = 0;
     uint32_t m2 = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
+      const int t = u / ksplit, ks = u % ksplit;
+      const int kb = ks * k64_per, ke = min(p.num_k64, kb + k64_per);
+      const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
       int64_t row0;
       int e = 0;
       if (scan) {
@@ -685,7 +695,7 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
             ok = false;
             break;
           }
-          const int nsub = min(kLoraSub, p.num_k64 - st * kLoraSub);
+          const int nsub = min(kLoraSub, ke - (kb + st * kLoraSub));
           for (int j = 0; j < nsub; ++j) {
             const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + j * x_sub + r * 128);
 #pragma unroll
@@ -733,7 +743,7 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
             if (lane == 0) mbar_arrive(acc_empty);
           }
           if (!row_ok) continue;
-          float4 *dst = reinterpret_cast<float4 *>(p.t_f32 + row * p.rank + c * 32);
+          float4 *dst = reinterpret_cast<float4 *>(p.t_f32 + ((int64_t)ks * p.M + row) * p.rank + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
@@ -845,7 +855,7 @@ cudaError_t launch_lora_down(const LoraDownParams &p, const LoraDownMaps &m, int
     configured_bytes = smem;
   }
   int grid = num_sms;
-  if (!p.gtiles) grid = std::min(p.tiles_m, num_sms);
+  if (!p.gtiles) grid = std::min(p.tiles_m * std::max(1, p.ksplit), num_sms);
   if (grid <= 0) return cudaSuccess;
   k_lora_down<<<grid, kLoraThreads, smem, st>>>(m.x, m.a, p, stages);
   return cudaGetLastError();

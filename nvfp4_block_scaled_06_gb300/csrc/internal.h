@@ -27,7 +27,8 @@ struct QuantParams {
   const int32_t *row_map;             // optional gather: dst row -> src row (<0: skip)
   int64_t dst_rows;                   // rows written by the row packing
   // optional LoRA hand-off: T' = bf16(T * (lora_scale / (g * g_b))) per row
-  const float *t_f32;                 // [dst_rows][rank]
+  const float *t_f32;                 // [t_splits][dst_rows][rank], summed in order
+  int t_splits;
   __nv_bfloat16 *t_out;               // [dst_rows][rank]
   int rank;
   float lora_scale;
@@ -98,6 +99,7 @@ struct LoraDownParams {
   const int32_t *row_map;     // grouped: padded row -> token (gather)
   uint32_t *amax_part;        // optional: per-CTA max |x| magnitude bits of the X tiles read
   float *t_f32;               // optional: write T in fp32 (unscaled) instead of T'
+  int ksplit;                 // with t_f32: K split in ranges, partials [ksplit][M][rank]
   int *status;
   uint64_t timeout_ns;
 };

@@ -184,8 +184,11 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
     if (p.row_map && sr < 0) continue;   // unmapped (padding) rows are left untouched
     if (p.t_f32 && r < p.dst_rows) {
       // LoRA hand-off: the down-projection's fp32 row, scaled and rounded once to bf16
-      for (int j = lane; j < p.rank; j += 32)
-        p.t_out[r * p.rank + j] = __float2bfloat16_rn(__fmul_rn(p.t_f32[r * p.rank + j], t_scale));
+      for (int j = lane; j < p.rank; j += 32) {
+        float t = p.t_f32[r * p.rank + j];
+        for (int k = 1; k < p.t_splits; ++k) t = __fadd_rn(t, p.t_f32[(k * p.dst_rows + r) * p.rank + j]);
+        p.t_out[r * p.rank + j] = __float2bfloat16_rn(__fmul_rn(t, t_scale));
+      }
     }
     const __nv_bfloat16 *srow = src + sr * p.ld;
     for (int64_t blk0 = 0; blk0 < sfc_pad; blk0 += 128) {
