@@ -132,11 +132,18 @@ def mean_ms(pairs):
     return sum(a.elapsed_time(b) for a, b in pairs) / max(1, len(pairs))
 
 
-def time_loop(torch, fn, steps, warmup, prof=None):
-    """Run fn(i) warmup + steps times; return ms/step of the timed steps."""
+def time_loop(torch, fn, steps, warmup, prof=None, queue_ahead=True):
+    """Run fn(i) warmup + steps times; return ms/step of the timed steps.
+
+    With queue_ahead the timed steps are enqueued behind a short GPU sleep, so
+    the host has queued them before the first one starts and the GPU runs them
+    back to back: short kernels (decode) are then timed without the host's
+    per-call launch latency between them, as a pipelined caller would see."""
     for i in range(warmup):
         fn(i, None)
     torch.cuda.synchronize()
+    if queue_ahead:
+        torch.cuda._sleep(int(5e7))          # ~25 ms at 2 GHz: covers enqueueing the steps
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for i in range(steps):
@@ -182,6 +189,15 @@ def run_main(args, torch, nv, device, rank, world):
     if world > 1:
         torch.distributed.barrier()
     with ClockSampler(torch.cuda.current_device()) as clk:
+        # the same step, untimed, for ~0.5 s so that nvidia-smi samples the
+        # clocks under this load; the timed region follows immediately
+        t_end = time.perf_counter() + 0.5
+        i = 0
+        while time.perf_counter() < t_end:
+            step(i, None)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
         ms = time_loop(torch, step, args.steps, 0, prof)
     if world > 1:
         t = torch.tensor([ms], device=device)
@@ -355,6 +371,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--only", choices=["quantize", "decode", "grouped"],
+                    help="run just this secondary workload (for profiling) and print its numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
 
@@ -375,6 +393,13 @@ def main():
     import nvfp4_block_scaled_06_gb300 as nv
     nv.load()
     pk = peaks()
+
+    if args.only:
+        fn = dict(quantize=run_quantize_sweep, decode=run_decode, grouped=run_grouped)[args.only]
+        res = fn(torch, nv, device, args.steps, args.warmup, pk)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, **res}))
+        return
 
     main_res = run_main(args, torch, nv, device, rank, world)
     sec = {}
