@@ -66,8 +66,13 @@ template <int MX>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int64_t K = p.K, nblk = K / 16;
-  uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // [MX][K/2] half2
-  float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // [MX][K/16]
+  // Shared layout chosen so that the 32 lanes of a warp, which take 32
+  // consecutive 64-element groups g4, read consecutive 16-byte words:
+  //   xs  [m][half h][bb][g4] = 4 half2 (elements 8h..8h+7 of block 4*g4 + bb)
+  //   sxs [m][bb][g4]         = E4M3 block scale as fp32
+  const int64_t G4 = K / 64;
+  uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
+  float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
 
   const float g = *p.g_x;
   const float t6g = __fmul_rn(6.0f, g);
@@ -77,10 +82,11 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
     uint32_t h2[8];
     float sx;
     quant_x_block(p.x + m * p.ldx + b * 16, g, t6g, h2, sx);
-    uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2) + b * 8);
-    dst[0] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-    dst[1] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
-    sxs[m * nblk + b] = sx;
+    const int64_t g4 = b >> 2, bb = b & 3;
+    uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2));
+    dst[(0 * 4 + bb) * G4 + g4] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+    dst[(1 * 4 + bb) * G4 + g4] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+    sxs[m * nblk + bb * G4 + g4] = sx;
   }
   __syncthreads();
 
@@ -132,11 +138,10 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
             wh[i] = e2m1x2_to_h2(c[j][2 * bb] >> (8 * i));
             wh[4 + i] = e2m1x2_to_h2(c[j][2 * bb + 1] >> (8 * i));
           }
-          const int64_t b = g4v[j] * 4 + bb;
 #pragma unroll
           for (int m = 0; m < MX; ++m) {
-            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2) + b * 8);
-            const uint4 x0 = xp[0], x1 = xp[1];
+            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2));
+            const uint4 x0 = xp[(0 * 4 + bb) * G4 + g4v[j]], x1 = xp[(1 * 4 + bb) * G4 + g4v[j]];
             const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             __half2 s2 = __float2half2_rn(0.0f);
 #pragma unroll
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
               s2 = __hfma2(*reinterpret_cast<const __half2 *>(&wh[i]),
                            *reinterpret_cast<const __half2 *>(&xv[i]), s2);
             const float dot = __fadd_rn(__low2float(s2), __high2float(s2));
-            acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + b]), acc[m]);
+            acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + bb * G4 + g4v[j]]), acc[m]);
           }
         }
       }

@@ -62,14 +62,84 @@ __device__ __forceinline__ float resolve_global_scale(const QuantParams &p, int 
 struct BlockScale {
   float t6g, g;
   bool gzero;
+  const float *senc;   // per-CTA table: senc[c] = min(1 / fl(E4M3(c) * g), FLT_MAX)
 };
 
-__device__ __forceinline__ BlockScale make_block_scale(float g) {
+// Every thread of the block must call this (it fills a shared table of >= 128
+// floats and synchronizes).  A block's encode scale depends only on its E4M3
+// code, so the reciprocal of each of the 127 possible decode scales is formed
+// once per CTA -- with the same IEEE operations as per block -- and looked up.
+__device__ __forceinline__ BlockScale make_block_scale(float g, float *tab) {
   BlockScale s;
   s.g = g;
   s.t6g = __fmul_rn(6.0f, g);
   s.gzero = !(g > 0.0f);
+  for (int c = threadIdx.x; c < 128; c += blockDim.x)
+    tab[c] = fminf(__frcp_rn(__fmul_rn(e4m3_to_f32((uint32_t)c), g)), FLT_MAX);
+  __syncthreads();
+  s.senc = tab;
   return s;
+}
+
+// max of |x| over the two bf16 halves of each word (sign bits cleared; the bf16
+// maximum of non-negative values is exact).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Eight bf16 pairs times one fp32 scale (one IEEE rounding each), encoded as
+// 16 E2M1 codes: element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint64_t encode16(const uint32_t (&w)[8], float senc) {
+  const uint64_t ss = ((uint64_t)__float_as_uint(senc) << 32) | __float_as_uint(senc);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t x = ((uint64_t)(w[i] & 0xFFFF0000u) << 32) | (uint64_t)(w[i] << 16);
+    uint64_t y;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(ss));
+    v[2 * i] = __uint_as_float((uint32_t)y);
+    v[2 * i + 1] = __uint_as_float((uint32_t)(y >> 32));
+  }
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(out[h])
+        : "f"(v[8 * h]), "f"(v[8 * h + 1]), "f"(v[8 * h + 2]), "f"(v[8 * h + 3]),
+          "f"(v[8 * h + 4]), "f"(v[8 * h + 5]), "f"(v[8 * h + 6]), "f"(v[8 * h + 7]));
+  return (uint64_t)out[0] | ((uint64_t)out[1] << 32);
+}
+
+// Four bf16 pairs times one fp32 scale -> 8 E2M1 codes (element 2i in the low
+// nibble of byte i of the result).
+__device__ __forceinline__ uint32_t encode8(const uint32_t (&w)[4], float senc) {
+  const uint64_t ss = ((uint64_t)__float_as_uint(senc) << 32) | __float_as_uint(senc);
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint64_t x = ((uint64_t)(w[i] & 0xFFFF0000u) << 32) | (uint64_t)(w[i] << 16);
+    uint64_t y;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(y) : "l"(x), "l"(ss));
+    v[2 * i] = __uint_as_float((uint32_t)y);
+    v[2 * i + 1] = __uint_as_float((uint32_t)(y >> 32));
+  }
+  uint32_t out;
+  asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return out;
 }
 
 // Quantize 16 bf16 values held as 8 words (element 2i in the low half of w[i]).
@@ -77,26 +147,16 @@ __device__ __forceinline__ BlockScale make_block_scale(float g) {
 // E4M3 scale byte.
 __device__ __forceinline__ uint64_t quant16(const uint32_t (&w)[8], const BlockScale &s,
                                             uint32_t &sf_out) {
-  uint32_t m2 = 0;
+  uint32_t m2 = w[0] & 0x7FFF7FFFu;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+  for (int i = 1; i < 8; ++i) m2 = bmax2(m2, w[i] & 0x7FFF7FFFu);
   const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
   const float bamax = __uint_as_float(mb << 16);
   uint32_t sb = 0;
   if (!s.gzero) sb = cvt_e4m3(__fdiv_rn(bamax, s.t6g));
   sf_out = sb;
   if (sb == 0) return 0ull;
-  const float sdec = __fmul_rn(e4m3_to_f32(sb), s.g);
-  const float senc = fminf(__frcp_rn(sdec), FLT_MAX);
-  uint32_t lo = 0, hi = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    lo |= cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc)) << (8 * i);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    hi |= cvt_e2m1x2(__fmul_rn(bf16lo(w[4 + i]), senc), __fmul_rn(bf16hi(w[4 + i]), senc))
-          << (8 * i);
-  return (uint64_t)lo | ((uint64_t)hi << 32);
+  return encode16(w, s.senc[sb]);
 }
 
 template <bool kV8>
@@ -161,10 +221,11 @@ __global__ void __launch_bounds__(256) k_amax_partial(QuantParams p) {
 template <bool kV8>
 __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   __shared__ uint32_t scratch[32];
+  __shared__ float senc_tab[128];
   const int b = blockIdx.y;
   const float g = resolve_global_scale(p, b, scratch);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) p.g_out[b] = g;
-  const BlockScale s = make_block_scale(g);
+  const BlockScale s = make_block_scale(g, senc_tab);
 
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -230,107 +291,126 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
 }
 
 // ------------------------------------------------- tiled col (+row) packing --
-// A CTA quantizes 64x64 tiles of one matrix: the tile is staged in shared
-// memory; each thread quantizes one 16-element row block from registers (row
-// packing) and one 16-element column block from shared memory (column
-// packing).  Requires rows % 16 == 0 for the column packing.
-constexpr int kTile = 64;
+// A CTA quantizes 64 x 128 tiles of one matrix (grid-stride over tiles).  Each
+// thread loads two 16-element row blocks (64 contiguous bytes) and packs them
+// from registers (row packing); the tile is staged in shared memory, where each
+// thread reads two adjacent columns per 32-bit load and packs one 16-row block
+// of each (column packing).  Requires rows % 16 == 0 for the column packing.
+constexpr int kTR = 64, kTC = 128;
 
 __global__ void __launch_bounds__(256) k_quant_tiles(QuantParams p) {
   __shared__ uint32_t scratch[32];
-  __shared__ __align__(16) __nv_bfloat16 tile[kTile][kTile];
-  __shared__ uint8_t sfcol[kTile][4];
+  __shared__ float senc_tab[128];
+  __shared__ __align__(16) uint32_t tile[kTR][kTC / 2];   // bf16 pairs
+  __shared__ __align__(16) uint8_t sfcol[kTC][4];
   const int b = blockIdx.y;
   const float g = resolve_global_scale(p, b, scratch);
   if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) p.g_out[b] = g;
-  const BlockScale s = make_block_scale(g);
+  const BlockScale s = make_block_scale(g, senc_tab);
 
-  const int t = threadIdx.x, lane = t & 31;
-  const int64_t tiles_r = (p.rows + kTile - 1) / kTile, tiles_c = (p.cols + kTile - 1) / kTile;
+  const int t = threadIdx.x;
+  const int64_t tiles_r = (p.rows + kTR - 1) / kTR, tiles_c = (p.cols + kTC - 1) / kTC;
   const __nv_bfloat16 *src = p.src + (int64_t)b * p.bstride;
   const bool do_row = p.codes_row != nullptr, do_col = p.codes_col != nullptr;
-  // row packing geometry
   const int64_t nblk_r = p.cols / 16, sfc_pad_r = (nblk_r + 3) & ~int64_t(3);
-  // column packing: output matrix is [cols][rows]
   const int64_t nblk_c = p.rows / 16, sfc_pad_c = (nblk_c + 3) & ~int64_t(3);
   uint8_t *codes_r = do_row ? p.codes_row + (int64_t)b * p.codes_row_bstride : nullptr;
   uint8_t *sf_r = do_row ? p.sf_row + (int64_t)b * p.sf_row_bstride : nullptr;
   uint8_t *codes_c = do_col ? p.codes_col + (int64_t)b * p.codes_col_bstride : nullptr;
   uint8_t *sf_c = do_col ? p.sf_col + (int64_t)b * p.sf_col_bstride : nullptr;
+  // Row role: load slot i of warp w covers tile rows 16i + 2w + (lane >> 4);
+  // lane & 15 is the 8-element chunk of that 256-byte row, so a warp-wide
+  // 16-byte load reads two whole rows (fully coalesced).  Lanes 2j, 2j+1 hold
+  // the two halves of 16-element block j of the row.
+  const int warp = t >> 5, lane = t & 31;
+  const int chunk = lane & 15, blk_in_row = chunk >> 1;
+  const int cp = t & 63, crb = t >> 6;        // column role: column pair, 16-row block
 
   for (int64_t tix = blockIdx.x; tix < tiles_r * tiles_c; tix += gridDim.x) {
-    const int64_t r0 = (tix / tiles_c) * kTile, c0 = (tix % tiles_c) * kTile;
-    // load: thread t holds tile row t/4, 16-column block t%4
-    const int tr = t >> 2, tb = t & 3;
-    const int64_t gr = r0 + tr, gc = c0 + tb * 16;
-    uint32_t w[8];
-    const bool in = gr < p.rows && gc < p.cols;
-    if (in) load16<false>(src + gr * p.ld + gc, w);
-    else {
+    const int64_t r0 = (tix / tiles_c) * kTR, c0 = (tix % tiles_c) * kTC;
+    const int64_t gc = c0 + 8 * chunk;
+    uint32_t w[4][4];
+    bool in[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) w[i] = 0;
+    for (int i = 0; i < 4; ++i) {
+      const int64_t gr = r0 + 16 * i + 2 * warp + (lane >> 4);
+      in[i] = gr < p.rows && gc < p.cols;
+      if (in[i]) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + gr * p.ld + gc));
+        w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
+      } else {
+        w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0;
+      }
     }
-    __syncthreads();   // previous tile's column readers are done
-    *reinterpret_cast<uint4 *>(&tile[tr][tb * 16]) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4 *>(&tile[tr][tb * 16 + 8]) = make_uint4(w[4], w[5], w[6], w[7]);
-
+    __syncthreads();   // the previous tile's column readers are done with `tile`
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<uint4 *>(&tile[16 * i + 2 * warp + (lane >> 4)][4 * chunk]) =
+          make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
     if (do_row) {
-      uint32_t sb = 0;
-      uint64_t c = in ? quant16(w, s, sb) : 0ull;
-      if (in)
-        *reinterpret_cast<uint2 *>(codes_r + gr * (p.cols / 2) + gc / 2) =
-            make_uint2((uint32_t)c, (uint32_t)(c >> 32));
-      const int64_t blk = gc / 16;
-      if (p.sf_swizzled) {
-        uint32_t v = sb;
-        v |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
-        v |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
-        v |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
-        if (tb == 0 && gr < p.rows && blk < sfc_pad_r)
-          *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = v;
-      } else if (in) {
-        sf_r[gr * nblk_r + blk] = (uint8_t)sb;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t gr = r0 + 16 * i + 2 * warp + (lane >> 4);
+        // block max over this lane's 8 values and its partner's
+        uint32_t m2 = bmax2(bmax2(w[i][0] & 0x7FFF7FFFu, w[i][1] & 0x7FFF7FFFu),
+                            bmax2(w[i][2] & 0x7FFF7FFFu, w[i][3] & 0x7FFF7FFFu));
+        m2 = bmax2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
+        const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
+        uint32_t sb = 0;
+        if (!s.gzero && in[i]) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(mb << 16), s.t6g));
+        const uint32_t code = sb ? encode8(w[i], s.senc[sb]) : 0u;
+        if (in[i]) *reinterpret_cast<uint32_t *>(codes_r + gr * (p.cols / 2) + gc / 2) = code;
+        const int64_t blk = gc / 16;
+        if (p.sf_swizzled) {
+          // even lanes of each 8-lane group hold blocks 4g .. 4g+3 of the row
+          uint32_t v = sb;
+          v |= __shfl_down_sync(0xffffffffu, sb, 2) << 8;
+          v |= __shfl_down_sync(0xffffffffu, sb, 4) << 16;
+          v |= __shfl_down_sync(0xffffffffu, sb, 6) << 24;
+          if ((lane & 7) == 0 && gr < p.rows && blk < sfc_pad_r)
+            *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = v;
+        } else if (in[i] && (lane & 1) == 0) {
+          sf_r[gr * nblk_r + blk] = (uint8_t)sb;
+        }
+        (void)blk_in_row;
       }
     }
     __syncthreads();
     if (do_col) {
-      // thread t: tile column t%64, row block t/64 (16 rows)
-      const int cc = t & 63, rb = t >> 6;
-      const int64_t oc = c0 + cc;                 // output row (= input column)
-      const int64_t orow_blk = (r0 + rb * 16) / 16;
-      const bool cin = oc < p.cols && r0 + rb * 16 < p.rows;
-      uint32_t cw[8];
+      // columns 2cp, 2cp+1 of the tile, rows 16*crb .. 16*crb+15
+      uint32_t ca[8], cb[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = __bfloat16_as_ushort(tile[rb * 16 + 2 * i][cc]);
-        const uint32_t hi = __bfloat16_as_ushort(tile[rb * 16 + 2 * i + 1][cc]);
-        cw[i] = lo | (hi << 16);
+        const uint32_t w0 = tile[crb * 16 + 2 * i][cp], w1 = tile[crb * 16 + 2 * i + 1][cp];
+        ca[i] = __byte_perm(w0, w1, 0x5410);    // column 2cp: rows 2i, 2i+1
+        cb[i] = __byte_perm(w0, w1, 0x7632);    // column 2cp+1
       }
-      uint32_t sb = 0;
-      const uint64_t c = cin ? quant16(cw, s, sb) : 0ull;
-      if (cin)
-        *reinterpret_cast<uint2 *>(codes_c + oc * (p.rows / 2) + (r0 + rb * 16) / 2) =
-            make_uint2((uint32_t)c, (uint32_t)(c >> 32));
-      if (p.sf_swizzled) {
-        sfcol[cc][rb] = (uint8_t)sb;
-      } else if (cin) {
-        sf_c[oc * nblk_c + orow_blk] = (uint8_t)sb;
-      }
-      __syncthreads();
-      if (p.sf_swizzled && t < kTile) {
-        const int64_t oc2 = c0 + t;
-        const int64_t blk = r0 / 16;    // first of 4 column blocks of this tile
-        if (oc2 < p.cols && blk < sfc_pad_c) {
-          uint32_t v = 0;
+      const int64_t rr = r0 + 16 * crb;         // first input row of the block
+      const bool rin = rr < p.rows;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (r0 + k * 16 < p.rows) v |= (uint32_t)sfcol[t][k] << (8 * k);
-          *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc2, blk, sfc_pad_c)) = v;
+      for (int k = 0; k < 2; ++k) {
+        const int64_t oc = c0 + 2 * cp + k;     // output row (= input column)
+        const bool cin = rin && oc < p.cols;
+        uint32_t sbc = 0;
+        const uint64_t cd = cin ? quant16(k ? cb : ca, s, sbc) : 0ull;
+        if (cin)
+          *reinterpret_cast<uint2 *>(codes_c + oc * (p.rows / 2) + rr / 2) =
+              make_uint2((uint32_t)cd, (uint32_t)(cd >> 32));
+        if (p.sf_swizzled) sfcol[2 * cp + k][crb] = (uint8_t)sbc;
+        else if (cin) sf_c[oc * nblk_c + rr / 16] = (uint8_t)sbc;
+      }
+      if (p.sf_swizzled) {
+        __syncthreads();
+        if (t < kTC) {
+          const int64_t oc2 = c0 + t;
+          const int64_t blk = r0 / 16;          // first of the tile's 4 column blocks
+          if (oc2 < p.cols && blk < sfc_pad_c)
+            *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc2, blk, sfc_pad_c)) =
+                *reinterpret_cast<const uint32_t *>(sfcol[t]);
         }
       }
     }
   }
-  (void)lane;
 }
 
 // Zero the swizzled padding of a scale buffer that the tile kernel does not
@@ -372,9 +452,12 @@ cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st
 }
 
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
-  const int64_t tiles = ((p.rows + kTile - 1) / kTile) * ((p.cols + kTile - 1) / kTile);
-  int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * 8 / std::max<int64_t>(1, p.batch));
-  ctas = std::max<int64_t>(ctas, 1);
+  const int64_t tiles = ((p.rows + kTR - 1) / kTR) * ((p.cols + kTC - 1) / kTC);
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 0);
+  per_sm = std::max(per_sm, 1);
+  // one wave of resident CTAs, shared by the matrices of the batch
+  int64_t ctas = std::min<int64_t>(tiles, std::max<int64_t>(1, (int64_t)num_sms * per_sm / std::max<int64_t>(1, p.batch)));
   dim3 grid((unsigned)ctas, (unsigned)p.batch);
   k_quant_tiles<<<grid, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
