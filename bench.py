@@ -209,7 +209,7 @@ def run_main(args, torch, nv, device, rank, world):
     # end to end: pinned host X in, host Y out, through the same C-ABI call
     e2e = run_e2e(args, torch, nv, device, wq, c, xs[0])
     return dict(ms=ms, gemm_ms=gemm_ms, flops=flops, clocks=clk.summary(), e2e=e2e,
-                launches_per_step=4)
+                launches_per_step=3)   # LoRA-down/amax, packing, GEMM
 
 
 def run_e2e(args, torch, nv, device, wq, c, x_dev):

@@ -574,6 +574,8 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
+    // X is read again by the packing pass right after this one: ask L2 to keep it
+    const uint64_t xpol = l2_policy_evict_last();
     for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
       const int t = u / ksplit;
       const int kb = (u % ksplit) * k64_per, ke = min(p.num_k64, kb + k64_per);
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
           mbar_arrive_expect_tx_u(fb, nsub * (x_sub + a_sub));
           for (int j = 0; j < nsub; ++j) {
             tma_load_2d_u(sa + j * a_sub, &tmA, fb, (k64 + j) * 64, a_row);
-            if (!p.row_map) tma_load_2d_u(sx + j * x_sub, &tmX, fb, (k64 + j) * 64, (int)row0);
+            if (!p.row_map) tma_load_2d_hint_u(sx + j * x_sub, &tmX, fb, (k64 + j) * 64, (int)row0, xpol);
           }
         }
         __syncwarp();
@@ -698,9 +700,13 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
           const int nsub = min(kLoraSub, ke - (kb + st * kLoraSub));
           for (int j = 0; j < nsub; ++j) {
             const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + j * x_sub + r * 128);
+            // The tile is 128-byte swizzled (16-byte chunk c of row r sits at
+            // c ^ (r & 7)); visiting chunks in the order i ^ (r & 7) makes the
+            // eight lanes of each quarter-warp hit eight different chunks
+            // (conflict-free); the max over the row is order-independent.
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              const uint4 v = row[i];
+              const uint4 v = row[i ^ (r & 7)];
               m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
               m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
               m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);

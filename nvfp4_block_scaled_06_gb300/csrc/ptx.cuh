@@ -1,6 +1,6 @@
 // ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA, tcgen05.
 //
-// Every wait here is bounded by a %globaltimer budget.  A wait that runs out
+// Every wait here is bounded by a clock64 budget.  A wait that runs out
 // returns false; the caller records NVFP4_ERR_TIMEOUT in the device status
 // word and leaves its loop, so no kernel in this library can hang the GPU.
 #pragma once
@@ -124,6 +124,25 @@ __device__ __forceinline__ void tma_load_2d_u(uint32_t dst, const CUtensorMap *m
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+// L2 eviction priorities for the cache-hint forms (createpolicy descriptors).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_2d_hint_u(uint32_t dst, const CUtensorMap *m, uint32_t bar,
+                                                   int32_t c0, int32_t c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_load_u(uint32_t dst, const void *src, uint32_t bytes,

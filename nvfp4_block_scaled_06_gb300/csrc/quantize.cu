@@ -160,13 +160,13 @@ __device__ __forceinline__ uint64_t quant16(const uint32_t (&w)[8], const BlockS
 }
 
 template <bool kV8>
-__device__ __forceinline__ void load16(const __nv_bfloat16 *src, uint32_t (&w)[8]) {
+__device__ __forceinline__ void load16(const __nv_bfloat16 *src, uint32_t (&w)[8], uint64_t pol) {
   if (kV8) {
     asm volatile(
-        "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
           "=r"(w[7])
-        : "l"(src));
+        : "l"(src), "l"(pol));
   } else {
     const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
     const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   const int64_t row_bytes = p.cols / 2;
 
   const float t_scale = p.t_f32 ? __fdiv_rn(p.lora_scale, acc_scale_of(g, *p.g_b)) : 0.0f;
+  // last use of the source rows: let L2 drop them first
+  const uint64_t pol = l2_policy_evict_first();
   for (int64_t r = warp; r < rows_out; r += nwarps) {
     int64_t sr = -1;
     if (r < p.dst_rows) sr = p.row_map ? (int64_t)p.row_map[r] : r;
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int64_t blk = blk0 + u * 32 + lane;
-        if (sr >= 0 && blk < nblk) load16<kV8>(srow + blk * 16, w[u]);
+        if (sr >= 0 && blk < nblk) load16<kV8>(srow + blk * 16, w[u], pol);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
