@@ -161,6 +161,8 @@ nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int sm
     p.sf_col_bstride = (int64_t)nvfp4_sf_bytes(a->cols, a->rows, a->sf_layout);
   }
   p.dst_rows = a->rows;
+  p.status = static_cast<int *>(a->workspace);
+  p.timeout_ns = g_timeout_ns.load();
   if (!a->global_scale_in) {
     cudaError_t e = launch_amax(p, st);
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -351,6 +353,8 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     q.sf_row = pl.aq_sf;
     q.sf_swizzled = 1;
     q.dst_rows = a->M;
+    q.status = status;
+    q.timeout_ns = tmo;
     if (pl.t32) {
       // one pass over X forms T = X A^T (fp32) and the amax partials; the
       // packing pass then derives g, quantizes X and rounds T' = bf16(T s)
@@ -512,6 +516,8 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   q.sf_swizzled = 1;
   q.row_map = pl.row_map;
   q.dst_rows = pl.prow_max;
+  q.status = status;
+  q.timeout_ns = tmo;
   if (!a->x_global_scale && launch_amax(q, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   const float *g_x = a->x_global_scale ? a->x_global_scale : pl.g_x;

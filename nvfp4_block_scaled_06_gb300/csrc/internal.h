@@ -33,6 +33,9 @@ struct QuantParams {
   int rank;
   float lora_scale;
   const float *g_b;
+  // in-kernel waits (the staged packing kernel): budget and status word
+  int *status;
+  uint64_t timeout_ns;
 };
 
 int amax_parts_for(int64_t rows);

@@ -292,6 +292,232 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   }
 }
 
+// ------------------------------------------------------ staged row packing --
+// The row packing with the source staged through shared memory by bulk
+// copies.  The work is cut into units (matrix, row, K segment of <= 2048
+// elements); every warp owns a contiguous run of units and a private ring of
+// `slots` shared-memory buffers, and keeps the copies of its next units in
+// flight while it packs the current one (~130 KB of reads outstanding per SM
+// with few registers).  Units are walked with incremental cursors (no
+// integer division per unit).  A lane packs two 16-element blocks per step: 2 x 32
+// bytes from shared memory, 2 x 8 code bytes and two scale bytes out.
+// Same results, bit for bit, as k_quant_rows (the same per-block operations).
+constexpr int kQWarps = 16;
+constexpr uint64_t kQDrainNs = 200000000ull;
+constexpr int64_t kQSegMax = 2048;
+constexpr int kQHeaderBytes = 8704;   // barriers (<= 512 B) + per-warp 128-entry tables
+
+struct StagedCfg {
+  int64_t seg = 0;   // elements per unit (multiple of 64), last segment of a row may be shorter
+  int nseg = 0, slots = 0;
+  size_t smem = 0;
+};
+
+StagedCfg staged_cfg(int64_t cols) {
+  StagedCfg c;
+  c.nseg = (int)((cols + kQSegMax - 1) / kQSegMax);
+  const int64_t per = (cols + c.nseg - 1) / c.nseg;
+  c.seg = (per + 63) / 64 * 64;
+  const int64_t ring = (int64_t)kQWarps * c.seg * 2;
+  c.slots = (int)std::min<int64_t>(4, (224 * 1024 - kQHeaderBytes) / ring);
+  c.smem = (size_t)kQHeaderBytes + (size_t)c.slots * (size_t)ring;
+  return c;
+}
+
+// Global scale of matrix b computed by one warp (same operations as
+// resolve_global_scale).
+__device__ __forceinline__ float warp_global_scale(const QuantParams &p, int64_t b) {
+  if (p.g_in) return p.g_in[b];
+  uint32_t m = 0;
+  for (int i = threadIdx.x & 31; i < p.nparts; i += 32) m = max(m, p.amax_part[b * p.nparts + i]);
+  m = warp_max_u32(m);
+  return __fdiv_rn(__uint_as_float(m << 16), 2688.0f);
+}
+
+// max(|a|, |b|) per bf16 half; the sign bits of the result are not
+// meaningful (cleared by the caller).  Exact for finite inputs.
+__device__ __forceinline__ uint32_t bmaxabs2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// One 16-element block held as two 16-byte halves: `a` = elements 8h..8h+7,
+// `c` = the other half (h = which half `a` is).  Returns the code bytes
+// (element 2i in the low nibble of byte i) and the E4M3 scale.
+__device__ __forceinline__ uint2 pack_block(const uint4 a, const uint4 c, int h, float t6g, bool gzero,
+                                            const float *tab, uint32_t &sb) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
+  const uint32_t m2 = bmaxabs2(bmaxabs2(bmaxabs2(wa[0], wa[1]), bmaxabs2(wa[2], wa[3])),
+                               bmaxabs2(bmaxabs2(wc[0], wc[1]), bmaxabs2(wc[2], wc[3]))) &
+                      0x7FFF7FFFu;
+  const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
+  sb = gzero ? 0u : cvt_e4m3(__fdiv_rn(__uint_as_float(mb << 16), t6g));
+  uint32_t lo = 0, hi = 0;
+  if (sb) {
+    const float senc = tab[sb];
+    const uint32_t ea = encode8(wa, senc), ec = encode8(wc, senc);
+    lo = h ? ec : ea;
+    hi = h ? ea : ec;
+  }
+  return make_uint2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kQWarps * 32, 1)
+    k_quant_rows_staged(const QuantParams p, int64_t seg, int nseg, int slots) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t slot_bytes = seg * 2;
+  uint64_t *full = reinterpret_cast<uint64_t *>(qsm) + warp * slots;
+  float *tab = reinterpret_cast<float *>(qsm + 512) + warp * 128;
+  const uint32_t ring = smem_u32(qsm + kQHeaderBytes) + (uint32_t)(warp * slots * slot_bytes);
+  if (lane == 0) {
+    for (int s = 0; s < slots; ++s) mbar_init(&full[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const int64_t rows_out =
+      (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  const int64_t per_b = rows_out * nseg, U = per_b * p.batch;
+  const int64_t W = (int64_t)gridDim.x * kQWarps, gw = (int64_t)blockIdx.x * kQWarps + warp;
+  // an even split: every warp gets floor(U/W) or ceil(U/W) consecutive units
+  const int64_t u_begin = gw * U / W, u_end = (gw + 1) * U / W;
+  const int64_t nblk = p.cols / 16, sfc_pad = (nblk + 3) & ~int64_t(3);
+  const int64_t row_bytes = p.cols / 2;
+  const uint64_t pol = l2_policy_evict_first();   // last use of the source rows
+
+  // unit -> (matrix, row, segment, source row); source row < 0: nothing to copy
+  auto source_row = [&](int64_t r) -> int64_t {
+    if (r >= p.dst_rows) return -1;
+    return p.row_map ? (int64_t)p.row_map[r] : r;
+  };
+  struct Cursor {
+    int64_t b, r, sg;
+  };
+  auto advance = [&](Cursor &c) {
+    if (++c.sg == nseg) {
+      c.sg = 0;
+      if (++c.r == rows_out) {
+        c.r = 0;
+        ++c.b;
+      }
+    }
+  };
+  Cursor cur;   // the unit being packed
+  cur.b = u_begin / per_b;
+  cur.r = (u_begin % per_b) / nseg;
+  cur.sg = u_begin % nseg;
+  Cursor icur = cur;          // the next unit to copy (lane 0)
+  int64_t inext = u_begin;
+  uint32_t armed = 0, parity = 0;   // per slot: copy in flight / phase to wait for
+  auto issue = [&](int s) {   // lane 0 only: copy unit `inext` into slot s
+    if (inext >= u_end) return;
+    const int64_t sr = source_row(icur.r);
+    if (sr >= 0) {
+      const int64_t c0 = icur.sg * seg, len = seg < p.cols - c0 ? seg : p.cols - c0;
+      const uint32_t bar = smem_u32(&full[s]);
+      mbar_arrive_expect_tx_u(bar, (uint32_t)(len * 2));
+      bulk_load_hint_u(ring + (uint32_t)(s * slot_bytes), p.src + icur.b * p.bstride + sr * p.ld + c0,
+                       (uint32_t)(len * 2), bar, pol);
+      armed |= 1u << s;
+    }
+    ++inext;
+    advance(icur);
+  };
+  if (lane == 0)
+    for (int s = 0; s < slots; ++s) issue(s);
+
+  int64_t cur_b = -1;
+  float g = 0.0f, t6g = 0.0f, t_scale = 0.0f;
+  bool gzero = true;
+  int s = 0;
+  // lanes alternate which 16-byte half of a block they read first, so the
+  // eight lanes of each quarter-warp touch eight different bank groups
+  const int h = (lane >> 2) & 1;
+  for (int64_t u = u_begin; u < u_end; ++u, advance(cur)) {
+    const int64_t b = cur.b, r = cur.r, sg = cur.sg;
+    if (b != cur_b) {
+      // this warp's block-scale table for matrix b
+      g = warp_global_scale(p, b);
+      t6g = __fmul_rn(6.0f, g);
+      gzero = !(g > 0.0f);
+      for (int c = lane; c < 128; c += 32)
+        tab[c] = fminf(__frcp_rn(__fmul_rn(e4m3_to_f32((uint32_t)c), g)), FLT_MAX);
+      if (p.t_f32) t_scale = __fdiv_rn(p.lora_scale, acc_scale_of(g, *p.g_b));
+      __syncwarp();
+      cur_b = b;
+    }
+    if (r == 0 && sg == 0 && lane == 0 && p.g_out) p.g_out[b] = g;   // the matrix's first unit
+    const int64_t sr = source_row(r);
+    const bool skip = p.row_map && sr < 0;   // unmapped (padding) rows are left untouched
+    if (!skip) {
+      if (sr >= 0) {
+        const bool got = mbar_wait_u(smem_u32(&full[s]), (parity >> s) & 1, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) record_timeout(p.status);
+          break;
+        }
+        parity ^= 1u << s;
+        if (lane == 0) armed &= ~(1u << s);
+      }
+      if (p.t_f32 && sg == 0 && r < p.dst_rows) {
+        // LoRA hand-off: the down-projection's fp32 row, scaled and rounded once to bf16
+        for (int j = lane; j < p.rank; j += 32) {
+          float t = p.t_f32[r * p.rank + j];
+          for (int k = 1; k < p.t_splits; ++k) t = __fadd_rn(t, p.t_f32[(k * p.dst_rows + r) * p.rank + j]);
+          p.t_out[r * p.rank + j] = __float2bfloat16_rn(__fmul_rn(t, t_scale));
+        }
+      }
+      const int64_t c0 = sg * seg, len = seg < p.cols - c0 ? seg : p.cols - c0;
+      const int blk0 = (int)(c0 / 16), nb = (int)(len / 16);
+      const int nb_sf = (p.sf_swizzled && sg == nseg - 1) ? (int)(sfc_pad - blk0) : nb;
+      const bool live = sr >= 0;
+      uint2 *codes = reinterpret_cast<uint2 *>(p.codes_row + b * p.codes_row_bstride + r * row_bytes) + blk0;
+      // scale addresses: row part once per unit, block part in 32-bit arithmetic
+      uint8_t *sfr = p.sf_row + b * p.sf_row_bstride +
+                     (p.sf_swizzled ? 512 * ((r >> 7) * (sfc_pad >> 2)) + 16 * (r & 31) + 4 * ((r & 127) >> 5)
+                                    : r * nblk);
+      const uint32_t sbase = ring + (uint32_t)(s * slot_bytes) + 16 * h;
+      const uint32_t other = h ? (uint32_t)-16 : 16u;
+      for (int bi = lane; bi < nb_sf; bi += 64) {
+        const int bj = bi + 32;
+        const bool v0 = live && bi < nb, v1 = live && bj < nb;
+        uint4 a0 = make_uint4(0, 0, 0, 0), c0v = a0, a1 = a0, c1v = a0;
+        if (v0) {
+          a0 = lds128(sbase + 32u * bi);
+          c0v = lds128(sbase + 32u * bi + other);
+        }
+        if (v1) {
+          a1 = lds128(sbase + 32u * bj);
+          c1v = lds128(sbase + 32u * bj + other);
+        }
+        uint32_t sb0 = 0, sb1 = 0;
+        const uint2 k0 = pack_block(a0, c0v, h, t6g, gzero || !v0, tab, sb0);
+        const uint2 k1 = pack_block(a1, c1v, h, t6g, gzero || !v1, tab, sb1);
+        if (v0) codes[bi] = k0;
+        if (v1) codes[bj] = k1;
+        if (p.sf_swizzled) {
+          const int x0 = blk0 + bi, x1 = blk0 + bj;
+          sfr[512 * (int64_t)(x0 >> 2) + (x0 & 3)] = (uint8_t)sb0;
+          if (bj < nb_sf) sfr[512 * (int64_t)(x1 >> 2) + (x1 & 3)] = (uint8_t)sb1;
+        } else {
+          if (v0) sfr[blk0 + bi] = (uint8_t)sb0;
+          if (v1) sfr[blk0 + bj] = (uint8_t)sb1;
+        }
+      }
+    }
+    // slot s is free again: start the copy of the unit `slots` ahead
+    __syncwarp();
+    if (lane == 0) issue(s);
+    if (++s == slots) s = 0;
+  }
+  // copies still in flight (only after a timeout): wait for them before exiting
+  if (lane == 0)
+    for (int k = 0; k < slots; ++k)
+      if (armed & (1u << k)) mbar_wait(&full[k], (parity >> k) & 1, kQDrainNs);
+}
+
 // ------------------------------------------------- tiled col (+row) packing --
 // A CTA quantizes 64 x 128 tiles of one matrix (grid-stride over tiles).  Each
 // thread loads two 16-element row blocks (64 contiguous bytes) and packs them
@@ -440,7 +666,28 @@ cudaError_t launch_amax(const QuantParams &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+static cudaError_t launch_quant_rows_staged(const QuantParams &p, int num_sms, cudaStream_t st) {
+  const StagedCfg c = staged_cfg(p.cols);
+  static size_t configured = 48 * 1024;
+  if (c.smem > configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_quant_rows_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)c.smem);
+    if (e != cudaSuccess) return e;
+    configured = c.smem;
+  }
+  const int64_t rows_out =
+      (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  const int64_t units = rows_out * c.nseg * p.batch;
+  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(num_sms, (units + kQWarps - 1) / kQWarps));
+  k_quant_rows_staged<<<(unsigned)ctas, kQWarps * 32, c.smem, st>>>(p, c.seg, c.nseg, c.slots);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st) {
+  // bulk copies need 16-byte aligned rows and segments
+  const bool staged = ((reinterpret_cast<uintptr_t>(p.src) & 15) == 0) && (p.ld % 8 == 0) &&
+                      (p.bstride % 8 == 0) && (p.cols % 16 == 0);
+  if (staged) return launch_quant_rows_staged(p, num_sms, st);
   const int64_t rows_out = p.sf_swizzled ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
   int64_t ctas = (rows_out + 7) / 8;      // 8 warps per CTA, one row each per pass
   const int64_t cap = (int64_t)num_sms * 8 / std::max<int64_t>(1, p.batch);
