@@ -40,6 +40,10 @@ UNIT = "TFLOP/s"
 PREFILL = dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0)
 L2_BYTES = 129 * 1024 * 1024
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
+# DRAM bytes of one k_gemm_fp4<256> launch on the prefill workload, from one ncu
+# capture of the current kernel (36.84 MB read + 1.00 MB written); set to None
+# whenever the kernel changes until it is captured again.
+GEMM_TRAFFIC_BYTES = 37834240
 
 
 def peaks():
@@ -418,7 +422,8 @@ def main():
 
     ms = main_res["ms"]
     value = world * main_res["flops"] / (ms * 1e-3) / 1e12
-    fp4_peak = pk["bf16"] * FP4_PER_BF16
+    # the GEMM is timed inside a long run of steps: the sustained bf16 figure
+    fp4_peak = pk["bf16_sustained"] * FP4_PER_BF16
     gemm_tflops = main_res["flops"] / (main_res["gemm_ms"] * 1e-3) / 1e12
     e2e = main_res["e2e"]
     line = dict(
@@ -433,8 +438,11 @@ def main():
                     parallelism=f"replicas x{world}"),
         roofline=dict(bound="tensor", kernel="k_gemm_fp4<256>", achieved=gemm_tflops,
                       peak=fp4_peak, unit="TFLOP/s", frac=gemm_tflops / fp4_peak,
-                      traffic=None,
-                      peak_note=f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x 6 (nominal fp4:bf16)"),
+                      traffic=GEMM_TRAFFIC_BYTES,
+                      traffic_note="dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu "
+                                   "capture (profiles/k_gemm_fp4_prefill_M8192_N2048_K6144.md)",
+                      peak_note=f"{pk['source']} bf16 sustained {pk['bf16_sustained']} TFLOP/s x 6 "
+                                f"(nominal fp4:bf16)"),
         e2e=dict(value=world * main_res["flops"] / (e2e["ms"] * 1e-3) / 1e12, unit=UNIT,
                  h2d_bytes_per_step=e2e["h2d"], d2h_bytes_per_step=e2e["d2h"]),
         gpu_launches=main_res["launches_per_step"] * args.steps,
