@@ -9,15 +9,15 @@
 // binds" / "The bottom line"), plus the bf16 rank-r LoRA over the frozen FP4
 // base (same page, TL;DR and "A model no kernel wanted to serve").
 //
-// Design (sm_103a): a persistent kernel, one CTA per SM, 192 threads:
+// Design (sm_103a): a persistent kernel, one CTA per SM, 320 threads:
 //   warp 0      TMA producer: 128x256 FP4 A tile, BNx256 FP4 B tile (128-byte
-//               swizzle), their 128x4 scale atoms by bulk copy; a 4-stage ring.
-//   warp 1      one thread issues tcgen05.cp (scales -> TMEM) and
-//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M=128,
-//               N=BN, K=64) into a BN-column fp32 accumulator in TMEM; then,
+//               swizzle), their 128x4 scale atoms by bulk copy; a 4- or 6-stage ring.
+//   warp 1      one thread issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (M=128, N=BN, K=64) into a BN-column fp32 accumulator in TMEM; then,
 //               for the LoRA, kind::f16 MMAs of T' (bf16, pre-scaled by
 //               (alpha/r)/(g_a g_b)) against LB into the same accumulator.
-//   warps 2..5  epilogue: tcgen05.ld -> * g_a g_b -> bf16/fp32 -> global.
+//   warps 2..5  scales: shared memory -> TMEM with tcgen05.st (one lane quarter each).
+//   warps 6..9  epilogue: tcgen05.ld -> * g_a g_b -> bf16/fp32 -> global.
 // Every mbarrier wait is bounded; on expiry the CTA records a timeout, waits
 // for its own copies and MMAs in flight, frees TMEM and exits.
 #include <cstdlib>
