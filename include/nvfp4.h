@@ -260,6 +260,10 @@ size_t nvfp4_codes_bytes(int64_t rows, int64_t cols);
 size_t nvfp4_sf_bytes(int64_t rows, int64_t cols, int32_t sf_layout);
 /* Static text for a status code. */
 const char *nvfp4_status_string(nvfp4_status s);
+/* Text of the last CUDA runtime error that a library call on the calling
+ * host thread met (the cause behind NVFP4_ERR_CUDA); "no error" if none.
+ * Library diagnostics only: the pages have no counterpart. */
+const char *nvfp4_last_cuda_error(void);
 /* Synchronizes `stream`, reads (and clears) the device status word at the
  * start of `workspace` and returns it (NVFP4_OK when no wait expired). */
 nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream);

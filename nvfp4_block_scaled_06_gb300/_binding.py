@@ -26,6 +26,7 @@ EXPORTS = [
     "nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", "nvfp4_codes_bytes",
     "nvfp4_sf_bytes", "nvfp4_status_string", "nvfp4_read_device_status",
     "nvfp4_set_wait_timeout_ns", "nvfp4_version", "nvfp4_quantize_noalloc",
+    "nvfp4_last_cuda_error",
 ]
 
 
@@ -120,6 +121,8 @@ def load(path: str | None = None):
     lib.nvfp4_sf_bytes.restype = C.c_size_t
     lib.nvfp4_status_string.argtypes = [C.c_int]
     lib.nvfp4_status_string.restype = C.c_char_p
+    lib.nvfp4_last_cuda_error.argtypes = []
+    lib.nvfp4_last_cuda_error.restype = C.c_char_p
     lib.nvfp4_read_device_status.argtypes = [vp, vp]
     lib.nvfp4_read_device_status.restype = C.c_int
     lib.nvfp4_set_wait_timeout_ns.argtypes = [C.c_uint64]
@@ -134,7 +137,10 @@ def load(path: str | None = None):
 class NVFP4Error(RuntimeError):
     def __init__(self, status: int, where: str):
         lib = load()
-        super().__init__(f"{where}: {lib.nvfp4_status_string(status).decode()} (status {status})")
+        msg = f"{where}: {lib.nvfp4_status_string(status).decode()} (status {status})"
+        if status == ERR_CUDA:
+            msg += f": {lib.nvfp4_last_cuda_error().decode()}"
+        super().__init__(msg)
         self.status = status
 
 

@@ -84,7 +84,15 @@ size_t sf_swizzled_bytes(int64_t rows, int64_t cols) {
   return (size_t)pad_up(rows, 128) * (size_t)pad_up(cols / 16, 4);
 }
 
-nvfp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+// The last CUDA runtime error this thread saw inside the library (for
+// nvfp4_last_cuda_error).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+nvfp4_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return NVFP4_OK;
+  g_last_cuda_error = e;
+  return NVFP4_ERR_CUDA;
+}
 
 // K ranges of the fused LoRA-down + amax pass (fp32 partials, summed in order
 // by the packing kernel): two ranges put 2x as many SMs on the pass over X.
@@ -165,9 +173,9 @@ nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int sm
   p.timeout_ns = g_timeout_ns.load();
   if (!a->global_scale_in) {
     cudaError_t e = launch_amax(p, st);
-    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   }
-  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = col ? launch_quant_tiles(p, sms, st) : launch_quant_rows(p, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
   return cuda_status(e);
@@ -307,7 +315,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     g.d = a->d;
     g.ldd = a->ldd;
     g.out_fp32 = a->out_dtype == NVFP4_OUT_FP32;
-    if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
     cudaError_t e = launch_gemv_ws(g, sms, st, pl.gemv_partial);
     if (e == cudaSuccess) e = mark(a->prof_end, st);
     return cuda_status(e);
@@ -361,7 +369,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
       lp.amax_part = pl.aq_amax;
       lp.t_f32 = pl.t32;
       lp.ksplit = pl.lsplit;
-      if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+      if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
       q.nparts = std::min(lp.tiles_m * pl.lsplit, sms);
       q.t_f32 = pl.t32;
       q.t_splits = pl.lsplit;
@@ -369,17 +377,17 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
       q.rank = a->rank;
       q.lora_scale = lp.lora_scale;
       q.g_b = a->b_global_scale;
-    } else if (!a->a_global_scale && launch_amax(q, st) != cudaSuccess) {
-      return NVFP4_ERR_CUDA;
+    } else if (!a->a_global_scale) {
+      if (cudaError_t e_ = launch_amax(q, st); e_ != cudaSuccess) return cuda_status(e_);
     }
-    if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
     a_codes = pl.aq_codes;
     a_sf = pl.aq_sf;
     g_a = pl.aq_g;
   }
   if (a->lora_a && !pl.t32) {
     lp.g_a = g_a;
-    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
   }
   if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, a->K / 2, a->M, a->K / 2, 128, 128) ||
       !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, bn))
@@ -412,7 +420,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
-  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess && pl.ksplit > 1) e = launch_splitk_reduce(p, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
@@ -499,7 +507,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   r.gtiles = pl.gtiles;
   r.gnum_mtiles = pl.nmt;
   r.offsets_out = a->expert_offsets_out;
-  if (launch_route(r, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = launch_route(r, st); e_ != cudaSuccess) return cuda_status(e_);
 
   QuantParams q{};
   q.src = static_cast<const __nv_bfloat16 *>(a->x_bf16);
@@ -518,8 +526,10 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   q.dst_rows = pl.prow_max;
   q.status = status;
   q.timeout_ns = tmo;
-  if (!a->x_global_scale && launch_amax(q, st) != cudaSuccess) return NVFP4_ERR_CUDA;
-  if (launch_quant_rows(q, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (!a->x_global_scale) {
+    if (cudaError_t e_ = launch_amax(q, st); e_ != cudaSuccess) return cuda_status(e_);
+  }
+  if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
   const float *g_x = a->x_global_scale ? a->x_global_scale : pl.g_x;
 
   const int bn = 256;
@@ -555,7 +565,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
     lp.row_map = pl.row_map;
     lp.status = status;
     lp.timeout_ns = tmo;
-    if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
     lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
   }
   GemmParams p{};
@@ -581,7 +591,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
-  if (mark(a->prof_begin, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
   return cuda_status(e);
@@ -637,7 +647,7 @@ nvfp4_status run_lora(const nvfp4_lora_args *a, const LoraPlan &pl, int sms, cud
   lp.tiles_m = (int)ceil_div(a->M, 128);
   lp.status = status;
   lp.timeout_ns = tmo;
-  if (launch_lora_down(lp, lm, sms, st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
   if (a->delta_sq_norm_out && cudaMemsetAsync(a->delta_sq_norm_out, 0, 4, st) != cudaSuccess)
     return NVFP4_ERR_CUDA;
   GemmParams p{};
@@ -709,6 +719,8 @@ size_t nvfp4_sf_bytes(int64_t rows, int64_t cols, int32_t sf_layout) {
   return (size_t)rows * (size_t)(cols / 16);
 }
 
+const char *nvfp4_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
 const char *nvfp4_status_string(nvfp4_status s) {
   switch (s) {
     case NVFP4_OK: return "ok";
@@ -731,9 +743,11 @@ nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream) {
   if (!workspace) return NVFP4_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int v = 0;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return NVFP4_ERR_CUDA;
-  if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NVFP4_ERR_CUDA;
-  if (v != 0 && cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+  if (cudaError_t e_ = cudaStreamSynchronize(st); e_ != cudaSuccess) return cuda_status(e_);
+  if (cudaError_t e_ = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost); e_ != cudaSuccess) return cuda_status(e_);
+  if (v != 0) {
+    if (cudaError_t e_ = cudaMemset(workspace, 0, sizeof(int)); e_ != cudaSuccess) return cuda_status(e_);
+  }
   return static_cast<nvfp4_status>(v);
 }
 

@@ -40,6 +40,7 @@ def test_size_queries(clib):
     assert clib.nvfp4_sf_bytes(37, 80, 1) == 128 * 8
     assert clib.nvfp4_status_string(4).decode().startswith("workspace")
     assert clib.nvfp4_version() == 0x000100
+    assert clib.nvfp4_last_cuda_error().decode() == "no error"
 
 
 def test_host_validation_without_device(clib):
