@@ -438,7 +438,8 @@ struct GroupedPlan {
   uint32_t *amax = nullptr;
   int nparts = 0;
   float *g_x = nullptr;
-  uint8_t *xq = nullptr, *xsf = nullptr;
+  uint8_t *xq = nullptr, *xsf = nullptr;      // grouped, padded A operand
+  uint8_t *xq_tok = nullptr, *xsf_tok = nullptr;  // X quantized once per token (linear scales)
   __nv_bfloat16 *t = nullptr;
 };
 
@@ -461,6 +462,8 @@ nvfp4_status plan_grouped(const nvfp4_grouped_args *a, GroupedPlan *pl) {
   pl->g_x = c.take<float>(4);
   pl->xq = c.take<uint8_t>((size_t)pl->prow_max * a->K / 2);
   pl->xsf = c.take<uint8_t>(sf_swizzled_bytes(pl->prow_max, a->K));
+  pl->xq_tok = c.take<uint8_t>((size_t)a->num_tokens * a->K / 2);
+  pl->xsf_tok = c.take<uint8_t>((size_t)a->num_tokens * (a->K / 16));
   if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)pl->prow_max * a->rank * 2);
   pl->ws = c.off;
   return NVFP4_OK;
@@ -519,17 +522,22 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   q.g_out = pl.g_x;
   q.amax_part = pl.amax;
   q.nparts = pl.nparts;
-  q.codes_row = pl.xq;
-  q.sf_row = pl.xsf;
-  q.sf_swizzled = 1;
-  q.row_map = pl.row_map;
-  q.dst_rows = pl.prow_max;
+  // every token row is quantized once (one tensor-wide g), then its codes and
+  // scales are copied to each of its top_k rows of the grouped operand
+  q.codes_row = pl.xq_tok;
+  q.sf_row = pl.xsf_tok;
+  q.sf_swizzled = 0;
+  q.dst_rows = a->num_tokens;
   q.status = status;
   q.timeout_ns = tmo;
   if (!a->x_global_scale) {
     if (cudaError_t e_ = launch_amax(q, st); e_ != cudaSuccess) return cuda_status(e_);
   }
   if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
+  if (cudaError_t e_ = launch_gather_packed(pl.xq_tok, pl.xsf_tok, pl.row_map, pl.prow_max, a->K, pl.xq,
+                                            pl.xsf, sms, st);
+      e_ != cudaSuccess)
+    return cuda_status(e_);
   const float *g_x = a->x_global_scale ? a->x_global_scale : pl.g_x;
 
   const int bn = 256;
@@ -563,6 +571,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
     lp.gtiles = pl.gtiles;
     lp.gnum_mtiles = pl.nmt;
     lp.row_map = pl.row_map;
+    lp.x = static_cast<const __nv_bfloat16 *>(a->x_bf16);
     lp.status = status;
     lp.timeout_ns = tmo;
     if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);

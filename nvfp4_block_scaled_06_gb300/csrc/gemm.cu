@@ -507,9 +507,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // T'[row, j] = bf16( s_row * sum_k X[src(row), k] A[j, k] ), fp32 accumulation
 // in TMEM (kind::f16, M=128, N=rank, K=16 per instruction).  s_row =
 // (alpha/r) / (g_a g_b[e]) when the result feeds the FP4 accumulator, alpha/r
-// for the standalone path.  Grouped mode gathers X rows with tile::gather4.
+// for the standalone path.  Grouped mode gathers X rows with 16-byte cp.async
+// copies issued by warps 2..5 (one tile row per thread, written in the
+// 128-byte swizzled arrangement the MMA descriptor expects), up to three
+// stages in flight per thread; the A tiles still come by TMA.
 constexpr int kLoraStages = 6;
 constexpr int kLoraThreads = 192;
+constexpr int kGatherThreads = 128;   // warps 2..5 gather X rows in grouped mode
 
 // A stage holds two 64-wide K sub-tiles: [X0 | X1 | A0 | A1], X tiles 128 rows x 128 B.
 constexpr int kLoraSub = 2;
@@ -544,7 +548,8 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
   const bool scan = p.amax_part != nullptr;   // epilogue warps also scan X for amax
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(&full[s], 1);
+      // grouped: the producer's arrival + one per gathering thread
+      mbar_init(&full[s], p.row_map ? 1 + kGatherThreads : 1);
       mbar_init(&empty[s], scan ? 5 : 1);
     }
     mbar_init(acc_full, 1);
@@ -582,14 +587,6 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
       const int64_t row0 = p.gtiles ? (int64_t)p.gtiles[t].a_row0 : (int64_t)t * kBM;
       const int a_row = p.gtiles ? p.gtiles[t].expert * p.rank : 0;   // this expert's A
-      int32_t src[4] = {0, 0, 0, 0};
-      if (p.row_map) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int32_t sr = p.row_map[row0 + lane * 4 + i];
-          src[i] = sr < 0 ? 0 : sr;
-        }
-      }
       for (int st = 0; st < nsteps; ++st) {
         bool good = true;
         if (lane == 0)
@@ -605,17 +602,13 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
         const int k64 = kb + st * kLoraSub;
         const int nsub = min(kLoraSub, ke - k64);
         if (lane == 0) {
-          mbar_arrive_expect_tx_u(fb, nsub * (x_sub + a_sub));
+          mbar_arrive_expect_tx_u(fb, nsub * ((p.row_map ? 0 : x_sub) + a_sub));
           for (int j = 0; j < nsub; ++j) {
             tma_load_2d_u(sa + j * a_sub, &tmA, fb, (k64 + j) * 64, a_row);
             if (!p.row_map) tma_load_2d_hint_u(sx + j * x_sub, &tmX, fb, (k64 + j) * 64, (int)row0, xpol);
           }
         }
         __syncwarp();
-        if (p.row_map)
-          for (int j = 0; j < nsub; ++j)
-            tma_gather4(base + stage * sbytes + j * x_sub + lane * 4 * 128, &tmX, &full[stage],
-                        (k64 + j) * 64, src[0], src[1], src[2], src[3]);
         if (lane == 0) {
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -689,6 +682,53 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
       int64_t row0;
       int e = 0;
+      if (p.row_map) {
+        // gather this unit's X rows: thread r copies tile row r (token
+        // row_map[row0 + r]; padding rows read as zeros) chunk by chunk
+        const int64_t g_row0 = p.gtiles ? (int64_t)p.gtiles[t].a_row0 : (int64_t)t * kBM;
+        const int32_t srow = p.row_map[g_row0 + r];
+        const __nv_bfloat16 *xrow = p.x + (srow < 0 ? 0 : (int64_t)srow * p.K);
+        const uint32_t sw = (uint32_t)(r & 7);
+        int pend[3];
+        int npend = 0;
+        for (int st = 0; st < nsteps; ++st) {
+          if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(&empty[stage], phase ^ 1, p.timeout_ns))) {
+            if (lane == 0) signal_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          const int k64 = kb + st * kLoraSub;
+          const int nsub = min(kLoraSub, ke - k64);
+          const uint32_t dst0 = smem_u32(base + stage * sbytes) + (uint32_t)(r * 128);
+          for (int j = 0; j < nsub; ++j) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int64_t kel = (int64_t)(k64 + j) * 64 + c * 8;
+              const bool in = srow >= 0 && kel < p.K;
+              cp_async_16(dst0 + j * x_sub + ((c ^ sw) << 4), in ? xrow + kel : p.x, in ? 16u : 0u);
+            }
+          }
+          cp_async_commit();
+          pend[npend++] = stage;
+          if (npend == 3) {
+            // the oldest group has landed: publish it to the MMA (async proxy)
+            cp_async_wait<2>();
+            fence_proxy_async_shared();
+            mbar_arrive(&full[pend[0]]);
+            pend[0] = pend[1];
+            pend[1] = pend[2];
+            npend = 2;
+          }
+          if (++stage == stages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_shared();
+        for (int i = 0; i < npend; ++i) mbar_arrive(&full[pend[i]]);
+        if (!ok) break;
+      }
       if (scan) {
         // max |x| over this warp's 32 rows of every X tile, read from shared memory
         for (int st = 0; st < nsteps; ++st) {

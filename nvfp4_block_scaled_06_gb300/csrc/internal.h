@@ -45,6 +45,10 @@ nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scr
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
+// Token-row codes + linear scales -> expert-grouped rows + swizzled scales.
+cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
+                                 int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
+                                 cudaStream_t st);
 
 // --------------------------------------------------------------------- GEMM --
 // One grouped m-tile: expert, first A row (padded grouped order), valid rows,
@@ -100,6 +104,7 @@ struct LoraDownParams {
   const GroupTile *gtiles;
   const int32_t *gnum_mtiles;
   const int32_t *row_map;     // grouped: padded row -> token (gather)
+  const __nv_bfloat16 *x;     // grouped: token rows of X, leading dimension K
   uint32_t *amax_part;        // optional: per-CTA max |x| magnitude bits of the X tiles read
   float *t_f32;               // optional: write T in fp32 (unscaled) instead of T'
   int ksplit;                 // with t_f32: K split in ranges, partials [ksplit][M][rank]

@@ -641,6 +641,65 @@ __global__ void __launch_bounds__(256) k_quant_tiles(QuantParams p) {
   }
 }
 
+// ---------------------------------------------------------- grouped gather --
+// The expert-grouped, 128-padded A operand of the grouped GEMM from the token
+// rows quantized once (one tensor-wide g): destination row r takes the codes
+// and scales of token row_map[r]; rows with row_map < 0 (padding) are left
+// untouched.  Scales arrive in the linear [tokens][K/16] layout and leave in
+// the swizzled 128x4-atom layout (scale columns past K/16 inside the last
+// 4-column group are zero).  One warp per destination row: 16-byte copies of
+// the codes, one 4-scale word per lane step.
+__global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict__ codes_src,
+                                                       const uint8_t *__restrict__ sf_src,
+                                                       const int32_t *__restrict__ row_map, int64_t rows,
+                                                       int64_t K, uint8_t *__restrict__ codes_dst,
+                                                       uint8_t *__restrict__ sf_dst) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t vec_per_row = K / 32;               // 16-byte vectors of codes
+  const int64_t nblk = K / 16, sfc_pad = (nblk + 3) & ~int64_t(3);
+  int64_t sr_next = warp < rows ? row_map[warp] : -1;
+  for (int64_t r = warp; r < rows; r += nwarps) {
+    const int64_t sr = sr_next;
+    if (r + nwarps < rows) sr_next = row_map[r + nwarps];   // prefetch the next row's source
+    if (sr < 0) continue;
+    const uint4 *cs = reinterpret_cast<const uint4 *>(codes_src + sr * (K / 2));
+    uint4 *cd = reinterpret_cast<uint4 *>(codes_dst + r * (K / 2));
+    // eight 16-byte loads in flight per lane before their stores
+    for (int64_t i0 = 0; i0 < vec_per_row; i0 += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + 32 * j + lane;
+        if (i < vec_per_row) v[j] = __ldg(cs + i);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t i = i0 + 32 * j + lane;
+        if (i < vec_per_row) cd[i] = v[j];
+      }
+    }
+    const uint8_t *ss = sf_src + sr * nblk;
+    uint8_t *sd = sf_dst + 16 * (r & 31) + 4 * ((r & 127) >> 5) + 512 * ((r >> 7) * (sfc_pad >> 2));
+    for (int64_t g = lane; g < (sfc_pad >> 2); g += 32) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * g + j < nblk) w |= (uint32_t)__ldg(ss + 4 * g + j) << (8 * j);
+      *reinterpret_cast<uint32_t *>(sd + 512 * g) = w;
+    }
+  }
+}
+
+cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
+                                 int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
+                                 cudaStream_t st) {
+  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms * 8));
+  k_gather_packed<<<(unsigned)ctas, 256, 0, st>>>(codes_src, sf_src, row_map, rows, K, codes_dst, sf_dst);
+  return cudaGetLastError();
+}
+
 // Zero the swizzled padding of a scale buffer that the tile kernel does not
 // reach: rows in [rows, pad128(rows)) of every matrix.  Columns beyond the
 // matrix inside a reached row are written by the kernels themselves.

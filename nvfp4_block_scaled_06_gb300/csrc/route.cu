@@ -4,10 +4,11 @@
 // grouped stably by expert id (rows of one expert contiguous, ordered by pair
 // index token*top_k + slot).  Three small kernels, no atomics on global memory:
 //   hist     per 1024-pair chunk, per-expert counts -> hist[chunk][e]
-//   scan     one CTA: chunk bases per expert, counts, offsets, 128-padded
-//            offsets, the m-tile table and the padding rows of row_map
-//   scatter  per chunk, the stable rank of each pair among same-expert pairs
-//            (warp match + per-warp counts) -> perm and row_map
+//   scan     one CTA: counts, offsets, 128-padded offsets, the m-tile table
+//            and the padding rows of row_map
+//   scatter  per chunk: its base per expert (offset + earlier chunks' counts),
+//            then the stable rank of each pair among same-expert pairs (warp
+//            match + per-warp counts) -> perm and row_map
 // Expert ids outside [0, E) are dropped.
 #include "internal.h"
 #include "ptx.cuh"
@@ -63,11 +64,17 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
   const bool act = e < p.num_experts;
   int32_t count = 0;
   if (act) {
-    for (int c = 0; c < p.nchunks; ++c) {
-      const int32_t v = p.hist[(int64_t)c * p.num_experts + e];
-      p.hist[(int64_t)c * p.num_experts + e] = count;
-      count += v;
+    // eight independent loads in flight per step (the chunk bases are formed
+    // by the scatter kernel)
+    int c = 0;
+    for (; c + 8 <= p.nchunks; c += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = p.hist[(int64_t)(c + j) * p.num_experts + e];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) count += v[j];
     }
+    for (; c < p.nchunks; ++c) count += p.hist[(int64_t)c * p.num_experts + e];
   }
   const int32_t padded = (count + 127) & ~127;
   const int32_t mt = padded / 128;
@@ -80,7 +87,6 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
     p.offsets[e] = off;
     p.poffsets[e] = poff;
     if (p.offsets_out) p.offsets_out[e] = off;
-    for (int c = 0; c < p.nchunks; ++c) p.hist[(int64_t)c * p.num_experts + e] += off;
     for (int j = 0; j < mt; ++j) {
       GroupTile g;
       g.expert = e;
@@ -101,9 +107,15 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
 }
 
 __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
-  extern __shared__ uint16_t sh_cnt[];   // [32 warps][E]
+  extern __shared__ int32_t sh_base[];   // [E] first grouped position of this chunk's pairs
   const int E = p.num_experts;
+  uint16_t *sh_cnt = reinterpret_cast<uint16_t *>(sh_base + E);   // [32 warps][E]
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) sh_cnt[i] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t b = p.offsets[e];
+    for (int c = 0; c < (int)blockIdx.x; ++c) b += p.hist[(int64_t)c * E + e];
+    sh_base[e] = b;
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t i = (int64_t)blockIdx.x * p.chunk + threadIdx.x;
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
   if (e >= 0) {
     int before = 0;
     for (int v = 0; v < w; ++v) before += sh_cnt[v * E + e];
-    const int32_t pos = p.hist[(int64_t)blockIdx.x * E + e] + before + rank_w;
+    const int32_t pos = sh_base[e] + before + rank_w;
     p.perm[pos] = (int32_t)i;
     p.row_map[p.poffsets[e] + (pos - p.offsets[e])] = (int32_t)(i / p.top_k);
   }
@@ -133,7 +145,7 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
   k_route_scan<<<1, 1024, 0, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t sm = (size_t)32 * p.num_experts * sizeof(uint16_t);
+  const size_t sm = (size_t)p.num_experts * sizeof(int32_t) + (size_t)32 * p.num_experts * sizeof(uint16_t);
   static size_t configured = 48 * 1024;
   if (sm > configured) {
     e = cudaFuncSetAttribute(k_route_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
