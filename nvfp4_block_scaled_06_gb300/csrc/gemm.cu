@@ -508,8 +508,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // in TMEM (kind::f16, M=128, N=rank, K=16 per instruction).  s_row =
 // (alpha/r) / (g_a g_b[e]) when the result feeds the FP4 accumulator, alpha/r
 // for the standalone path.  Grouped mode gathers X rows with 16-byte cp.async
-// copies issued by warps 2..5 (one tile row per thread, written in the
-// 128-byte swizzled arrangement the MMA descriptor expects), up to three
+// copies issued by warps 2..5 (eight lanes per row: coalesced reads, written in
+// the 128-byte swizzled arrangement the MMA descriptor expects), up to three
 // stages in flight per thread; the A tiles still come by TMA.
 constexpr int kLoraStages = 6;
 constexpr int kLoraThreads = 192;
@@ -683,12 +683,16 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
       int64_t row0;
       int e = 0;
       if (p.row_map) {
-        // gather this unit's X rows: thread r copies tile row r (token
-        // row_map[row0 + r]; padding rows read as zeros) chunk by chunk
+        // gather this unit's X rows: thread r copies 16-byte chunk (r & 7) of
+        // tile rows (r >> 3) + 16 i, i = 0..7 (token row_map[row0 + row];
+        // padding rows read as zeros), so the eight lanes of a row read its
+        // 128 contiguous bytes (coalesced) and land in the swizzled slots
         const int64_t g_row0 = p.gtiles ? (int64_t)p.gtiles[t].a_row0 : (int64_t)t * kBM;
-        const int32_t srow = p.row_map[g_row0 + r];
-        const __nv_bfloat16 *xrow = p.x + (srow < 0 ? 0 : (int64_t)srow * p.K);
-        const uint32_t sw = (uint32_t)(r & 7);
+        const int gc = r & 7, grow = r >> 3;
+        const uint32_t swz = (uint32_t)((gc ^ (grow & 7)) << 4);
+        int32_t srow[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) srow[i] = p.row_map[g_row0 + grow + 16 * i];
         int pend[3];
         int npend = 0;
         for (int st = 0; st < nsteps; ++st) {
@@ -699,13 +703,14 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
           }
           const int k64 = kb + st * kLoraSub;
           const int nsub = min(kLoraSub, ke - k64);
-          const uint32_t dst0 = smem_u32(base + stage * sbytes) + (uint32_t)(r * 128);
+          const uint32_t dst0 = smem_u32(base + stage * sbytes) + (uint32_t)(grow * 128) + swz;
           for (int j = 0; j < nsub; ++j) {
+            const int64_t kel = (int64_t)(k64 + j) * 64 + gc * 8;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int64_t kel = (int64_t)(k64 + j) * 64 + c * 8;
-              const bool in = srow >= 0 && kel < p.K;
-              cp_async_16(dst0 + j * x_sub + ((c ^ sw) << 4), in ? xrow + kel : p.x, in ? 16u : 0u);
+            for (int i = 0; i < 8; ++i) {
+              const bool in = srow[i] >= 0 && kel < p.K;
+              cp_async_16(dst0 + j * x_sub + (uint32_t)(i * 16 * 128),
+                          in ? p.x + (int64_t)srow[i] * p.K + kel : p.x, in ? 16u : 0u);
             }
           }
           cp_async_commit();
