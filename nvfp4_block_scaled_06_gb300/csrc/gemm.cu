@@ -162,6 +162,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();   // inputs of this kernel come from the previous one in the stream
 
   const int nmt = p.gtiles ? *p.gnum_mtiles : p.tiles_m;
   const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
@@ -567,6 +569,8 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();   // inputs of this kernel come from the previous one in the stream
   const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
   const int num_tiles = (p.gtiles ? *p.gnum_mtiles : p.tiles_m) * ksplit;   // (tile, K range)
   // K range of a unit, in 64-wide steps, a multiple of the stage width
@@ -882,8 +886,7 @@ static cudaError_t launch_bn(const GemmParams &p, const GemmMaps &m, int num_sms
 #endif
   if (!p.gtiles) grid = (int)std::min<int64_t>(tiles, grid);
   if (grid <= 0) return cudaSuccess;
-  k_gemm_fp4<BN><<<grid, kGemmThreads, C::kSmemBytes, st>>>(m.a, m.b, m.t, m.lb, p);
-  return cudaGetLastError();
+  return launch_pdl(k_gemm_fp4<BN>, dim3(grid), dim3(kGemmThreads), C::kSmemBytes, st, m.a, m.b, m.t, m.lb, p);
 }
 
 cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &m, int bn, int num_sms,
@@ -908,8 +911,7 @@ cudaError_t launch_lora_down(const LoraDownParams &p, const LoraDownMaps &m, int
   int grid = num_sms;
   if (!p.gtiles) grid = std::min(p.tiles_m * std::max(1, p.ksplit), num_sms);
   if (grid <= 0) return cudaSuccess;
-  k_lora_down<<<grid, kLoraThreads, smem, st>>>(m.x, m.a, p, stages);
-  return cudaGetLastError();
+  return launch_pdl(k_lora_down, dim3(grid), dim3(kLoraThreads), smem, st, m.x, m.a, p, stages);
 }
 
 }  // namespace nvfp4

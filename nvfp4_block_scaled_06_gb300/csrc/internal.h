@@ -1,6 +1,8 @@
 // internal.h -- host/device structures shared by the library's translation units.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -163,5 +165,24 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
                  uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner,
                  uint32_t box_rows, CUtensorMapSwizzle sw);
+
+// Launch with programmatic stream serialization: the kernel may begin (its
+// setup) while the previous kernel in the stream drains; every kernel launched
+// this way calls griddep_wait() before touching global memory.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace nvfp4

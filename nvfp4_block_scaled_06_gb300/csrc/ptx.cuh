@@ -200,6 +200,19 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialization may start while its
+// predecessor in the stream finishes: it does its private setup, then waits
+// here until the predecessor grid has completed and its memory is visible
+// (a no-op for an ordinary launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled once every CTA of this grid
+// has called it (or exited); the next kernel still waits in griddep_wait()
+// for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05 --
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -376,6 +376,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
     fence_barrier_init();
   }
   __syncwarp();
+  griddep_launch_dependents();
+  griddep_wait();   // inputs of this kernel come from the previous one in the stream
 
   const int64_t rows_out =
       (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
@@ -738,8 +740,8 @@ static cudaError_t launch_quant_rows_staged(const QuantParams &p, int num_sms, c
       (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
   const int64_t units = rows_out * c.nseg * p.batch;
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(num_sms, (units + kQWarps - 1) / kQWarps));
-  k_quant_rows_staged<<<(unsigned)ctas, kQWarps * 32, c.smem, st>>>(p, c.seg, c.nseg, c.slots);
-  return cudaGetLastError();
+  return launch_pdl(k_quant_rows_staged, dim3((unsigned)ctas), dim3(kQWarps * 32), c.smem, st, p, c.seg,
+                    c.nseg, c.slots);
 }
 
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st) {
