@@ -328,6 +328,38 @@ def run_grouped(torch, nv, device, steps, warmup, pk):
                 tensor_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16"] * FP4_PER_BF16))
 
 
+def run_dgrad(torch, nv, device, steps, warmup, pk):
+    """dX = dY W for the prefill linear's backward, both ways the pages weigh:
+    dequantize the rowwise packing to bf16 (transposed) + bf16 GEMM, or the
+    column packing + W4A4 GEMM with dY quantized in the call."""
+    import ctypes as C
+    from synth import torch_case
+    c = torch_case("dgrad", seed=0, device=device)
+    M, N, K = c["M"], c["N"], c["K"]
+    q = nv.nvfp4_quantize(c["w"], pack="both", sf_layout="swizzled")
+    flops = 2.0 * M * N * K
+    out = {}
+    for name, kw in (("dequant_bf16", dict(w=(q["codes_row"][0], q["sf_row"][0], q["global_scale"]))),
+                     ("fp4_colpack", dict(wcol=(q["codes_col"][0], q["sf_col"][0], q["global_scale"])))):
+        call, dx = nv.prepare_dgrad(c["dy"], N, K, **kw)
+        prof = ev_pairs(torch, steps)
+
+        def step(i, pr, call=call):
+            arm(C, call.args, pr)
+            call()
+        ms = time_loop(torch, step, steps, warmup, prof)
+        kms = mean_ms(prof)
+        peak = pk["bf16_sustained"] * (1.0 if name == "dequant_bf16" else FP4_PER_BF16)
+        out[name] = dict(ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+                         gemm_tflops=flops / (kms * 1e-3) / 1e12,
+                         gemm_frac=flops / (kms * 1e-3) / 1e12 / peak,
+                         pre_ms=ms - kms)
+    out["workload"] = f"dX[{M},{K}] = dY[{M},{N}] W[{N},{K}] (prefill linear backward), bf16 out"
+    out["note"] = ("pre_ms = dequantization (bf16 mode) or dY quantization (fp4 mode); "
+                   "gemm_frac against the sustained bf16 / 6x bf16 peak")
+    return out
+
+
 # ----------------------------------------------------------- CPU baseline --
 def cpu_baseline(rows: int = 96):
     """The oracle on a row sample of the headline workload (host cores)."""
@@ -375,7 +407,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", choices=["quantize", "decode", "grouped"],
+    ap.add_argument("--only", choices=["quantize", "decode", "grouped", "dgrad"],
                     help="run just this secondary workload (for profiling) and print its numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
@@ -399,7 +431,8 @@ def main():
     pk = peaks()
 
     if args.only:
-        fn = dict(quantize=run_quantize_sweep, decode=run_decode, grouped=run_grouped)[args.only]
+        fn = dict(quantize=run_quantize_sweep, decode=run_decode, grouped=run_grouped,
+                  dgrad=run_dgrad)[args.only]
         res = fn(torch, nv, device, args.steps, args.warmup, pk)
         if rank == 0:
             print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, **res}))
@@ -414,6 +447,8 @@ def main():
         sec["decode"] = run_decode(torch, nv, device, steps2, max(3, args.warmup), pk)
         torch.cuda.empty_cache()
         sec["grouped"] = run_grouped(torch, nv, device, steps2, max(3, args.warmup), pk)
+        torch.cuda.empty_cache()
+        sec["dgrad"] = run_dgrad(torch, nv, device, steps2, max(3, args.warmup), pk)
         torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:

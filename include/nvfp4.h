@@ -252,6 +252,74 @@ nvfp4_status nvfp4_lora_epilogue(const nvfp4_lora_args *args, nvfp4_stream strea
 size_t nvfp4_lora_workspace_bytes(const nvfp4_lora_args *args);
 
 /* ------------------------------------------------------------------------ *
+ * nvfp4_dequantize -- NVFP4 -> bf16, optionally transposed.
+ *
+ * The backward of the frozen QLoRA base keeps only the rowwise (forward)
+ * packing and rebuilds the weight in bf16, transposed, on the fly
+ * ("Getting GLM-5.2 NVFP4 Post-Training off the ground", "Why can't we just
+ * transpose the one copy?" and "For a frozen QLoRA base").  Per element, in
+ * IEEE fp32 with one rounding per operation:
+ *     s_dec = E4M3(sb) * g;   v = E2M1(code) * s_dec;   out = bf16_rn(v)
+ * (s_dec is the quantizer's decode scale).  codes [rows][cols/2] with scales
+ * in `sf_layout`; transpose = 0 writes out[r][c] (ldo >= cols), 1 writes
+ * out[c][r] (ldo >= rows).
+ * Requirements: cols % 64 == 0; rows % 2 == 0 when transposed; codes/sf/out
+ *   16-byte aligned; ldo % 8 == 0 (ldo % 2 == 0 when transposed).  No workspace.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const void *codes, *sf;
+  int32_t sf_layout;             /* nvfp4_sf_layout */
+  const float *global_scale;     /* device scalar g */
+  int64_t rows, cols;            /* of the packed matrix */
+  int32_t transpose;
+  void *out;                     /* bf16 */
+  int64_t ldo;
+} nvfp4_dequant_args;
+
+nvfp4_status nvfp4_dequantize(const nvfp4_dequant_args *args, nvfp4_stream stream);
+
+/* ------------------------------------------------------------------------ *
+ * nvfp4_dgrad -- input gradient of the frozen linear: dX = dY W.
+ *
+ * dY bf16 [M][N] (lddy), W the [N][K] base weight, dX [M][K] (lddx), fp32
+ * accumulation.  Two ways to serve the backward's contraction over N, the two
+ * the page weighs ("Why can't we just transpose the one copy?", "The bottom
+ * line"):
+ *   NVFP4_DGRAD_DEQUANT_BF16: w_codes/w_sf (the rowwise packing, swizzled
+ *     scales) + w_global_scale are dequantized into the workspace as W^T in
+ *     bf16 (nvfp4_dequantize's arithmetic), then a bf16 tensor-core GEMM.
+ *   NVFP4_DGRAD_FP4_COLPACK: wcol_codes/wcol_sf = the column packing of W
+ *     (nvfp4_quantize pack=COL: codes [K][N/2], swizzled scales, blocks of 16
+ *     along N) with its global scale w_global_scale; dY is quantized in the
+ *     call along N (dynamic amax, or dy_global_scale when given) and the
+ *     product is the W4A4 FP4 GEMM (nvfp4_gemm's arithmetic).
+ * Requirements: N % 64 == 0 and K % 32 == 0; dy 16-byte aligned, lddy % 8;
+ *   dx 16-byte aligned, lddx % 8 (bf16) or % 4 (fp32).
+ * Workspace: nvfp4_dgrad_workspace_bytes(&args).
+ * ------------------------------------------------------------------------ */
+typedef enum { NVFP4_DGRAD_DEQUANT_BF16 = 0, NVFP4_DGRAD_FP4_COLPACK = 1 } nvfp4_dgrad_mode;
+
+typedef struct {
+  int64_t M, N, K;
+  int32_t mode;                  /* nvfp4_dgrad_mode */
+  const void *dy;                /* bf16 [M][lddy] */
+  int64_t lddy;
+  const void *w_codes, *w_sf;    /* DEQUANT_BF16 */
+  const void *wcol_codes, *wcol_sf;   /* FP4_COLPACK */
+  const float *w_global_scale;
+  const float *dy_global_scale;  /* FP4_COLPACK: NULL = dynamic */
+  int32_t out_dtype;             /* nvfp4_out_dtype */
+  void *dx;
+  int64_t lddx;
+  void *workspace;
+  size_t workspace_bytes;
+  void *prof_begin, *prof_end;   /* optional cudaEvent_t pair around the GEMM */
+} nvfp4_dgrad_args;
+
+nvfp4_status nvfp4_dgrad(const nvfp4_dgrad_args *args, nvfp4_stream stream);
+size_t nvfp4_dgrad_workspace_bytes(const nvfp4_dgrad_args *args);
+
+/* ------------------------------------------------------------------------ *
  * Size queries and status.
  * ------------------------------------------------------------------------ */
 /* Bytes of packed codes of a [rows][cols] matrix: rows * cols / 2. */

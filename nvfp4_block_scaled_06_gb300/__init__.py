@@ -12,15 +12,17 @@ import ctypes as C
 
 import torch
 
-from ._binding import (EXPORTS, GemmArgs, GroupedArgs, LoraArgs, NVFP4Error, OUT_BF16,
-                       OUT_FP32, PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR,
-                       SF_SWIZZLED, check, load)
+from ._binding import (DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK, EXPORTS, DequantArgs, DgradArgs,
+                       GemmArgs, GroupedArgs, LoraArgs, NVFP4Error, OUT_BF16, OUT_FP32,
+                       PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR, SF_SWIZZLED, check,
+                       load)
 
 __all__ = [
     "load", "NVFP4Error", "nvfp4_quantize", "nvfp4_gemm", "nvfp4_grouped_gemm",
     "nvfp4_lora_epilogue", "nvfp4_codes_bytes", "nvfp4_sf_bytes", "read_device_status",
     "set_wait_timeout_ns", "Prepared", "prepare_gemm", "prepare_quantize", "prepare_grouped",
     "SF_LINEAR", "SF_SWIZZLED", "PACK_ROW", "PACK_COL", "PACK_BOTH", "EXPORTS",
+    "nvfp4_dequantize", "nvfp4_dgrad", "prepare_dgrad",
 ]
 
 _PACK = {"row": PACK_ROW, "col": PACK_COL, "both": PACK_BOTH}
@@ -233,3 +235,61 @@ def nvfp4_lora_epilogue(y, x, lora_a, lora_b, alpha: float, want_norm: bool = Fa
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
     check(lib.nvfp4_lora_epilogue(C.byref(a), _stream(stream)), "nvfp4_lora_epilogue")
     return norm
+
+
+# ----------------------------------------------------------------- backward --
+
+def nvfp4_dequantize(codes, sf, global_scale, rows: int, cols: int, transpose: bool = False,
+                     sf_layout: str = "swizzled", out=None, stream=None) -> torch.Tensor:
+    """NVFP4 [rows, cols] -> bf16 [rows, cols] (or [cols, rows] with transpose)."""
+    lib = load()
+    if out is None:
+        shape = (cols, rows) if transpose else (rows, cols)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=codes.device)
+    a = DequantArgs(codes=codes.data_ptr(), sf=sf.data_ptr(), sf_layout=_SF[sf_layout],
+                    global_scale=global_scale.data_ptr(), rows=rows, cols=cols,
+                    transpose=1 if transpose else 0, out=out.data_ptr(), ldo=out.stride(0))
+    check(lib.nvfp4_dequantize(C.byref(a), _stream(stream)), "nvfp4_dequantize")
+    return out
+
+
+def prepare_dgrad(dy, N: int, K: int, *, w=None, wcol=None, dy_global_scale=None,
+                  out_dtype=torch.bfloat16, out=None) -> tuple[Prepared, torch.Tensor]:
+    """dX [M, K] = dY [M, N] W [N, K].  w = (codes [N, K/2], swizzled sf, g): the
+    rowwise packing, dequantized to bf16 (transposed) for a bf16 GEMM; or
+    wcol = (codes [K, N/2], swizzled sf, g): the column packing, for the W4A4
+    GEMM with dY quantized in the call."""
+    lib = load()
+    M = dy.shape[0]
+    if out is None:
+        out = torch.empty((M, K), dtype=out_dtype, device=dy.device)
+    a = DgradArgs(M=M, N=N, K=K, dy=dy.data_ptr(), lddy=dy.stride(0),
+                  out_dtype=OUT_FP32 if out.dtype == torch.float32 else OUT_BF16,
+                  dx=out.data_ptr(), lddx=out.stride(0))
+    keep = [dy, out, dy_global_scale]
+    if w is not None:
+        a.mode = DGRAD_DEQUANT_BF16
+        a.w_codes, a.w_sf, a.w_global_scale = w[0].data_ptr(), w[1].data_ptr(), w[2].data_ptr()
+        keep += list(w)
+    else:
+        a.mode = DGRAD_FP4_COLPACK
+        a.wcol_codes, a.wcol_sf = wcol[0].data_ptr(), wcol[1].data_ptr()
+        a.w_global_scale = wcol[2].data_ptr()
+        keep += list(wcol)
+    if dy_global_scale is not None:
+        a.dy_global_scale = dy_global_scale.data_ptr()
+    ws = _ws(lib.nvfp4_dgrad_workspace_bytes(C.byref(a)), dy.device)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    keep.append(ws)
+    call = Prepared(lib.nvfp4_dgrad, a, keep, "nvfp4_dgrad")
+    call.workspace = ws
+    return call, out
+
+
+def nvfp4_dgrad(dy, N: int, K: int, *, w=None, wcol=None, dy_global_scale=None,
+                out_dtype=torch.bfloat16, out=None, stream=None) -> torch.Tensor:
+    """See prepare_dgrad."""
+    call, out = prepare_dgrad(dy, N, K, w=w, wcol=wcol, dy_global_scale=dy_global_scale,
+                              out_dtype=out_dtype, out=out)
+    call(stream)
+    return out

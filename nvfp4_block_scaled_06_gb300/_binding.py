@@ -26,8 +26,10 @@ EXPORTS = [
     "nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", "nvfp4_codes_bytes",
     "nvfp4_sf_bytes", "nvfp4_status_string", "nvfp4_read_device_status",
     "nvfp4_set_wait_timeout_ns", "nvfp4_version", "nvfp4_quantize_noalloc",
-    "nvfp4_last_cuda_error",
+    "nvfp4_last_cuda_error", "nvfp4_dequantize", "nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes",
 ]
+
+DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK = 0, 1
 
 
 class QuantArgs(C.Structure):
@@ -86,6 +88,32 @@ class LoraArgs(C.Structure):
     ]
 
 
+class DequantArgs(C.Structure):
+    _fields_ = [
+        ("codes", C.c_void_p), ("sf", C.c_void_p),
+        ("sf_layout", C.c_int32),
+        ("global_scale", C.c_void_p),
+        ("rows", C.c_int64), ("cols", C.c_int64),
+        ("transpose", C.c_int32),
+        ("out", C.c_void_p), ("ldo", C.c_int64),
+    ]
+
+
+class DgradArgs(C.Structure):
+    _fields_ = [
+        ("M", C.c_int64), ("N", C.c_int64), ("K", C.c_int64),
+        ("mode", C.c_int32),
+        ("dy", C.c_void_p), ("lddy", C.c_int64),
+        ("w_codes", C.c_void_p), ("w_sf", C.c_void_p),
+        ("wcol_codes", C.c_void_p), ("wcol_sf", C.c_void_p),
+        ("w_global_scale", C.c_void_p), ("dy_global_scale", C.c_void_p),
+        ("out_dtype", C.c_int32),
+        ("dx", C.c_void_p), ("lddx", C.c_int64),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+        ("prof_begin", C.c_void_p), ("prof_end", C.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -106,13 +134,16 @@ def load(path: str | None = None):
     for fn, wsq, st in [("nvfp4_quantize", "nvfp4_quantize_workspace_bytes", QuantArgs),
                         ("nvfp4_gemm", "nvfp4_gemm_workspace_bytes", GemmArgs),
                         ("nvfp4_grouped_gemm", "nvfp4_grouped_workspace_bytes", GroupedArgs),
-                        ("nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", LoraArgs)]:
+                        ("nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", LoraArgs),
+                        ("nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes", DgradArgs)]:
         f = getattr(lib, fn)
         f.argtypes = [C.POINTER(st), vp]
         f.restype = C.c_int
         w = getattr(lib, wsq)
         w.argtypes = [C.POINTER(st)]
         w.restype = C.c_size_t
+    lib.nvfp4_dequantize.argtypes = [C.POINTER(DequantArgs), vp]
+    lib.nvfp4_dequantize.restype = C.c_int
     lib.nvfp4_quantize_noalloc.argtypes = [C.POINTER(QuantArgs), vp]
     lib.nvfp4_quantize_noalloc.restype = C.c_int
     lib.nvfp4_codes_bytes.argtypes = [C.c_int64, C.c_int64]

@@ -679,6 +679,133 @@ nvfp4_status run_lora(const nvfp4_lora_args *a, const LoraPlan &pl, int sms, cud
   return cuda_status(launch_gemm_fp4(p, maps, bn, sms, st));
 }
 
+// ---------------------------------------------------------------- dequant --
+nvfp4_status validate_dequant(const nvfp4_dequant_args *a) {
+  if (!a || !a->codes || !a->sf || !a->global_scale || !a->out) return NVFP4_ERR_INVALID_ARG;
+  if (a->rows < 1 || a->cols < 1) return NVFP4_ERR_INVALID_ARG;
+  if (a->sf_layout != NVFP4_SF_LINEAR && a->sf_layout != NVFP4_SF_SWIZZLED) return NVFP4_ERR_INVALID_ARG;
+  if (a->cols % 64 != 0 || (a->transpose && a->rows % 2 != 0)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->ldo < (a->transpose ? a->rows : a->cols)) return NVFP4_ERR_INVALID_ARG;
+  // transposed rows are written as bf16 pairs (4-byte words), untransposed as 16-byte vectors
+  if (!aligned(a->codes, 16) || !aligned(a->sf, 16) || !aligned(a->out, 16) ||
+      a->ldo % (a->transpose ? 2 : 8) != 0)
+    return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+// ------------------------------------------------------------------ dgrad --
+// A bf16 tensor-core GEMM D[M][Nout] = A[M][Kc] B[Nout][Kc]^T on the FP4 GEMM
+// kernel with no FP4 steps: every pipeline stage is a 64-wide kind::f16 step
+// (the path the LoRA up-projection uses), fp32 accumulation, scale 1.
+nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, int64_t lda, const void *B,
+                           int64_t ldb, void *D, int64_t ldd, int out_fp32, int *status, void *prof_begin,
+                           void *prof_end, int sms, cudaStream_t st) {
+  const uint64_t tmo = g_timeout_ns.load();
+  const int bn = pick_bn(M, Nout, sms);
+  GemmMaps maps;
+  if (!map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, Kc, M, lda * 2, 64, 128) ||
+      !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, Kc, Nout, ldb * 2, 64, bn))
+    return NVFP4_ERR_CUDA;
+  maps.a = maps.t;
+  maps.b = maps.lb;
+  GemmParams p{};
+  p.M = M;
+  p.N = Nout;
+  p.K = 0;
+  p.num_kt = 0;
+  p.nk64 = 0;
+  p.d = D;
+  p.ldd = ldd;
+  p.out_fp32 = out_fp32;
+  p.lora_steps = (int)ceil_div(Kc, 64);
+  p.tiles_m = (int)ceil_div(M, 128);
+  p.tiles_n = (int)ceil_div(Nout, bn);
+  p.ksplit = 1;
+  p.status = status;
+  p.timeout_ns = tmo;
+  p.stall_probe = tmo == 0;
+  if (cudaError_t e_ = mark(prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
+  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  if (e == cudaSuccess) e = mark(prof_end, st);
+  return cuda_status(e);
+}
+
+nvfp4_gemm_args dgrad_as_gemm(const nvfp4_dgrad_args *a) {
+  nvfp4_gemm_args g{};
+  g.M = a->M;
+  g.N = a->K;   // output columns
+  g.K = a->N;   // contraction
+  g.a_bf16 = a->dy;
+  g.lda = a->lddy;
+  g.a_global_scale = a->dy_global_scale;
+  g.b_codes = static_cast<const uint8_t *>(a->wcol_codes);
+  g.b_sf = static_cast<const uint8_t *>(a->wcol_sf);
+  g.b_global_scale = a->w_global_scale;
+  g.out_dtype = a->out_dtype;
+  g.d = a->dx;
+  g.ldd = a->lddx;
+  g.workspace = a->workspace;
+  g.workspace_bytes = a->workspace_bytes;
+  g.prof_begin = a->prof_begin;
+  g.prof_end = a->prof_end;
+  return g;
+}
+
+nvfp4_status validate_dgrad(const nvfp4_dgrad_args *a) {
+  if (!a || !a->dy || !a->dx || !a->w_global_scale) return NVFP4_ERR_INVALID_ARG;
+  if (a->M < 1 || a->N < 1 || a->K < 1 || a->lddy < a->N || a->lddx < a->K) return NVFP4_ERR_INVALID_ARG;
+  if (a->out_dtype != NVFP4_OUT_BF16 && a->out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+  if (a->N % 64 != 0 || a->K % 64 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->M > (1ll << 31) - 256 || a->N > (1ll << 24) || a->K > (1ll << 31) - 256)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->mode == NVFP4_DGRAD_DEQUANT_BF16) {
+    if (!a->w_codes || !a->w_sf) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(a->w_codes, 16) || !aligned(a->w_sf, 16)) return NVFP4_ERR_ALIGNMENT;
+  } else if (a->mode == NVFP4_DGRAD_FP4_COLPACK) {
+    if (!a->wcol_codes || !a->wcol_sf) return NVFP4_ERR_INVALID_ARG;
+    const nvfp4_gemm_args g = dgrad_as_gemm(a);
+    return validate_gemm(&g);
+  } else {
+    return NVFP4_ERR_INVALID_ARG;
+  }
+  if (!aligned(a->dy, 16) || a->lddy % 8 != 0) return NVFP4_ERR_ALIGNMENT;
+  const int64_t dalign = a->out_dtype == NVFP4_OUT_BF16 ? 8 : 4;
+  if (!aligned(a->dx, 16) || a->lddx % dalign != 0) return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+size_t dgrad_workspace(const nvfp4_dgrad_args *a) {
+  if (a->mode == NVFP4_DGRAD_FP4_COLPACK) {
+    nvfp4_gemm_args g = dgrad_as_gemm(a);
+    g.workspace = nullptr;
+    GemmPlan pl;
+    plan_gemm(&g, &pl);
+    return pl.ws;
+  }
+  Carve c(nullptr);
+  c.take<__nv_bfloat16>((size_t)a->K * a->N * 2);   // W^T in bf16
+  return c.off;
+}
+
+nvfp4_status run_dgrad(const nvfp4_dgrad_args *a, int sms, cudaStream_t st) {
+  if (a->mode == NVFP4_DGRAD_FP4_COLPACK) {
+    const nvfp4_gemm_args g = dgrad_as_gemm(a);
+    GemmPlan pl;
+    plan_gemm(&g, &pl);
+    return run_gemm(&g, pl, sms, st);
+  }
+  Carve c(a->workspace);
+  __nv_bfloat16 *wt = c.take<__nv_bfloat16>((size_t)a->K * a->N * 2);
+  if (cudaError_t e_ = launch_dequant(static_cast<const uint8_t *>(a->w_codes),
+                                      static_cast<const uint8_t *>(a->w_sf), 1, a->w_global_scale, a->N,
+                                      a->K, 1, wt, a->N, sms, st);
+      e_ != cudaSuccess)
+    return cuda_status(e_);
+  return run_bf16_gemm(a->M, a->K, a->N, a->dy, a->lddy, wt, a->N, a->dx, a->lddx,
+                       a->out_dtype == NVFP4_OUT_FP32, static_cast<int *>(a->workspace), a->prof_begin,
+                       a->prof_end, sms, st);
+}
+
 }  // namespace
 
 namespace nvfp4 {
@@ -838,6 +965,31 @@ nvfp4_status nvfp4_lora_epilogue(const nvfp4_lora_args *a, nvfp4_stream stream) 
   plan_lora(a, &pl);
   if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
   return run_lora(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_dequantize(const nvfp4_dequant_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_dequant(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  return cuda_status(launch_dequant(static_cast<const uint8_t *>(a->codes), static_cast<const uint8_t *>(a->sf),
+                                    a->sf_layout == NVFP4_SF_SWIZZLED, a->global_scale, a->rows, a->cols,
+                                    a->transpose, static_cast<__nv_bfloat16 *>(a->out), a->ldo, d.sms,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t nvfp4_dgrad_workspace_bytes(const nvfp4_dgrad_args *a) {
+  if (!a) return 0;
+  return dgrad_workspace(a);
+}
+
+nvfp4_status nvfp4_dgrad(const nvfp4_dgrad_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_dgrad(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, dgrad_workspace(a))) != NVFP4_OK) return s;
+  return run_dgrad(a, d.sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -27,15 +27,6 @@ constexpr int kGemvThreads = 256;
 constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lanes x 64
 constexpr int kRows = 4;           // units (rows) a warp has in flight
 
-__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
-  uint32_t r;
-  const uint16_t b = (uint16_t)(byte & 0xFF);
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "h"(b));
-  return r;
-}
-
 // Same block quantizer as the row packing (kept local: tiny X, static scale).
 __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g, float t6g,
                                               uint32_t (&h2)[8], float &sx) {

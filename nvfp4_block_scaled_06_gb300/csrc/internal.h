@@ -47,6 +47,10 @@ nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scr
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
+// NVFP4 -> bf16 (transpose: out[c][r]).
+cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *sf, int sf_swz, const float *g, int64_t rows,
+                           int64_t cols, int transpose, __nv_bfloat16 *out, int64_t ldo, int num_sms,
+                           cudaStream_t st);
 // Token-row codes + linear scales -> expert-grouped rows + swizzled scales.
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
                                  int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,

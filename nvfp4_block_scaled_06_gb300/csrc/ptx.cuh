@@ -359,6 +359,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
   return r & 0xFFu;
 }
+// Two E2M1 codes (low nibble = first element) -> f16x2 (low half = first), exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+  uint32_t r;
+  const uint16_t b = (uint16_t)(byte & 0xFF);
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "h"(b));
+  return r;
+}
 // E4M3 byte -> fp32 (exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   uint32_t h2;

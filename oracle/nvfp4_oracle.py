@@ -47,6 +47,11 @@ R7  The product uses the unquantized bf16 X for the LoRA branch:
     Y = dq(Xq) dq(Wq)^T + (alpha/r) (X A^T) B^T, with A stored [r, K] and B
     stored [N, r] (the Linear-weight layout); fp64 throughout.
 R8  Grouped rows are ordered by expert id, then by (token, slot) index.
+R9  Dequantization to bf16 (the backward's rebuilt weight, [P1] "Why can't
+    we just transpose the one copy?" / "For a frozen QLoRA base") is IEEE
+    fp32 in the quantizer's decode order, s_dec = sb*g then v = E2M1*s_dec,
+    rounded once more to bf16 (nearest, ties to even).  The Dgrad product
+    dX = dY W contracts over N with fp32 accumulation.
 
 Parity of the swizzled layout and nibble order is pinned only through the
 hardware (the tensor core consumes them); everything else is pinned by the
@@ -62,6 +67,7 @@ __all__ = [
     "quantize_colwise", "dequantize", "sf_swizzle", "sf_unswizzle",
     "gemm_fp64", "lora_delta_fp64", "linear_fp64", "error_scale",
     "round_fp64_to_bf16", "bf16_ulp", "group_rows", "grouped_linear_rows",
+    "dequantize_bf16", "f32_to_bf16_rne",
 ]
 
 # ---------------------------------------------------------------------------
@@ -203,6 +209,27 @@ def dequantize(packed: np.ndarray, sf: np.ndarray, g) -> np.ndarray:
     scale = E4M3_VALUES[sf.astype(np.int64)] * float(g)       # [R, C/16]
     elem = (sgn * mag).reshape(R, C // 16, 16)
     return (elem * scale[:, :, None]).reshape(R, C)
+
+
+def f32_to_bf16_rne(v: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, round to nearest, ties to even (finite
+    inputs): add 0x7FFF plus the lowest kept bit, keep the top 16 bits."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep_lsb = (u >> 16) & 1
+    return (((u + 0x7FFF + keep_lsb) >> 16) & 0xFFFF).astype(np.uint16)
+
+
+def dequantize_bf16(packed: np.ndarray, sf: np.ndarray, g) -> np.ndarray:
+    """R9: bf16 bit patterns of fl32(E2M1(code) * fl32(E4M3(sb) * g)).
+
+    ``packed`` [R, C/2] codes (R5), ``sf`` [R, C/16] linear E4M3 codes."""
+    codes = unpack_codes(packed)
+    R, C = codes.shape
+    mag = E2M1_MAGNITUDES[codes & 7].astype(np.float32)
+    elem = np.where(codes & 8, -mag, mag).astype(np.float32)          # sign of code (R4)
+    s_dec = (E4M3_VALUES[sf.astype(np.int64)].astype(np.float32) * _F32(g)).astype(np.float32)
+    v = (elem.reshape(R, C // 16, 16) * s_dec[:, :, None]).astype(np.float32)
+    return f32_to_bf16_rne(v.reshape(R, C))
 
 
 # ---------------------------------------------------------------------------

@@ -34,6 +34,8 @@ Recipes (shapes and distributions follow the pages' layers: hidden 6144,
              routing logits N(0,1)[4096,256] plus bias_e = -1.1*ln(rank_e)
              (rank_e a seeded permutation of 1..256: the log of a Zipf(1.1)
              pmf), top-8 per token by logit, ties to the lower expert id.
+* dgrad:     the backward of the prefill linear: W[2048,6144] ~N(0,0.02),
+             dY[8192,2048] ~N(0,0.01) (gradient-sized values).
 """
 from __future__ import annotations
 
@@ -54,6 +56,8 @@ CONFIGS = {
     "quantize": dict(E=32, N=2048, K=6144),
     "prefill": dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0),
     "grouped": dict(T=4096, E=256, topk=8, N=2048, K=6144, rank=64, alpha=128.0),
+    # the backward of the prefill linear: dX [M, K] = dY [M, N] W [N, K]
+    "dgrad": dict(M=8192, N=2048, K=6144),
 }
 
 
@@ -166,6 +170,11 @@ def make_case(name: str, seed: int = 0, **over) -> dict:
         a = d.normal_bf16((c["rank"], c["K"]), 0.01)
         b = d.normal_bf16((c["N"], c["rank"]), 0.01)
         return dict(x=x, w=w, lora_a=a, lora_b=b, **c)
+    if name == "dgrad":
+        c = dict(CONFIGS["dgrad"], **over)
+        w = d.normal_bf16((c["N"], c["K"]), 0.02)
+        dy = d.normal_bf16((c["M"], c["N"]), 0.01)
+        return dict(w=w, dy=dy, **c)
     if name == "grouped":
         c = dict(CONFIGS["grouped"], **over)
         x = d.normal_bf16((c["T"], c["K"]), 1.0)
@@ -256,6 +265,10 @@ def torch_case(name: str, seed: int = 0, device="cuda", **over) -> dict:
                     lora_a=torch_normal_bf16((c["E"], c["rank"], c["K"]), 0.01, gen, device),
                     lora_b=torch_normal_bf16((c["E"], c["N"], c["rank"]), 0.01, gen, device),
                     expert_ids=torch_route_top_k(c["T"], c["E"], c["topk"], gen, device), **c)
+    if name == "dgrad":
+        c = dict(CONFIGS["dgrad"], **over)
+        return dict(w=torch_normal_bf16((c["N"], c["K"]), 0.02, gen, device),
+                    dy=torch_normal_bf16((c["M"], c["N"]), 0.01, gen, device), **c)
     if name == "quantize":
         c = dict(CONFIGS["quantize"], **over)
         w = torch_normal_bf16((c["E"], c["N"], c["K"]), 0.02, gen, device)

@@ -304,3 +304,67 @@ def test_group_rows_matches_brute_force():
     assert offsets[-1] == ids.size
     # every token's slots hold distinct experts
     assert all(len(set(r)) == r.size for r in ids)
+
+
+# --- dequantization to bf16 (the backward's rebuilt weight) ---------------------
+
+def test_bf16_rne_matches_torch():
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    v[:8] = [0.0, -0.0, 1.0, 1.00390625, 1.005859375, 1.01171875, -3.0, 65504.0]   # ties included
+    want = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(o.f32_to_bf16_rne(v), want)
+
+
+def test_dequantize_bf16_exact_when_scales_are_powers_of_two():
+    # g a power of two: every fp32 product is exact, so the bf16 result is the
+    # nearest bf16 of the exact value (an independent rounding routine)
+    rng = np.random.default_rng(22)
+    R, C = 64, 256
+    w = f32_to_bf16_bits((rng.standard_normal((R, C)) * 0.05).astype(np.float32))
+    codes, sf, _ = o.quantize(w, np.float32(2.0 ** -12))
+    got = o.dequantize_bf16(codes, sf, np.float32(2.0 ** -12))
+    exact = o.dequantize(codes, sf, 2.0 ** -12)
+    want = o.f32_to_bf16_rne(exact.astype(np.float32))     # exact in fp32 (<= 7 significant bits)
+    assert np.array_equal(got, want)
+    assert np.array_equal(bf16_bits_to_f32(got).astype(np.float64), exact)
+
+
+def test_dequantize_bf16_within_two_roundings_for_any_scale():
+    rng = np.random.default_rng(23)
+    R, C = 32, 512
+    w = f32_to_bf16_bits((rng.standard_normal((R, C)) * 0.3).astype(np.float32))
+    codes, sf, g = o.quantize(w)                              # g = amax / 2688, not a power of two
+    got = bf16_bits_to_f32(o.dequantize_bf16(codes, sf, g)).astype(np.float64)
+    exact = o.dequantize(codes, sf, g)
+    # fp32 rounding of s_dec and of the product (2 x 2^-24), then bf16 (2^-8)
+    bound = np.abs(exact) * (2.0 ** -8 + 3 * 2.0 ** -24) + 1e-45
+    assert np.all(np.abs(got - exact) <= bound)
+    assert np.mean(got == exact) < 1.0                       # the roundings do act
+
+
+def test_dequantize_bf16_requantizes_to_the_same_codes():
+    # grid-representable tensor (power-of-two g): dequantize then quantize is the identity
+    rng = np.random.default_rng(24)
+    R, C = 48, 128
+    g = np.float32(2.0 ** -9)
+    sfc = rng.integers(1, 127, size=(R, C // 16)).astype(np.uint8)
+    mag = rng.integers(0, 8, size=(R, C))
+    mag.reshape(R, C // 16, 16)[:, :, 0] = 7                  # each block reaches 6 * sb
+    sign = rng.integers(0, 2, size=(R, C))
+    vals = (np.where(sign, -1.0, 1.0) * o.E2M1_MAGNITUDES[mag]).reshape(R, C // 16, 16)
+    x = (vals * o.E4M3_VALUES[sfc][:, :, None] * float(g)).reshape(R, C)
+    codes, sf, _ = o.quantize(f32_to_bf16_bits(x.astype(np.float32)), g)
+    back = o.dequantize_bf16(codes, sf, g)
+    codes2, sf2, _ = o.quantize(back, g)
+    assert np.array_equal(codes2, codes) and np.array_equal(sf2, sf)
+
+
+def test_dequantize_bf16_signed_zero_and_zero_scale():
+    codes = np.zeros((1, 8), np.uint8)
+    codes[0, 0] = 0x08 | (0x01 << 4)      # element 0 = -0, element 1 = +0.5
+    sf = np.array([[56]], np.uint8)       # E4M3 code 56 = 1.0
+    out = o.dequantize_bf16(codes, sf, np.float32(1.0))
+    assert out[0, 0] == 0x8000 and out[0, 1] == 0x3F00 and np.all(out[0, 2:] == 0)
+    out0 = o.dequantize_bf16(codes, np.array([[0]], np.uint8), np.float32(1.0))
+    assert out0[0, 1] == 0 and out0[0, 0] == 0x8000   # zero scale: +-0 by the code's sign
