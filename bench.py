@@ -354,8 +354,23 @@ def run_dgrad(torch, nv, device, steps, warmup, pk):
                          gemm_tflops=flops / (kms * 1e-3) / 1e12,
                          gemm_frac=flops / (kms * 1e-3) / 1e12 / peak,
                          pre_ms=ms - kms)
-    out["workload"] = f"dX[{M},{K}] = dY[{M},{N}] W[{N},{K}] (prefill linear backward), bf16 out"
-    out["note"] = ("pre_ms = dequantization (bf16 mode) or dY quantization (fp4 mode); "
+    # the weight-gradient product on the FP4 datapath: dW[N,K] = dY^T X, both packed along M
+    x = torch_case("prefill", seed=1, device=device)["x"]
+    call, dw = nv.prepare_wgrad(c["dy"], x)
+    prof = ev_pairs(torch, steps)
+
+    def wstep(i, pr):
+        arm(C, call.args, pr)
+        call()
+    ms = time_loop(torch, wstep, steps, warmup, prof)
+    kms = mean_ms(prof)
+    out["wgrad_fp4"] = dict(ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+                            gemm_tflops=flops / (kms * 1e-3) / 1e12,
+                            gemm_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16_sustained"] * FP4_PER_BF16),
+                            pre_ms=ms - kms)
+    out["workload"] = (f"dX[{M},{K}] = dY[{M},{N}] W[{N},{K}] and dW[{N},{K}] = dY^T X[{M},{K}] "
+                       f"(prefill linear backward), bf16 out")
+    out["note"] = ("pre_ms = dequantization (bf16 mode) or the in-call quantizations (fp4 modes); "
                    "gemm_frac against the sustained bf16 / 6x bf16 peak")
     return out
 

@@ -320,6 +320,40 @@ nvfp4_status nvfp4_dgrad(const nvfp4_dgrad_args *args, nvfp4_stream stream);
 size_t nvfp4_dgrad_workspace_bytes(const nvfp4_dgrad_args *args);
 
 /* ------------------------------------------------------------------------ *
+ * nvfp4_wgrad -- weight-gradient product on the FP4 datapath: dW = dY^T X.
+ *
+ * The contraction runs over the M tokens, so both operands need blocks of 16
+ * along M: the columnwise packing of the activations and of the output
+ * gradient (the layout the weight-gradient GEMM prefers, "Going deeper: why a
+ * 4-bit weight needs two copies"; the per-axis blocking of "Why can't we just
+ * transpose the one copy?").  dY bf16 [M][N] (lddy) and X bf16 [M][K] (ldx)
+ * are quantized in the call (nvfp4_quantize pack=COL: dynamic amax, or the
+ * given static scales), then dW [N][K] (lddw) = the W4A4 GEMM of the two
+ * column packings (nvfp4_gemm's arithmetic).
+ * Requirements: M % 32 == 0, N % 16 == 0, K % 16 == 0; dy, x 16-byte aligned
+ *   with lddy, ldx % 8 == 0; dw 16-byte aligned, lddw % 8 (bf16) or % 4 (fp32).
+ * Workspace: nvfp4_wgrad_workspace_bytes(&args).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int64_t M, N, K;
+  const void *dy;                /* bf16 [M][lddy] */
+  int64_t lddy;
+  const void *x;                 /* bf16 [M][ldx] */
+  int64_t ldx;
+  const float *dy_global_scale;  /* NULL = dynamic */
+  const float *x_global_scale;   /* NULL = dynamic */
+  int32_t out_dtype;             /* nvfp4_out_dtype */
+  void *dw;
+  int64_t lddw;
+  void *workspace;
+  size_t workspace_bytes;
+  void *prof_begin, *prof_end;   /* optional cudaEvent_t pair around the GEMM */
+} nvfp4_wgrad_args;
+
+nvfp4_status nvfp4_wgrad(const nvfp4_wgrad_args *args, nvfp4_stream stream);
+size_t nvfp4_wgrad_workspace_bytes(const nvfp4_wgrad_args *args);
+
+/* ------------------------------------------------------------------------ *
  * Size queries and status.
  * ------------------------------------------------------------------------ */
 /* Bytes of packed codes of a [rows][cols] matrix: rows * cols / 2. */

@@ -14,15 +14,15 @@ import torch
 
 from ._binding import (DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK, EXPORTS, DequantArgs, DgradArgs,
                        GemmArgs, GroupedArgs, LoraArgs, NVFP4Error, OUT_BF16, OUT_FP32,
-                       PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR, SF_SWIZZLED, check,
-                       load)
+                       PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR, SF_SWIZZLED, WgradArgs,
+                       check, load)
 
 __all__ = [
     "load", "NVFP4Error", "nvfp4_quantize", "nvfp4_gemm", "nvfp4_grouped_gemm",
     "nvfp4_lora_epilogue", "nvfp4_codes_bytes", "nvfp4_sf_bytes", "read_device_status",
     "set_wait_timeout_ns", "Prepared", "prepare_gemm", "prepare_quantize", "prepare_grouped",
     "SF_LINEAR", "SF_SWIZZLED", "PACK_ROW", "PACK_COL", "PACK_BOTH", "EXPORTS",
-    "nvfp4_dequantize", "nvfp4_dgrad", "prepare_dgrad",
+    "nvfp4_dequantize", "nvfp4_dgrad", "prepare_dgrad", "nvfp4_wgrad", "prepare_wgrad",
 ]
 
 _PACK = {"row": PACK_ROW, "col": PACK_COL, "both": PACK_BOTH}
@@ -291,5 +291,39 @@ def nvfp4_dgrad(dy, N: int, K: int, *, w=None, wcol=None, dy_global_scale=None,
     """See prepare_dgrad."""
     call, out = prepare_dgrad(dy, N, K, w=w, wcol=wcol, dy_global_scale=dy_global_scale,
                               out_dtype=out_dtype, out=out)
+    call(stream)
+    return out
+
+
+def prepare_wgrad(dy, x, *, dy_global_scale=None, x_global_scale=None, out_dtype=torch.bfloat16,
+                  out=None) -> tuple[Prepared, torch.Tensor]:
+    """dW [N, K] = dY[M, N]^T X[M, K] on the FP4 datapath (both operands packed
+    along M in the call)."""
+    lib = load()
+    M, N = dy.shape
+    K = x.shape[1]
+    if out is None:
+        out = torch.empty((N, K), dtype=out_dtype, device=dy.device)
+    a = WgradArgs(M=M, N=N, K=K, dy=dy.data_ptr(), lddy=dy.stride(0), x=x.data_ptr(),
+                  ldx=x.stride(0), out_dtype=OUT_FP32 if out.dtype == torch.float32 else OUT_BF16,
+                  dw=out.data_ptr(), lddw=out.stride(0))
+    if dy_global_scale is not None:
+        a.dy_global_scale = dy_global_scale.data_ptr()
+    if x_global_scale is not None:
+        a.x_global_scale = x_global_scale.data_ptr()
+    keep = [dy, x, out, dy_global_scale, x_global_scale]
+    ws = _ws(lib.nvfp4_wgrad_workspace_bytes(C.byref(a)), dy.device)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    keep.append(ws)
+    call = Prepared(lib.nvfp4_wgrad, a, keep, "nvfp4_wgrad")
+    call.workspace = ws
+    return call, out
+
+
+def nvfp4_wgrad(dy, x, *, dy_global_scale=None, x_global_scale=None, out_dtype=torch.bfloat16,
+                out=None, stream=None) -> torch.Tensor:
+    """See prepare_wgrad."""
+    call, out = prepare_wgrad(dy, x, dy_global_scale=dy_global_scale,
+                              x_global_scale=x_global_scale, out_dtype=out_dtype, out=out)
     call(stream)
     return out

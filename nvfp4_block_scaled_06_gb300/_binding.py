@@ -27,6 +27,7 @@ EXPORTS = [
     "nvfp4_sf_bytes", "nvfp4_status_string", "nvfp4_read_device_status",
     "nvfp4_set_wait_timeout_ns", "nvfp4_version", "nvfp4_quantize_noalloc",
     "nvfp4_last_cuda_error", "nvfp4_dequantize", "nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes",
+    "nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes",
 ]
 
 DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK = 0, 1
@@ -114,6 +115,19 @@ class DgradArgs(C.Structure):
     ]
 
 
+class WgradArgs(C.Structure):
+    _fields_ = [
+        ("M", C.c_int64), ("N", C.c_int64), ("K", C.c_int64),
+        ("dy", C.c_void_p), ("lddy", C.c_int64),
+        ("x", C.c_void_p), ("ldx", C.c_int64),
+        ("dy_global_scale", C.c_void_p), ("x_global_scale", C.c_void_p),
+        ("out_dtype", C.c_int32),
+        ("dw", C.c_void_p), ("lddw", C.c_int64),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+        ("prof_begin", C.c_void_p), ("prof_end", C.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -135,7 +149,8 @@ def load(path: str | None = None):
                         ("nvfp4_gemm", "nvfp4_gemm_workspace_bytes", GemmArgs),
                         ("nvfp4_grouped_gemm", "nvfp4_grouped_workspace_bytes", GroupedArgs),
                         ("nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", LoraArgs),
-                        ("nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes", DgradArgs)]:
+                        ("nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes", DgradArgs),
+                        ("nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes", WgradArgs)]:
         f = getattr(lib, fn)
         f.argtypes = [C.POINTER(st), vp]
         f.restype = C.c_int

@@ -806,6 +806,122 @@ nvfp4_status run_dgrad(const nvfp4_dgrad_args *a, int sms, cudaStream_t st) {
                        a->prof_end, sms, st);
 }
 
+// ------------------------------------------------------------------ wgrad --
+struct WgradPlan {
+  size_t ws = 0;
+  uint8_t *dy_codes = nullptr, *dy_sf = nullptr, *x_codes = nullptr, *x_sf = nullptr;
+  float *g_dy = nullptr, *g_x = nullptr;
+  uint8_t *q_dy_ws = nullptr, *q_x_ws = nullptr, *gemm_ws = nullptr;
+  size_t q_dy_bytes = 0, q_x_bytes = 0, gemm_bytes = 0;
+};
+
+nvfp4_quant_args wgrad_quant(const void *src, int64_t M, int64_t cols, int64_t ld, const float *g_in,
+                             float *g_out, uint8_t *codes, uint8_t *sf, void *ws, size_t ws_bytes) {
+  nvfp4_quant_args q{};
+  q.src = src;
+  q.batch = 1;
+  q.rows = M;
+  q.cols = cols;
+  q.ld = ld;
+  q.pack = NVFP4_PACK_COL;
+  q.sf_layout = NVFP4_SF_SWIZZLED;
+  q.global_scale_in = g_in;
+  q.global_scale_out = g_out;
+  q.codes_col = codes;
+  q.sf_col = sf;
+  q.workspace = ws;
+  q.workspace_bytes = ws_bytes;
+  return q;
+}
+
+nvfp4_gemm_args wgrad_gemm(const nvfp4_wgrad_args *a, const WgradPlan &pl) {
+  nvfp4_gemm_args g{};
+  g.M = a->N;   // rows of dW
+  g.N = a->K;   // columns of dW
+  g.K = a->M;   // contraction over the tokens
+  g.a_codes = pl.dy_codes;
+  g.a_sf = pl.dy_sf;
+  g.a_global_scale = pl.g_dy;
+  g.b_codes = pl.x_codes;
+  g.b_sf = pl.x_sf;
+  g.b_global_scale = pl.g_x;
+  g.out_dtype = a->out_dtype;
+  g.d = a->dw;
+  g.ldd = a->lddw;
+  g.workspace = pl.gemm_ws;
+  g.workspace_bytes = pl.gemm_bytes;
+  g.prof_begin = a->prof_begin;
+  g.prof_end = a->prof_end;
+  return g;
+}
+
+void plan_wgrad(const nvfp4_wgrad_args *a, WgradPlan *pl) {
+  Carve c(a->workspace);
+  pl->dy_codes = c.take<uint8_t>((size_t)a->N * a->M / 2);
+  pl->dy_sf = c.take<uint8_t>(sf_swizzled_bytes(a->N, a->M));
+  pl->g_dy = c.take<float>(4);
+  pl->x_codes = c.take<uint8_t>((size_t)a->K * a->M / 2);
+  pl->x_sf = c.take<uint8_t>(sf_swizzled_bytes(a->K, a->M));
+  pl->g_x = c.take<float>(4);
+  {
+    nvfp4_quant_args q = wgrad_quant(a->dy, a->M, a->N, a->lddy, a->dy_global_scale, pl->g_dy, pl->dy_codes,
+                                     pl->dy_sf, nullptr, 0);
+    QuantPlan qp;
+    plan_quantize(&q, &qp);
+    pl->q_dy_bytes = qp.ws;
+    pl->q_dy_ws = c.take<uint8_t>(qp.ws);
+  }
+  {
+    nvfp4_quant_args q = wgrad_quant(a->x, a->M, a->K, a->ldx, a->x_global_scale, pl->g_x, pl->x_codes,
+                                     pl->x_sf, nullptr, 0);
+    QuantPlan qp;
+    plan_quantize(&q, &qp);
+    pl->q_x_bytes = qp.ws;
+    pl->q_x_ws = c.take<uint8_t>(qp.ws);
+  }
+  {
+    nvfp4_gemm_args g = wgrad_gemm(a, *pl);
+    g.workspace = nullptr;
+    GemmPlan gp;
+    plan_gemm(&g, &gp);
+    pl->gemm_bytes = gp.ws;
+    pl->gemm_ws = c.take<uint8_t>(gp.ws);
+  }
+  pl->ws = c.off;
+}
+
+nvfp4_status validate_wgrad(const nvfp4_wgrad_args *a) {
+  if (!a || !a->dy || !a->x || !a->dw) return NVFP4_ERR_INVALID_ARG;
+  if (a->M < 1 || a->N < 1 || a->K < 1 || a->lddy < a->N || a->ldx < a->K || a->lddw < a->K)
+    return NVFP4_ERR_INVALID_ARG;
+  if (a->out_dtype != NVFP4_OUT_BF16 && a->out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
+  if (a->M % 32 != 0 || a->N % 16 != 0 || a->K % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->M > (1ll << 24) || a->N > (1ll << 31) - 256 || a->K > (1ll << 31) - 256)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(a->dy, 16) || !aligned(a->x, 16) || a->lddy % 8 != 0 || a->ldx % 8 != 0)
+    return NVFP4_ERR_ALIGNMENT;
+  const int64_t dalign = a->out_dtype == NVFP4_OUT_BF16 ? 8 : 4;
+  if (!aligned(a->dw, 16) || a->lddw % dalign != 0) return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_wgrad(const nvfp4_wgrad_args *a, const WgradPlan &pl, int sms, cudaStream_t st) {
+  const nvfp4_quant_args qd = wgrad_quant(a->dy, a->M, a->N, a->lddy, a->dy_global_scale, pl.g_dy, pl.dy_codes,
+                                          pl.dy_sf, pl.q_dy_ws, pl.q_dy_bytes);
+  const nvfp4_quant_args qx = wgrad_quant(a->x, a->M, a->K, a->ldx, a->x_global_scale, pl.g_x, pl.x_codes,
+                                          pl.x_sf, pl.q_x_ws, pl.q_x_bytes);
+  nvfp4_status s;
+  QuantPlan qp;
+  plan_quantize(&qd, &qp);
+  if ((s = run_quantize(&qd, qp, sms, st)) != NVFP4_OK) return s;
+  plan_quantize(&qx, &qp);
+  if ((s = run_quantize(&qx, qp, sms, st)) != NVFP4_OK) return s;
+  const nvfp4_gemm_args g = wgrad_gemm(a, pl);
+  GemmPlan gp;
+  plan_gemm(&g, &gp);
+  return run_gemm(&g, gp, sms, st);
+}
+
 }  // namespace
 
 namespace nvfp4 {
@@ -990,6 +1106,26 @@ nvfp4_status nvfp4_dgrad(const nvfp4_dgrad_args *a, nvfp4_stream stream) {
   if ((s = device_info(&d)) != NVFP4_OK) return s;
   if ((s = check_workspace(a->workspace, a->workspace_bytes, dgrad_workspace(a))) != NVFP4_OK) return s;
   return run_dgrad(a, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_wgrad_workspace_bytes(const nvfp4_wgrad_args *a) {
+  if (!a) return 0;
+  nvfp4_wgrad_args c = *a;
+  c.workspace = nullptr;
+  WgradPlan pl;
+  plan_wgrad(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_wgrad(const nvfp4_wgrad_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_wgrad(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  WgradPlan pl;
+  plan_wgrad(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_wgrad(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,4 +1,4 @@
-"""nvfp4_dequantize and nvfp4_dgrad on the GPU against the oracle.
+"""nvfp4_dequantize, nvfp4_dgrad and nvfp4_wgrad on the GPU against the oracle.
 
 Dequantization is bit-exact (the oracle's fp32 decode order, then bf16).  The
 Dgrad products are checked like the forward GEMM: fp32 out |dX - dX_or| <=
@@ -102,3 +102,30 @@ def test_dgrad_full_size_sampled_rows():
     dyq = o.quantize(dyb, gdy)
     wq = o.quantize_colwise(wb, g)
     assert_gemm_close(dx2[ridx], o.linear_fp64(dyq, wq), o.error_scale(dyq, wq), what="dgrad fp4 full")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (96, 208, 640), (544, 128, 48)])
+def test_wgrad_fp4(M, N, K, out_dtype):
+    """dW = dY^T X with both operands quantized along M (their column packings)."""
+    rng = np.random.default_rng(M + N + K)
+    dy = f32_to_bf16_bits((rng.standard_normal((M, N)) * 0.01).astype(np.float32))
+    x = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    dw = nv.nvfp4_wgrad(dev_bf16(dy), dev_bf16(x), out_dtype=out_dtype)
+    a = o.quantize_colwise(dy)       # dY^T [N, M], blocks along M
+    b = o.quantize_colwise(x)        # X^T  [K, M]
+    assert_gemm_close(dw, o.linear_fp64(a, b), o.error_scale(a, b), what=f"wgrad {M}x{N}x{K}")
+
+
+def test_wgrad_static_scales():
+    rng = np.random.default_rng(31)
+    M, N, K = 128, 256, 256
+    dy = f32_to_bf16_bits((rng.standard_normal((M, N)) * 0.01).astype(np.float32))
+    x = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    gdy, gx = np.float32(0.05 / 2688), np.float32(4.0 / 2688)
+    dw = nv.nvfp4_wgrad(dev_bf16(dy), dev_bf16(x), out_dtype=torch.float32,
+                        dy_global_scale=torch.tensor([float(gdy)], device="cuda"),
+                        x_global_scale=torch.tensor([float(gx)], device="cuda"))
+    a = o.quantize_colwise(dy, gdy)
+    b = o.quantize_colwise(x, gx)
+    assert_gemm_close(dw, o.linear_fp64(a, b), o.error_scale(a, b), what="wgrad static")
