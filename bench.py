@@ -375,6 +375,42 @@ def run_dgrad(torch, nv, device, steps, warmup, pk):
     return out
 
 
+def run_moe_down(torch, nv, device, steps, warmup, pk):
+    """The routed experts' down-projection W2_e[6144,2048] + gate-weighted combine
+    for 4096 tokens x top-8 (the grouped up-projection's successor)."""
+    import ctypes as C
+    from synth import torch_case
+    c = torch_case("moe_down", seed=0, device=device)
+    E, N, K, T, k = c["E"], c["N"], c["K"], c["T"], c["topk"]
+    wq = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
+    del c["w"]
+    torch.cuda.empty_cache()
+    flat = c["expert_ids"].reshape(-1).long()
+    perm = torch.sort(flat, stable=True).indices.to(torch.int32)
+    counts = torch.bincount(flat, minlength=E)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=device)
+    offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    lora = dict(a=c["lora_a"], b=c["lora_b"], alpha=c["alpha"])
+    call, y = nv.prepare_moe_down(c["h"], perm, offsets, c["route_weights"], wq["codes_row"],
+                                  wq["sf_row"], wq["global_scale"], N, K, E, lora=lora)
+    prof = ev_pairs(torch, steps)
+
+    def step(i, pr):
+        arm(C, call.args, pr)
+        call()
+    ms = time_loop(torch, step, steps, warmup, prof)
+    kms = mean_ms(prof)
+    active = int((counts > 0).sum())
+    P = T * k
+    flops = 2.0 * P * N * K
+    wbytes = active * N * K * 0.5625
+    return dict(workload=f"{T} tokens x top-{k}: down-projection of {E} experts W2_e[{N},{K}] + LoRA "
+                         f"r{c['rank']} + gate-weighted combine -> y[{T},{N}]",
+                ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+                gemm_tflops=flops / (kms * 1e-3) / 1e12,
+                gemm_weight_gbs=wbytes / (kms * 1e-3) / 1e9, active_experts=active)
+
+
 # ----------------------------------------------------------- CPU baseline --
 def cpu_baseline(rows: int = 96):
     """The oracle on a row sample of the headline workload (host cores)."""
@@ -422,7 +458,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--only-main", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--only", choices=["quantize", "decode", "grouped", "dgrad"],
+    ap.add_argument("--only", choices=["quantize", "decode", "grouped", "dgrad", "moe_down"],
                     help="run just this secondary workload (for profiling) and print its numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     args = ap.parse_args()
@@ -447,7 +483,7 @@ def main():
 
     if args.only:
         fn = dict(quantize=run_quantize_sweep, decode=run_decode, grouped=run_grouped,
-                  dgrad=run_dgrad)[args.only]
+                  dgrad=run_dgrad, moe_down=run_moe_down)[args.only]
         res = fn(torch, nv, device, args.steps, args.warmup, pk)
         if rank == 0:
             print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, **res}))
@@ -464,6 +500,8 @@ def main():
         sec["grouped"] = run_grouped(torch, nv, device, steps2, max(3, args.warmup), pk)
         torch.cuda.empty_cache()
         sec["dgrad"] = run_dgrad(torch, nv, device, steps2, max(3, args.warmup), pk)
+        torch.cuda.empty_cache()
+        sec["moe_down"] = run_moe_down(torch, nv, device, steps2, max(3, args.warmup), pk)
         torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:

@@ -354,6 +354,48 @@ nvfp4_status nvfp4_wgrad(const nvfp4_wgrad_args *args, nvfp4_stream stream);
 size_t nvfp4_wgrad_workspace_bytes(const nvfp4_wgrad_args *args);
 
 /* ------------------------------------------------------------------------ *
+ * nvfp4_moe_down_combine -- routed-expert down-projection and combine.
+ *
+ * Completes the routed expert FFN after nvfp4_grouped_gemm (256 routed
+ * experts, 8 per token: "GLM-5.2-NVFP4" model card; an expert's contribution
+ * is weighted by its gate weight: the REAP saliency gate_weight x
+ * ||expert_output|| on the "vroomfondel/glm-5.2-reap-504B-v2-W4A4" card):
+ *   h      bf16 [P = num_tokens*top_k][K], the (activated) up-projection
+ *          output in the expert-grouped order nvfp4_grouped_gemm produced;
+ *   D[i]   = W4A4(h_i, W_e) [+ LoRA_e] for grouped row i of expert e, with h
+ *          quantized once with one tensor-wide g (dynamic amax, or
+ *          h_global_scale), stored as bf16;
+ *   y[t]   = sum over slots j = 0..top_k-1, in order, of
+ *            route_weights[t][j] * D[row of pair t*top_k + j], fp32 (one
+ *            fused multiply-add per slot), rounded once to bf16.
+ * perm and expert_offsets are nvfp4_grouped_gemm's perm_out and
+ * expert_offsets_out.  W_e: stacked codes [E][N][K/2], swizzled scales over
+ * [E*N][K/16], global scales [E]; optional LoRA A [E][rank][K], B [E][N][rank].
+ * Requirements: N % 256 == 0, K % 32 == 0; as nvfp4_grouped_gemm otherwise.
+ * Workspace: nvfp4_moe_down_workspace_bytes(&args).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int64_t num_tokens, top_k, num_experts, N, K;
+  const void *h;                 /* bf16 [num_tokens*top_k][K], expert-grouped rows */
+  const int32_t *perm;           /* [P]: grouped row -> token*top_k + slot */
+  const int32_t *expert_offsets; /* [E+1] */
+  const float *route_weights;    /* [num_tokens][top_k] */
+  const float *h_global_scale;   /* NULL = dynamic */
+  const void *w_codes, *w_sf;
+  const float *w_global_scale;   /* [E] */
+  const void *lora_a, *lora_b;   /* NULL = no LoRA */
+  int32_t rank;
+  float alpha;
+  void *y;                       /* bf16 [num_tokens][N] */
+  void *workspace;
+  size_t workspace_bytes;
+  void *prof_begin, *prof_end;   /* optional cudaEvent_t pair around the grouped GEMM */
+} nvfp4_moe_down_args;
+
+nvfp4_status nvfp4_moe_down_combine(const nvfp4_moe_down_args *args, nvfp4_stream stream);
+size_t nvfp4_moe_down_workspace_bytes(const nvfp4_moe_down_args *args);
+
+/* ------------------------------------------------------------------------ *
  * Size queries and status.
  * ------------------------------------------------------------------------ */
 /* Bytes of packed codes of a [rows][cols] matrix: rows * cols / 2. */

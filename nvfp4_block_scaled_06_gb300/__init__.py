@@ -13,7 +13,7 @@ import ctypes as C
 import torch
 
 from ._binding import (DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK, EXPORTS, DequantArgs, DgradArgs,
-                       GemmArgs, GroupedArgs, LoraArgs, NVFP4Error, OUT_BF16, OUT_FP32,
+                       GemmArgs, GroupedArgs, LoraArgs, MoeDownArgs, NVFP4Error, OUT_BF16, OUT_FP32,
                        PACK_BOTH, PACK_COL, PACK_ROW, QuantArgs, SF_LINEAR, SF_SWIZZLED, WgradArgs,
                        check, load)
 
@@ -23,6 +23,7 @@ __all__ = [
     "set_wait_timeout_ns", "Prepared", "prepare_gemm", "prepare_quantize", "prepare_grouped",
     "SF_LINEAR", "SF_SWIZZLED", "PACK_ROW", "PACK_COL", "PACK_BOTH", "EXPORTS",
     "nvfp4_dequantize", "nvfp4_dgrad", "prepare_dgrad", "nvfp4_wgrad", "prepare_wgrad",
+    "nvfp4_moe_down_combine", "prepare_moe_down",
 ]
 
 _PACK = {"row": PACK_ROW, "col": PACK_COL, "both": PACK_BOTH}
@@ -325,5 +326,49 @@ def nvfp4_wgrad(dy, x, *, dy_global_scale=None, x_global_scale=None, out_dtype=t
     """See prepare_wgrad."""
     call, out = prepare_wgrad(dy, x, dy_global_scale=dy_global_scale,
                               x_global_scale=x_global_scale, out_dtype=out_dtype, out=out)
+    call(stream)
+    return out
+
+
+# ------------------------------------------------------------ MoE down-proj --
+
+def prepare_moe_down(h, perm, expert_offsets, route_weights, w_codes, w_sf, w_global_scale,
+                     N: int, K: int, num_experts: int, h_global_scale=None, lora=None,
+                     out=None) -> tuple[Prepared, torch.Tensor]:
+    """y [T, N] = sum_j route_weights[t, j] * W4A4(h[grouped row of (t, j)], W2_e).
+
+    h: bf16 [T*k, K] in the expert-grouped order of nvfp4_grouped_gemm's output;
+    perm / expert_offsets: that call's permutation and offsets; route_weights
+    fp32 [T, k]; W2 stacked codes [E, N, K/2], swizzled scales, [E] global scales."""
+    lib = load()
+    T, k = route_weights.shape
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=h.device)
+    a = MoeDownArgs(num_tokens=T, top_k=k, num_experts=num_experts, N=N, K=K, h=h.data_ptr(),
+                    perm=perm.data_ptr(), expert_offsets=expert_offsets.data_ptr(),
+                    route_weights=route_weights.data_ptr(),
+                    h_global_scale=None if h_global_scale is None else h_global_scale.data_ptr(),
+                    w_codes=w_codes.data_ptr(), w_sf=w_sf.data_ptr(),
+                    w_global_scale=w_global_scale.data_ptr(), y=out.data_ptr())
+    keep = [h, perm, expert_offsets, route_weights, h_global_scale, w_codes, w_sf, w_global_scale,
+            out]
+    if lora is not None:
+        a.lora_a, a.lora_b = lora["a"].data_ptr(), lora["b"].data_ptr()
+        a.rank, a.alpha = lora["a"].shape[1], float(lora["alpha"])
+        keep += [lora["a"], lora["b"]]
+    ws = _ws(lib.nvfp4_moe_down_workspace_bytes(C.byref(a)), h.device)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    keep.append(ws)
+    call = Prepared(lib.nvfp4_moe_down_combine, a, keep, "nvfp4_moe_down_combine")
+    call.workspace = ws
+    return call, out
+
+
+def nvfp4_moe_down_combine(h, perm, expert_offsets, route_weights, w_codes, w_sf, w_global_scale,
+                           N: int, K: int, num_experts: int, h_global_scale=None, lora=None,
+                           out=None, stream=None) -> torch.Tensor:
+    """See prepare_moe_down."""
+    call, out = prepare_moe_down(h, perm, expert_offsets, route_weights, w_codes, w_sf,
+                                 w_global_scale, N, K, num_experts, h_global_scale, lora, out)
     call(stream)
     return out

@@ -27,7 +27,8 @@ EXPORTS = [
     "nvfp4_sf_bytes", "nvfp4_status_string", "nvfp4_read_device_status",
     "nvfp4_set_wait_timeout_ns", "nvfp4_version", "nvfp4_quantize_noalloc",
     "nvfp4_last_cuda_error", "nvfp4_dequantize", "nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes",
-    "nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes",
+    "nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes", "nvfp4_moe_down_combine",
+    "nvfp4_moe_down_workspace_bytes",
 ]
 
 DGRAD_DEQUANT_BF16, DGRAD_FP4_COLPACK = 0, 1
@@ -128,6 +129,21 @@ class WgradArgs(C.Structure):
     ]
 
 
+class MoeDownArgs(C.Structure):
+    _fields_ = [
+        ("num_tokens", C.c_int64), ("top_k", C.c_int64), ("num_experts", C.c_int64),
+        ("N", C.c_int64), ("K", C.c_int64),
+        ("h", C.c_void_p), ("perm", C.c_void_p), ("expert_offsets", C.c_void_p),
+        ("route_weights", C.c_void_p), ("h_global_scale", C.c_void_p),
+        ("w_codes", C.c_void_p), ("w_sf", C.c_void_p), ("w_global_scale", C.c_void_p),
+        ("lora_a", C.c_void_p), ("lora_b", C.c_void_p),
+        ("rank", C.c_int32), ("alpha", C.c_float),
+        ("y", C.c_void_p),
+        ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
+        ("prof_begin", C.c_void_p), ("prof_end", C.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -150,7 +166,8 @@ def load(path: str | None = None):
                         ("nvfp4_grouped_gemm", "nvfp4_grouped_workspace_bytes", GroupedArgs),
                         ("nvfp4_lora_epilogue", "nvfp4_lora_workspace_bytes", LoraArgs),
                         ("nvfp4_dgrad", "nvfp4_dgrad_workspace_bytes", DgradArgs),
-                        ("nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes", WgradArgs)]:
+                        ("nvfp4_wgrad", "nvfp4_wgrad_workspace_bytes", WgradArgs),
+                        ("nvfp4_moe_down_combine", "nvfp4_moe_down_workspace_bytes", MoeDownArgs)]:
         f = getattr(lib, fn)
         f.argtypes = [C.POINTER(st), vp]
         f.restype = C.c_int

@@ -489,6 +489,93 @@ nvfp4_status validate_grouped(const nvfp4_grouped_args *a) {
   return NVFP4_OK;
 }
 
+// The expert products of a grouped operand already in the padded layout: the
+// optional per-expert LoRA down pass (X rows gathered through row_map) and the
+// grouped W4A4 GEMM with the fused LoRA up-projection, D in grouped row order.
+struct GroupedProducts {
+  int64_t E, N, K, prow_max;
+  const uint8_t *aq, *asf;        // padded A codes / swizzled scales
+  const float *g_a;
+  const int32_t *row_map;         // padded row -> row of x_src (-1: padding)
+  const GroupTile *gtiles;
+  const int32_t *nmt;
+  const void *x_src;              // bf16 source rows of the LoRA input [x_rows][K]
+  int64_t x_rows;
+  const void *w_codes, *w_sf;
+  const float *w_g;
+  const void *lora_a, *lora_b;
+  int32_t rank;
+  float alpha;
+  __nv_bfloat16 *t;               // [prow_max][rank] T' scratch
+  void *d;                        // bf16 [P][N]
+  void *prof_begin, *prof_end;
+};
+
+nvfp4_status run_grouped_products(const GroupedProducts &g, int *status, uint64_t tmo, int sms,
+                                  cudaStream_t st) {
+  const int bn = 256;
+  GemmMaps maps;
+  if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.aq, g.K / 2, g.prow_max, g.K / 2, 128, 128) ||
+      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w_codes, g.K / 2, g.E * g.N, g.K / 2, 128, bn))
+    return NVFP4_ERR_CUDA;
+  maps.t = maps.a;
+  maps.lb = maps.b;
+  int lora_steps = 0;
+  if (g.lora_a) {
+    LoraDownMaps lm;
+    if (!make_map_2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.x_src, g.K, g.x_rows, g.K * 2, 64, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.lora_a, g.K, g.E * g.rank, g.K * 2, 64, g.rank) ||
+        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.t, g.rank, g.prow_max, g.rank * 2, 64, 128) ||
+        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.lora_b, g.rank, g.E * g.N, g.rank * 2, 64, bn))
+      return NVFP4_ERR_CUDA;
+    LoraDownParams lp{};
+    lp.M = g.prow_max;
+    lp.K = g.K;
+    lp.rank = g.rank;
+    lp.num_k64 = (int)ceil_div(g.K, 64);
+    lp.lora_scale = g.alpha / (float)g.rank;
+    lp.g_a = g.g_a;
+    lp.g_b = g.w_g;
+    lp.t_out = g.t;
+    lp.gtiles = g.gtiles;
+    lp.gnum_mtiles = g.nmt;
+    lp.row_map = g.row_map;
+    lp.x = static_cast<const __nv_bfloat16 *>(g.x_src);
+    lp.status = status;
+    lp.timeout_ns = tmo;
+    if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
+    lora_steps = g.rank / 64 + (g.rank % 64 ? 1 : 0);
+  }
+  GemmParams p{};
+  p.M = g.prow_max;
+  p.N = g.N;
+  p.K = g.K;
+  p.num_kt = (int)ceil_div(g.K, 256);
+  p.nk64 = (int)ceil_div(g.K, 64);
+  p.a_sf = g.asf;
+  p.b_sf = static_cast<const uint8_t *>(g.w_sf);
+  p.a_sf_katoms = pad_up(g.K / 16, 4) / 4;
+  p.b_sf_katoms = p.a_sf_katoms;
+  p.b_sf_row_chunks = g.E * g.N / 128;
+  p.g_a = g.g_a;
+  p.g_b = g.w_g;
+  p.d = g.d;
+  p.ldd = g.N;
+  p.out_fp32 = 0;
+  p.lora_steps = lora_steps;
+  p.tiles_n = (int)(g.N / bn);
+  p.gtiles = g.gtiles;
+  p.gnum_mtiles = g.nmt;
+  p.status = status;
+  p.timeout_ns = tmo;
+  p.stall_probe = tmo == 0;
+  if (cudaError_t e_ = mark(g.prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
+  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  if (e == cudaSuccess) e = mark(g.prof_end, st);
+  return cuda_status(e);
+}
+
 nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int sms, cudaStream_t st) {
   int *status = static_cast<int *>(a->workspace);
   const uint64_t tmo = g_timeout_ns.load();
@@ -538,72 +625,146 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
                                             pl.xsf, sms, st);
       e_ != cudaSuccess)
     return cuda_status(e_);
-  const float *g_x = a->x_global_scale ? a->x_global_scale : pl.g_x;
+  GroupedProducts gp;
+  gp.E = a->num_experts;
+  gp.N = a->N;
+  gp.K = a->K;
+  gp.prow_max = pl.prow_max;
+  gp.aq = pl.xq;
+  gp.asf = pl.xsf;
+  gp.g_a = a->x_global_scale ? a->x_global_scale : pl.g_x;
+  gp.row_map = pl.row_map;
+  gp.gtiles = pl.gtiles;
+  gp.nmt = pl.nmt;
+  gp.x_src = a->x_bf16;
+  gp.x_rows = a->num_tokens;
+  gp.w_codes = a->w_codes;
+  gp.w_sf = a->w_sf;
+  gp.w_g = a->w_global_scale;
+  gp.lora_a = a->lora_a;
+  gp.lora_b = a->lora_b;
+  gp.rank = a->rank;
+  gp.alpha = a->alpha;
+  gp.t = pl.t;
+  gp.d = a->d;
+  gp.prof_begin = a->prof_begin;
+  gp.prof_end = a->prof_end;
+  return run_grouped_products(gp, status, tmo, sms, st);
+}
 
-  const int bn = 256;
-  GemmMaps maps;
-  if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, pl.xq, a->K / 2, pl.prow_max, a->K / 2, 128, 128) ||
-      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->w_codes, a->K / 2, a->num_experts * a->N, a->K / 2,
-             128, bn))
-    return NVFP4_ERR_CUDA;
-  maps.t = maps.a;
-  maps.lb = maps.b;
-  int lora_steps = 0;
-  if (a->lora_a) {
-    LoraDownMaps lm;
-    if (!make_map_2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->x_bf16, a->K, a->num_tokens, a->K * 2, 64,
-                     1, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->num_experts * a->rank, a->K * 2, 64,
-               a->rank) ||
-        !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, pl.prow_max, a->rank * 2, 64, 128) ||
-        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->num_experts * a->N,
-               a->rank * 2, 64, bn))
-      return NVFP4_ERR_CUDA;
-    LoraDownParams lp{};
-    lp.M = pl.prow_max;
-    lp.K = a->K;
-    lp.rank = a->rank;
-    lp.num_k64 = (int)ceil_div(a->K, 64);
-    lp.lora_scale = a->alpha / (float)a->rank;
-    lp.g_a = g_x;
-    lp.g_b = a->w_global_scale;
-    lp.t_out = pl.t;
-    lp.gtiles = pl.gtiles;
-    lp.gnum_mtiles = pl.nmt;
-    lp.row_map = pl.row_map;
-    lp.x = static_cast<const __nv_bfloat16 *>(a->x_bf16);
-    lp.status = status;
-    lp.timeout_ns = tmo;
-    if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
-    lora_steps = a->rank / 64 + (a->rank % 64 ? 1 : 0);
+// ------------------------------------------------------- MoE down + combine --
+struct MoeDownPlan {
+  size_t ws = 0;
+  int64_t prow_max = 0;
+  int32_t *poffsets = nullptr, *row_map = nullptr, *nmt = nullptr, *inv = nullptr;
+  GroupTile *gtiles = nullptr;
+  uint32_t *amax = nullptr;
+  int nparts = 0;
+  float *g_h = nullptr;
+  uint8_t *hq = nullptr, *hsf = nullptr;
+  __nv_bfloat16 *t = nullptr, *d = nullptr;
+};
+
+void plan_moe_down(const nvfp4_moe_down_args *a, MoeDownPlan *pl) {
+  Carve c(a->workspace);
+  const int64_t P = a->num_tokens * a->top_k;
+  pl->prow_max = pad_up(P + a->num_experts * 127, 128);
+  pl->poffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  pl->row_map = c.take<int32_t>((size_t)pl->prow_max * 4);
+  pl->gtiles = c.take<GroupTile>((size_t)(pl->prow_max / 128) * sizeof(GroupTile));
+  pl->nmt = c.take<int32_t>(4);
+  pl->inv = c.take<int32_t>((size_t)P * 4);
+  if (!a->h_global_scale) {
+    pl->nparts = amax_parts_for(P);
+    pl->amax = c.take<uint32_t>((size_t)pl->nparts * 4);
   }
-  GemmParams p{};
-  p.M = pl.prow_max;
-  p.N = a->N;
-  p.K = a->K;
-  p.num_kt = (int)ceil_div(a->K, 256);
-  p.nk64 = (int)ceil_div(a->K, 64);
-  p.a_sf = pl.xsf;
-  p.b_sf = a->w_sf;
-  p.a_sf_katoms = pad_up(a->K / 16, 4) / 4;
-  p.b_sf_katoms = p.a_sf_katoms;
-  p.b_sf_row_chunks = a->num_experts * a->N / 128;
-  p.g_a = g_x;
-  p.g_b = a->w_global_scale;
-  p.d = a->d;
-  p.ldd = a->N;
-  p.out_fp32 = 0;
-  p.lora_steps = lora_steps;
-  p.tiles_n = (int)(a->N / bn);
-  p.gtiles = pl.gtiles;
-  p.gnum_mtiles = pl.nmt;
-  p.status = status;
-  p.timeout_ns = tmo;
-  p.stall_probe = tmo == 0;
-  if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
-  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
-  if (e == cudaSuccess) e = mark(a->prof_end, st);
-  return cuda_status(e);
+  pl->g_h = c.take<float>(4);
+  pl->hq = c.take<uint8_t>((size_t)pl->prow_max * a->K / 2);
+  pl->hsf = c.take<uint8_t>(sf_swizzled_bytes(pl->prow_max, a->K));
+  if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)pl->prow_max * a->rank * 2);
+  pl->d = c.take<__nv_bfloat16>((size_t)P * a->N * 2);
+  pl->ws = c.off;
+}
+
+nvfp4_status validate_moe_down(const nvfp4_moe_down_args *a) {
+  if (!a || !a->h || !a->perm || !a->expert_offsets || !a->route_weights || !a->w_codes || !a->w_sf ||
+      !a->w_global_scale || !a->y)
+    return NVFP4_ERR_INVALID_ARG;
+  if (a->num_tokens < 1 || a->top_k < 1 || a->num_experts < 1 || a->N < 1 || a->K < 1)
+    return NVFP4_ERR_INVALID_ARG;
+  if (a->num_experts > 1024 || a->top_k > a->num_experts) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->N % 256 != 0 || a->K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->num_tokens * a->top_k > (1ll << 30) || a->num_experts * a->N > (1ll << 31) - 256)
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->lora_a || a->lora_b) {
+    if (!a->lora_a || !a->lora_b) return NVFP4_ERR_INVALID_ARG;
+    if (a->rank < 32 || a->rank > 256 || a->rank % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(a->lora_a, 16) || !aligned(a->lora_b, 16)) return NVFP4_ERR_ALIGNMENT;
+  }
+  if (!aligned(a->h, 16) || !aligned(a->w_codes, 16) || !aligned(a->w_sf, 16) || !aligned(a->y, 16))
+    return NVFP4_ERR_ALIGNMENT;
+  return NVFP4_OK;
+}
+
+nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, int sms, cudaStream_t st) {
+  int *status = static_cast<int *>(a->workspace);
+  const uint64_t tmo = g_timeout_ns.load();
+  const int64_t P = a->num_tokens * a->top_k;
+  if (cudaError_t e_ = launch_layout_from_offsets(a->expert_offsets, (int)a->num_experts, pl.prow_max,
+                                                  pl.poffsets, pl.gtiles, pl.nmt, pl.row_map, sms, st);
+      e_ != cudaSuccess)
+    return cuda_status(e_);
+  // h is quantized once (one tensor-wide g) straight into the padded layout:
+  // padded row r takes grouped row row_map[r]
+  QuantParams q{};
+  q.src = static_cast<const __nv_bfloat16 *>(a->h);
+  q.rows = P;
+  q.cols = a->K;
+  q.ld = a->K;
+  q.batch = 1;
+  q.g_in = a->h_global_scale;
+  q.g_out = pl.g_h;
+  q.amax_part = pl.amax;
+  q.nparts = pl.nparts;
+  q.codes_row = pl.hq;
+  q.sf_row = pl.hsf;
+  q.sf_swizzled = 1;
+  q.row_map = pl.row_map;
+  q.dst_rows = pl.prow_max;
+  q.status = status;
+  q.timeout_ns = tmo;
+  if (!a->h_global_scale) {
+    if (cudaError_t e_ = launch_amax(q, st); e_ != cudaSuccess) return cuda_status(e_);
+  }
+  if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
+  GroupedProducts gp;
+  gp.E = a->num_experts;
+  gp.N = a->N;
+  gp.K = a->K;
+  gp.prow_max = pl.prow_max;
+  gp.aq = pl.hq;
+  gp.asf = pl.hsf;
+  gp.g_a = a->h_global_scale ? a->h_global_scale : pl.g_h;
+  gp.row_map = pl.row_map;
+  gp.gtiles = pl.gtiles;
+  gp.nmt = pl.nmt;
+  gp.x_src = a->h;
+  gp.x_rows = P;
+  gp.w_codes = a->w_codes;
+  gp.w_sf = a->w_sf;
+  gp.w_g = a->w_global_scale;
+  gp.lora_a = a->lora_a;
+  gp.lora_b = a->lora_b;
+  gp.rank = a->rank;
+  gp.alpha = a->alpha;
+  gp.t = pl.t;
+  gp.d = pl.d;
+  gp.prof_begin = a->prof_begin;
+  gp.prof_end = a->prof_end;
+  nvfp4_status s = run_grouped_products(gp, status, tmo, sms, st);
+  if (s != NVFP4_OK) return s;
+  return cuda_status(launch_moe_combine(pl.d, a->perm, pl.inv, a->route_weights, a->num_tokens,
+                                        (int)a->top_k, a->N, static_cast<__nv_bfloat16 *>(a->y), sms, st));
 }
 
 // --------------------------------------------------------------------- LoRA --
@@ -1126,6 +1287,26 @@ nvfp4_status nvfp4_wgrad(const nvfp4_wgrad_args *a, nvfp4_stream stream) {
   plan_wgrad(a, &pl);
   if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
   return run_wgrad(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t nvfp4_moe_down_workspace_bytes(const nvfp4_moe_down_args *a) {
+  if (!a) return 0;
+  nvfp4_moe_down_args c = *a;
+  c.workspace = nullptr;
+  MoeDownPlan pl;
+  plan_moe_down(&c, &pl);
+  return pl.ws;
+}
+
+nvfp4_status nvfp4_moe_down_combine(const nvfp4_moe_down_args *a, nvfp4_stream stream) {
+  nvfp4_status s = validate_moe_down(a);
+  if (s != NVFP4_OK) return s;
+  DevInfo d;
+  if ((s = device_info(&d)) != NVFP4_OK) return s;
+  MoeDownPlan pl;
+  plan_moe_down(a, &pl);
+  if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
+  return run_moe_down(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

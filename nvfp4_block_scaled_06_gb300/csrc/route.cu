@@ -156,4 +156,130 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------- layout from given expert offsets --
+// The grouped operand's padded layout when the rows already arrive grouped
+// (the down-projection input, in the order of the up-projection's output):
+// per expert e, rows offsets[e] .. offsets[e+1]-1 keep their order and start
+// at the 128-aligned padded offset.
+__global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restrict__ offsets, int E,
+                                                         int32_t *poffsets, GroupTile *gtiles,
+                                                         int32_t *gnum_mtiles) {
+  __shared__ int32_t scratch[64];
+  const int e = threadIdx.x;
+  const bool act = e < E;
+  const int32_t count = act ? offsets[e + 1] - offsets[e] : 0;
+  const int32_t padded = (count + 127) & ~127;
+  const int32_t mt = padded / 128;
+  int32_t ptotal, mtotal;
+  const int32_t poff = block_exclusive_scan(padded, scratch, ptotal);
+  const int32_t moff = block_exclusive_scan(mt, scratch, mtotal);
+  if (act) {
+    poffsets[e] = poff;
+    for (int j = 0; j < mt; ++j) {
+      GroupTile g;
+      g.expert = e;
+      g.a_row0 = poff + 128 * j;
+      g.valid_rows = min(128, count - 128 * j);
+      g.out_row0 = offsets[e] + 128 * j;
+      gtiles[moff + j] = g;
+    }
+  }
+  if (threadIdx.x == 0) {
+    poffsets[E] = ptotal;
+    *gnum_mtiles = mtotal;
+  }
+}
+
+// row_map[r] = the grouped row that padded row r holds, or -1 (padding).
+__global__ void k_rowmap_from_offsets(const int32_t *__restrict__ offsets,
+                                      const int32_t *__restrict__ poffsets, int E, int64_t rows,
+                                      int32_t *row_map) {
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    int32_t v = -1;
+    if (r < poffsets[E]) {
+      int lo = 0, hi = E - 1;            // the last e with poffsets[e] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (poffsets[mid] <= r) lo = mid;
+        else hi = mid - 1;
+      }
+      const int64_t i = r - poffsets[lo];
+      if (i < offsets[lo + 1] - offsets[lo]) v = (int32_t)(offsets[lo] + i);
+    }
+    row_map[r] = v;
+  }
+}
+
+cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t padded_rows_max,
+                                       int32_t *poffsets, GroupTile *gtiles, int32_t *gnum_mtiles,
+                                       int32_t *row_map, int num_sms, cudaStream_t st) {
+  k_offsets_layout<<<1, 1024, 0, st>>>(offsets, E, poffsets, gtiles, gnum_mtiles);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((padded_rows_max + 255) / 256, (int64_t)num_sms * 4));
+  k_rowmap_from_offsets<<<(unsigned)ctas, 256, 0, st>>>(offsets, poffsets, E, padded_rows_max, row_map);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- combine --
+// y[t][n] = sum over slots j (in order) of w[t][j] * d[g(t, j)][n], fp32
+// accumulation (one fused multiply-add per slot), rounded once to bf16, where
+// g(t, j) is the grouped row of pair t*top_k + j (the inverse of perm).
+__global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, int32_t *inv) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pairs;
+       i += (int64_t)gridDim.x * blockDim.x)
+    inv[perm[i]] = (int32_t)i;
+}
+
+__global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__restrict__ d,
+                                                     const int32_t *__restrict__ inv,
+                                                     const float *__restrict__ w, int64_t tokens, int top_k,
+                                                     int64_t N, __nv_bfloat16 *__restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t vecs = N / 8;                       // 16-byte vectors of a row
+  for (int64_t t = warp; t < tokens; t += nwarps) {
+    for (int64_t v0 = 0; v0 < vecs; v0 += 32) {
+      const int64_t v = v0 + lane;
+      if (v >= vecs) break;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < top_k; ++j) {
+        const int64_t g = inv[t * top_k + j];
+        const float wj = w[t * top_k + j];
+        const uint4 q = __ldg(reinterpret_cast<const uint4 *>(d + g * N) + v);
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fmaf_rn(wj, __uint_as_float(qw[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(wj, __uint_as_float(qw[i] & 0xFFFF0000u), acc[2 * i + 1]);
+        }
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        o[i] = *reinterpret_cast<const uint32_t *>(&h);
+      }
+      reinterpret_cast<uint4 *>(y + t * N)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int32_t *inv, const float *w,
+                               int64_t tokens, int top_k, int64_t N, __nv_bfloat16 *y, int num_sms,
+                               cudaStream_t st) {
+  const int64_t pairs = tokens * top_k;
+  const int64_t c1 = std::max<int64_t>(1, std::min<int64_t>((pairs + 255) / 256, (int64_t)num_sms * 4));
+  k_invert_perm<<<(unsigned)c1, 256, 0, st>>>(perm, pairs, inv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t c2 = std::max<int64_t>(1, std::min<int64_t>((tokens + 7) / 8, (int64_t)num_sms * 8));
+  k_moe_combine<<<(unsigned)c2, 256, 0, st>>>(d, inv, w, tokens, top_k, N, y);
+  return cudaGetLastError();
+}
+
 }  // namespace nvfp4

@@ -53,6 +53,12 @@ R9  Dequantization to bf16 (the backward's rebuilt weight, [P1] "Why can't
     rounded once more to bf16 (nearest, ties to even).  The Dgrad product
     dX = dY W contracts over N with fp32 accumulation.
 
+R10 The routed down-projection takes its input already in the grouped order
+    of the up-projection's output, quantized once with one tensor-wide g;
+    the combine weights each expert output by its gate weight
+    (y[t] = sum_j w[t,j] D[t,j]; [P3] "How it was produced": REAP saliency
+    gate_weight x ||expert_output||), summed over the slots in order.
+
 Parity of the swizzled layout and nibble order is pinned only through the
 hardware (the tensor core consumes them); everything else is pinned by the
 tests in tests/test_oracle_pins.py.
@@ -67,7 +73,7 @@ __all__ = [
     "quantize_colwise", "dequantize", "sf_swizzle", "sf_unswizzle",
     "gemm_fp64", "lora_delta_fp64", "linear_fp64", "error_scale",
     "round_fp64_to_bf16", "bf16_ulp", "group_rows", "grouped_linear_rows",
-    "dequantize_bf16", "f32_to_bf16_rne",
+    "dequantize_bf16", "f32_to_bf16_rne", "grouped_input_rows", "moe_combine",
 ]
 
 # ---------------------------------------------------------------------------
@@ -373,6 +379,39 @@ def grouped_linear_rows(rows, x_bits, xq, w_codes, w_sf, w_g, perm, expert_ids,
         out.append(linear_fp64(xr, wr, x_bits[t:t + 1], lo)[0])
         scale.append(error_scale(xr, wr, x_bits[t:t + 1], lo)[0])
     return np.array(out), np.array(scale)
+
+
+def grouped_input_rows(h_bits, hq, row_expert, w_codes, w_sf, w_g, lora=None):
+    """Oracle output of every row of an input that is already in grouped order
+    (the down-projection: row i of ``h`` meets expert ``row_expert[i]``).
+
+    ``hq`` = (codes, sf, g) of the whole h (one tensor-wide scale).  Returns
+    fp64 D [P, N] and its error scale S."""
+    out, scale = [], []
+    for i, e in enumerate(np.asarray(row_expert)):
+        e = int(e)
+        hr = (hq[0][i:i + 1], hq[1][i:i + 1], hq[2])
+        wr = (w_codes[e], w_sf[e], w_g[e])
+        lo = None if lora is None else (lora[0][e], lora[1][e], lora[2])
+        out.append(linear_fp64(hr, wr, h_bits[i:i + 1], lo)[0])
+        scale.append(error_scale(hr, wr, h_bits[i:i + 1], lo)[0])
+    return np.array(out), np.array(scale)
+
+
+def moe_combine(d_rows, perm, weights, topk):
+    """y[t] = sum over slots j of w[t, j] * D[grouped row of pair t*topk + j]
+    (the routed experts' outputs weighted by their gate weights), fp64.
+
+    ``perm[i]`` is the pair index of grouped row i (R8)."""
+    P = len(perm)
+    inv = np.empty(P, dtype=np.int64)
+    inv[np.asarray(perm, dtype=np.int64)] = np.arange(P)
+    T = P // topk
+    w = np.asarray(weights, dtype=np.float64).reshape(T, topk)
+    y = np.zeros((T, d_rows.shape[1]))
+    for j in range(topk):
+        y += w[:, j:j + 1] * d_rows[inv[np.arange(T) * topk + j]]
+    return y
 
 
 def bytes_per_element() -> float:

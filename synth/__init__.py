@@ -36,6 +36,10 @@ Recipes (shapes and distributions follow the pages' layers: hidden 6144,
              pmf), top-8 per token by logit, ties to the lower expert id.
 * dgrad:     the backward of the prefill linear: W[2048,6144] ~N(0,0.02),
              dY[8192,2048] ~N(0,0.01) (gradient-sized values).
+* moe_down:  h[32768,2048] ~N(0,1) (the activated up-projection output, in
+             grouped order); 256 experts W2_e[6144,2048] ~N(0,0.02); LoRA
+             A_e[64,2048], B_e[6144,64] ~N(0,0.01); routing as grouped; gate
+             weights = softmax over each token's selected scores.
 """
 from __future__ import annotations
 
@@ -58,6 +62,9 @@ CONFIGS = {
     "grouped": dict(T=4096, E=256, topk=8, N=2048, K=6144, rank=64, alpha=128.0),
     # the backward of the prefill linear: dX [M, K] = dY [M, N] W [N, K]
     "dgrad": dict(M=8192, N=2048, K=6144),
+    # the routed experts' down-projection W2_e [6144, 2048] after the grouped
+    # up-projection, and the gate-weighted combine
+    "moe_down": dict(T=4096, E=256, topk=8, N=6144, K=2048, rank=64, alpha=128.0),
 }
 
 
@@ -138,6 +145,14 @@ def zipf_bias(E: int, g: np.random.Generator, s: float = 1.1) -> np.ndarray:
     return (-s * np.log(rank.astype(np.float64))).astype(np.float32)
 
 
+def gate_weights(scores: np.ndarray, experts: np.ndarray) -> np.ndarray:
+    """Gate weights of the chosen experts: softmax over each token's selected
+    scores (fp32 inputs to the combine)."""
+    sel = np.take_along_axis(np.asarray(scores, np.float64), experts, axis=1)
+    e = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
 def make_case(name: str, seed: int = 0, **over) -> dict:
     """Draw one workload with the numpy backend; returns uint16 bf16 bits.
 
@@ -175,6 +190,19 @@ def make_case(name: str, seed: int = 0, **over) -> dict:
         w = d.normal_bf16((c["N"], c["K"]), 0.02)
         dy = d.normal_bf16((c["M"], c["N"]), 0.01)
         return dict(w=w, dy=dy, **c)
+    if name == "moe_down":
+        c = dict(CONFIGS["moe_down"], **over)
+        P = c["T"] * c["topk"]
+        h = d.normal_bf16((P, c["K"]), 1.0)
+        w = d.normal_bf16((c["E"], c["N"], c["K"]), 0.02)
+        a = d.normal_bf16((c["E"], c["rank"], c["K"]), 0.01)
+        b = d.normal_bf16((c["E"], c["N"], c["rank"]), 0.01)
+        g = d.rng()
+        logits = g.standard_normal(size=(c["T"], c["E"]), dtype=np.float32)
+        bias = zipf_bias(c["E"], d.rng())
+        experts = route_top_k(logits, bias, c["topk"])
+        weights = gate_weights(logits + bias, experts)
+        return dict(h=h, w=w, lora_a=a, lora_b=b, expert_ids=experts, route_weights=weights, **c)
     if name == "grouped":
         c = dict(CONFIGS["grouped"], **over)
         x = d.normal_bf16((c["T"], c["K"]), 1.0)
@@ -234,6 +262,18 @@ def torch_route_top_k(T: int, E: int, k: int, gen, device):
     return order[:, :k].to(torch.int32).contiguous()
 
 
+def torch_route_top_k_weights(T: int, E: int, k: int, gen, device):
+    """``torch_route_top_k`` plus the gate weights (softmax over the selected scores)."""
+    import torch
+    logits = torch.randn((T, E), generator=gen, device=device, dtype=torch.float32)
+    perm = torch.randperm(E, generator=gen, device=device) + 1
+    bias = -1.1 * torch.log(perm.double())
+    s = logits.double() + bias[None, :]
+    order = torch.sort(s, dim=1, descending=True, stable=True).indices[:, :k]
+    w = torch.softmax(torch.gather(s, 1, order), dim=1).float()
+    return order.to(torch.int32).contiguous(), w.contiguous()
+
+
 def pad_up(v: int, m: int) -> int:
     return (v + m - 1) // m * m
 
@@ -265,6 +305,15 @@ def torch_case(name: str, seed: int = 0, device="cuda", **over) -> dict:
                     lora_a=torch_normal_bf16((c["E"], c["rank"], c["K"]), 0.01, gen, device),
                     lora_b=torch_normal_bf16((c["E"], c["N"], c["rank"]), 0.01, gen, device),
                     expert_ids=torch_route_top_k(c["T"], c["E"], c["topk"], gen, device), **c)
+    if name == "moe_down":
+        c = dict(CONFIGS["moe_down"], **over)
+        P = c["T"] * c["topk"]
+        ids, wts = torch_route_top_k_weights(c["T"], c["E"], c["topk"], gen, device)
+        return dict(h=torch_normal_bf16((P, c["K"]), 1.0, gen, device),
+                    w=torch_normal_bf16((c["E"], c["N"], c["K"]), 0.02, gen, device),
+                    lora_a=torch_normal_bf16((c["E"], c["rank"], c["K"]), 0.01, gen, device),
+                    lora_b=torch_normal_bf16((c["E"], c["N"], c["rank"]), 0.01, gen, device),
+                    expert_ids=ids, route_weights=wts, **c)
     if name == "dgrad":
         c = dict(CONFIGS["dgrad"], **over)
         return dict(w=torch_normal_bf16((c["N"], c["K"]), 0.02, gen, device),

@@ -368,3 +368,36 @@ def test_dequantize_bf16_signed_zero_and_zero_scale():
     assert out[0, 0] == 0x8000 and out[0, 1] == 0x3F00 and np.all(out[0, 2:] == 0)
     out0 = o.dequantize_bf16(codes, np.array([[0]], np.uint8), np.float32(1.0))
     assert out0[0, 1] == 0 and out0[0, 0] == 0x8000   # zero scale: +-0 by the code's sign
+
+
+def test_moe_combine_matches_brute_force():
+    rng = np.random.default_rng(41)
+    T, k, E, N = 12, 3, 5, 4
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    counts, offsets, perm = o.group_rows(ids, E)
+    d_rows = rng.standard_normal((T * k, N))
+    w = rng.random((T, k))
+    y = o.moe_combine(d_rows, perm, w, k)
+    for t in range(T):
+        want = np.zeros(N)
+        for j in range(k):
+            g = int(np.flatnonzero(perm == t * k + j)[0])    # the grouped row holding pair (t, j)
+            assert ids.reshape(-1)[perm[g]] == ids[t, j]
+            want += w[t, j] * d_rows[g]
+        assert np.allclose(y[t], want, rtol=0, atol=1e-12)
+
+
+def test_grouped_input_rows_is_the_per_expert_linear():
+    rng = np.random.default_rng(42)
+    P, K, N, E = 6, 64, 32, 3
+    h = f32_to_bf16_bits(rng.standard_normal((P, K)).astype(np.float32))
+    ws = [f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.1).astype(np.float32)) for _ in range(E)]
+    row_e = np.array([0, 0, 1, 2, 2, 2])
+    hq = o.quantize(h)
+    wq = [o.quantize(w) for w in ws]
+    d, _ = o.grouped_input_rows(h, hq, row_e, [q[0] for q in wq], [q[1] for q in wq], [q[2] for q in wq])
+    hd = o.dequantize(*hq)
+    for i in range(P):   # brute force: one dot product per output
+        wd = o.dequantize(*wq[row_e[i]])
+        for n in range(N):
+            assert abs(d[i, n] - sum(hd[i, kk] * wd[n, kk] for kk in range(K))) <= 1e-12 * (1 + abs(d[i, n]))
