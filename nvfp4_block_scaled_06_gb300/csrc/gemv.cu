@@ -6,15 +6,18 @@
 // activation quantized per call under the static per-tensor input_scale
 // ("How it was produced").  The CUDA-core path streams W once:
 //   * every CTA quantizes the (tiny) X into shared memory with the static
-//     scale, keeping the E2M1 values as exact fp16 pairs and the E4M3 block
-//     scales as fp32;
+//     scale, keeping each E2M1 value doubled as a signed 8-bit integer (the
+//     grid {0,.5,1,1.5,2,3,4,6} x 2 is {0,1,2,3,4,6,8,12}), both signs of it,
+//     and the E4M3 block scales as fp32;
 //   * a warp reads 32 x 32 contiguous bytes of W codes (64 elements per lane)
 //     and the matching 4-byte group of swizzled scales;
-//   * a 16-element block dot product of E2M1 values is exact in fp16x2 (every
-//     partial sum is a multiple of 1/4 below 512), sx_b*sw_b is exact in fp32
-//     (two 4-bit significands) and so is their product with the block dot;
-//     only the fp32 sum over blocks rounds.
-// Long rows (K > 4096) are split into 2048-element chunks written as fp32
+//   * four codes at a time become doubled magnitudes by one byte permute (a
+//     table lookup), the weight signs pick +x or -x by a second permute, and
+//     dp4a sums the four products: a 16-element block dot product is an exact
+//     integer (4x the E2M1 dot), sx_b*sw_b is exact in fp32 (two 4-bit
+//     significands) and so is their product with the block dot; only the fp32
+//     sum over blocks rounds.
+// Rows longer than 2048 elements are split into 2048-element chunks written as fp32
 // partials and summed in order by a second kernel (no atomics, deterministic).
 #include <cuda_fp16.h>
 
@@ -27,9 +30,15 @@ constexpr int kGemvThreads = 256;
 constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lanes x 64
 constexpr int kRows = 4;           // units (rows) a warp has in flight
 
+// Doubled E2M1 magnitudes {0,1,2,3,4,6,8,12} as bytes of two words: byte c of
+// (lo, hi) is 2*E2M1(c) for c = 0..7 (a byte-permute lookup table).
+constexpr uint32_t kE2m1x2Lo = 0x03020100u, kE2m1x2Hi = 0x0C080604u;
+
 // Same block quantizer as the row packing (kept local: tiny X, static scale).
+// Writes the block's 16 values as signed bytes 2*E2M1 (xp, 4 words) and their
+// negations (xn), and the E4M3 scale as fp32.
 __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g, float t6g,
-                                              uint32_t (&h2)[8], float &sx) {
+                                              uint32_t (&xp)[4], uint32_t (&xn)[4], float &sx) {
   uint32_t w[8];
   const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
   const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
@@ -42,15 +51,115 @@ __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g,
   uint32_t sb = 0;
   if (g > 0.0f) sb = cvt_e4m3(__fdiv_rn(bamax, t6g));
   sx = e4m3_to_f32(sb);
-  if (sb == 0) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) h2[i] = 0;
-    return;
-  }
+  for (int i = 0; i < 4; ++i) xp[i] = xn[i] = 0;
+  if (sb == 0) return;
   const float senc = fminf(__frcp_rn(__fmul_rn(sx, g)), 3.402823466e38f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    h2[i] = e2m1x2_to_h2(cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc)));
+  for (int i = 0; i < 8; ++i) {
+    // two codes (elements 2i, 2i+1) -> two signed doubled values
+    const uint32_t cc = cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t c = (cc >> (4 * h)) & 0xF;
+      const uint32_t mag = __byte_perm(kE2m1x2Lo, kE2m1x2Hi, c & 7);   // byte 0
+      const uint32_t v = (c & 8) ? ((0u - (mag & 0xFF)) & 0xFF) : (mag & 0xFF);
+      const uint32_t nv = (0u - v) & 0xFF;
+      const int e = 2 * i + h;             // element index in the block
+      xp[e >> 2] |= v << (8 * (e & 3));
+      xn[e >> 2] |= nv << (8 * (e & 3));
+    }
+  }
+}
+
+// A warp's work is a sequence of batches of kRows consecutive rows of one K
+// chunk.  The loads of the next batch are issued before the arithmetic of the
+// current one (two register buffers), and the first batch's loads before the
+// CTA quantizes X, so the weight stream starts at kernel entry.
+struct GemvBatch {
+  uint32_t c[kRows][8];   // 64 codes of each row for this lane
+  uint32_t sf[kRows];     // the 4 block scales of this lane's 64 codes
+  int32_t n0, g4;         // first row of the batch; this lane's 64-element group (-1: none)
+};
+
+__device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t batch, int32_t nb_per_chunk,
+                                          int32_t g4_total, int lane, GemvBatch &B) {
+  const int32_t kc = batch / nb_per_chunk;
+  B.n0 = (batch - kc * nb_per_chunk) * kRows;
+  const int32_t g4 = kc * (kGemvChunk / 64) + lane;
+  B.g4 = (g4 < g4_total && lane < kGemvChunk / 64) ? g4 : -1;
+  const int64_t row_bytes = p.K / 2;
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int32_t n = B.n0 + j;
+    if (B.g4 >= 0 && n < p.N) {
+      asm volatile(
+          "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+          : "=r"(B.c[j][0]), "=r"(B.c[j][1]), "=r"(B.c[j][2]), "=r"(B.c[j][3]), "=r"(B.c[j][4]),
+            "=r"(B.c[j][5]), "=r"(B.c[j][6]), "=r"(B.c[j][7])
+          : "l"(p.w_codes + (int64_t)n * row_bytes + (int64_t)B.g4 * 32));
+      B.sf[j] = __ldg(reinterpret_cast<const uint32_t *>(
+          p.w_sf + 512 * ((int64_t)(n >> 7) * p.w_sf_katoms + B.g4) + 16 * (n & 31) + 4 * ((n & 127) >> 5)));
+    }
+  }
+}
+
+template <int MX>
+__device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatch &B, int32_t batch,
+                                             int32_t nb_per_chunk, int nchunks, const uint32_t *xs,
+                                             const float *sxs, int64_t G4, int64_t nblk, float alpha,
+                                             int lane, float *partial) {
+  const int32_t kc = batch / nb_per_chunk;
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
+    const int32_t n = B.n0 + j;
+    float acc[MX];
+#pragma unroll
+    for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
+    if (B.g4 >= 0 && n < p.N) {
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const float sw = e4m3_to_f32((B.sf[j] >> (8 * bb)) & 0xFF);
+        // per group of four codes: doubled magnitudes, and the selector that
+        // takes +x or -x by the weight's sign
+        uint32_t mag[4], sel[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t nib = B.c[j][2 * bb + (q >> 1)] >> (16 * (q & 1));
+          mag[q] = __byte_perm(kE2m1x2Lo, kE2m1x2Hi, nib & 0x7777u);
+          sel[q] = 0x3210u | ((nib >> 1) & 0x4444u);
+        }
+#pragma unroll
+        for (int m = 0; m < MX; ++m) {
+          const uint4 *xq = reinterpret_cast<const uint4 *>(xs + m * (p.K / 2));
+          const uint4 xp = xq[(0 * 4 + bb) * G4 + B.g4], xn = xq[(1 * 4 + bb) * G4 + B.g4];
+          const uint32_t pw[4] = {xp.x, xp.y, xp.z, xp.w}, nw[4] = {xn.x, xn.y, xn.z, xn.w};
+          int isum = 0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) isum = __dp4a((int)mag[q], (int)__byte_perm(pw[q], nw[q], sel[q]), isum);
+          const float dot = __fmul_rn(__int2float_rn(isum), 0.25f);   // exact: |isum| <= 2304
+          acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + bb * G4 + B.g4]), acc[m]);
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MX; ++m)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+    if (n < p.N && lane < MX) {
+      float v = acc[0];
+#pragma unroll
+      for (int m = 1; m < MX; ++m)
+        if (lane == m) v = acc[m];
+      if (nchunks == 1) {
+        const float y = __fmul_rn(v, alpha);
+        if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n] = y;
+        else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n] = __float2bfloat16_rn(y);
+      } else {
+        partial[((int64_t)kc * MX + lane) * p.N + n] = v;
+      }
+    }
+  }
 }
 
 template <int MX>
@@ -59,111 +168,52 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   const int64_t K = p.K, nblk = K / 16;
   // Shared layout chosen so that the 32 lanes of a warp, which take 32
   // consecutive 64-element groups g4, read consecutive 16-byte words:
-  //   xs  [m][half h][bb][g4] = 4 half2 (elements 8h..8h+7 of block 4*g4 + bb)
-  //   sxs [m][bb][g4]         = E4M3 block scale as fp32
+  //   xs  [m][h][bb][g4] = the 16 values of block 4*g4 + bb as signed bytes
+  //                        2*E2M1 (h = 0) and their negations (h = 1)
+  //   sxs [m][bb][g4]    = E4M3 block scale as fp32
   const int64_t G4 = K / 64;
   uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
 
+  const int lane = threadIdx.x & 31;
+  const int32_t warp = blockIdx.x * (kGemvThreads / 32) + (threadIdx.x >> 5);
+  const int32_t nwarps = gridDim.x * (kGemvThreads / 32);
+  const int32_t nb_per_chunk = (int32_t)((p.N + kRows - 1) / kRows);
+  const int32_t batches = nb_per_chunk * nchunks;
+  const int32_t g4_total = (int32_t)(K / 64);
+
+  GemvBatch A, B;
+  int32_t b = warp;
+  if (b < batches) gemv_load(p, b, nb_per_chunk, g4_total, lane, A);   // weights in flight first
+
   const float g = *p.g_x;
   const float t6g = __fmul_rn(6.0f, g);
-  for (int64_t i = threadIdx.x; i < MX * nblk; i += blockDim.x) {
-    const int m = (int)(i / nblk);
-    const int64_t b = i % nblk;
-    uint32_t h2[8];
+  const int32_t nb32 = (int32_t)nblk;
+  for (int32_t i = threadIdx.x; i < MX * nb32; i += blockDim.x) {
+    const int32_t m = i / nb32;
+    const int32_t bk = i - m * nb32;
+    uint32_t xpv[4], xnv[4];
     float sx;
-    quant_x_block(p.x + m * p.ldx + b * 16, g, t6g, h2, sx);
-    const int64_t g4 = b >> 2, bb = b & 3;
+    quant_x_block(p.x + m * p.ldx + (int64_t)bk * 16, g, t6g, xpv, xnv, sx);
+    const int64_t g4 = bk >> 2, bb = bk & 3;
     uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2));
-    dst[(0 * 4 + bb) * G4 + g4] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-    dst[(1 * 4 + bb) * G4 + g4] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+    dst[(0 * 4 + bb) * G4 + g4] = make_uint4(xpv[0], xpv[1], xpv[2], xpv[3]);
+    dst[(1 * 4 + bb) * G4 + g4] = make_uint4(xnv[0], xnv[1], xnv[2], xnv[3]);
     sxs[m * nblk + bb * G4 + g4] = sx;
   }
   __syncthreads();
 
   const float alpha = __fmul_rn(g, *p.g_w);
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (int64_t)blockIdx.x * (kGemvThreads / 32) + (threadIdx.x >> 5);
-  const int64_t nwarps = (int64_t)gridDim.x * (kGemvThreads / 32);
-  const int64_t units = p.N * nchunks;
-  const int64_t row_bytes = K / 2;
-  const int64_t g4_total = K / 64;
-  // A warp takes kRows consecutive units (consecutive rows of one K chunk) and
-  // issues all of their loads before any arithmetic, so every lane keeps
-  // kRows x 32 bytes of weights in flight.
-  for (int64_t u0 = warp * kRows; u0 < units; u0 += nwarps * kRows) {
-    uint32_t c[kRows][8];
-    uint32_t sf4[kRows];
-    int64_t n[kRows], g4v[kRows];
-#pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const int64_t u = u0 + j;
-      const int64_t kc = u / p.N;
-      n[j] = u % p.N;
-      g4v[j] = kc * (kGemvChunk / 64) + lane;
-      const bool live = u < units && g4v[j] < g4_total && g4v[j] < (kc + 1) * (kGemvChunk / 64);
-      if (!live) g4v[j] = -1;
-      if (live) {
-        asm volatile(
-            "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-            : "=r"(c[j][0]), "=r"(c[j][1]), "=r"(c[j][2]), "=r"(c[j][3]), "=r"(c[j][4]),
-              "=r"(c[j][5]), "=r"(c[j][6]), "=r"(c[j][7])
-            : "l"(p.w_codes + n[j] * row_bytes + g4v[j] * 32));
-        sf4[j] = __ldg(reinterpret_cast<const uint32_t *>(
-            p.w_sf + 512 * ((n[j] >> 7) * p.w_sf_katoms + g4v[j]) + 16 * (n[j] & 31) +
-            4 * ((n[j] & 127) >> 5)));
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      float acc[MX];
-#pragma unroll
-      for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
-      if (g4v[j] >= 0) {
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          const float sw = e4m3_to_f32((sf4[j] >> (8 * bb)) & 0xFF);
-          uint32_t wh[8];   // wh[i] = elements 2i, 2i+1 of the block (same order as X)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            wh[i] = e2m1x2_to_h2(c[j][2 * bb] >> (8 * i));
-            wh[4 + i] = e2m1x2_to_h2(c[j][2 * bb + 1] >> (8 * i));
-          }
-#pragma unroll
-          for (int m = 0; m < MX; ++m) {
-            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + m * (K / 2));
-            const uint4 x0 = xp[(0 * 4 + bb) * G4 + g4v[j]], x1 = xp[(1 * 4 + bb) * G4 + g4v[j]];
-            const uint32_t xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            __half2 s2 = __float2half2_rn(0.0f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              s2 = __hfma2(*reinterpret_cast<const __half2 *>(&wh[i]),
-                           *reinterpret_cast<const __half2 *>(&xv[i]), s2);
-            const float dot = __fadd_rn(__low2float(s2), __high2float(s2));
-            acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + bb * G4 + g4v[j]]), acc[m]);
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < MX; ++m)
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-      const int64_t u = u0 + j;
-      if (u < units && lane < MX) {
-        float v = acc[0];
-#pragma unroll
-        for (int m = 1; m < MX; ++m)
-          if (lane == m) v = acc[m];
-        const int64_t kc = u / p.N;
-        if (nchunks == 1) {
-          const float y = __fmul_rn(v, alpha);
-          if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n[j]] = y;
-          else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n[j]] = __float2bfloat16_rn(y);
-        } else {
-          partial[(kc * MX + lane) * p.N + n[j]] = v;
-        }
-      }
-    }
+  while (b < batches) {
+    const int32_t b1 = b + nwarps;
+    if (b1 < batches) gemv_load(p, b1, nb_per_chunk, g4_total, lane, B);
+    gemv_compute<MX>(p, A, b, nb_per_chunk, nchunks, xs, sxs, G4, nblk, alpha, lane, partial);
+    b = b1;
+    if (b >= batches) break;
+    const int32_t b2 = b + nwarps;
+    if (b2 < batches) gemv_load(p, b2, nb_per_chunk, g4_total, lane, A);
+    gemv_compute<MX>(p, B, b, nb_per_chunk, nchunks, xs, sxs, G4, nblk, alpha, lane, partial);
+    b = b2;
   }
 }
 
@@ -182,7 +232,8 @@ __global__ void k_gemv_reduce(const GemvParams p, int nchunks, int mx, const flo
 }
 
 size_t gemv_smem_bytes(int64_t M, int64_t K) { return (size_t)M * (K / 2) * 4 + (size_t)M * (K / 16) * 4; }
-int gemv_chunks(int64_t K) { return K > 4096 ? (int)((K + kGemvChunk - 1) / kGemvChunk) : 1; }
+// a warp covers 2048 elements of a row (32 lanes x 64): longer rows are split
+int gemv_chunks(int64_t K) { return (int)((K + kGemvChunk - 1) / kGemvChunk); }
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const int c = gemv_chunks(K);
   return c > 1 ? (size_t)c * M * N * sizeof(float) : 0;
@@ -201,8 +252,10 @@ static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, 
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX>, kGemvThreads, smem);
   per_sm = std::max(1, std::min(per_sm, 8));
-  const int64_t warps_needed = (p.N * nchunks + 8 * kRows - 1) / (8 * kRows);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, warps_needed));
+  // one wave of resident CTAs (or fewer when there is less work)
+  const int64_t batches = (p.N + kRows - 1) / kRows * nchunks;
+  const int64_t ctas_needed = (batches + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, ctas_needed));
   k_gemv<MX><<<grid, kGemvThreads, smem, st>>>(p, nchunks, partial);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nchunks == 1) return e;

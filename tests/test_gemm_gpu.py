@@ -100,10 +100,12 @@ def test_prefill_full_size_sampled_rows():
     assert_gemm_close(y[torch.from_numpy(rows).cuda()], y_or, S, term, what="prefill full")
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 32])
-def test_decode_static_scale(M):
-    """Decode: X quantized per call with a static input_scale (GEMV for M <= 4)."""
-    N, K = 1024, 2048
+@pytest.mark.parametrize("M,K", [(1, 2048), (2, 2048), (4, 2048), (8, 2048), (32, 2048),
+                                 (1, 3072), (3, 4096), (1, 1088)])
+def test_decode_static_scale(M, K):
+    """Decode: X quantized per call with a static input_scale (GEMV for M <= 4;
+    rows longer than 2048 are split into chunks summed in order)."""
+    N = 1024
     c = make_case("decode_q_b_proj", M=M, N=N, K=K)
     static = 16.0 / 2688.0
     wc, ws, wg = quant_dev(c["w"])
