@@ -17,8 +17,9 @@
 //     integer (4x the E2M1 dot), sx_b*sw_b is exact in fp32 (two 4-bit
 //     significands) and so is their product with the block dot; only the fp32
 //     sum over blocks rounds.
-// Rows longer than 2048 elements are split into 2048-element chunks written as fp32
-// partials and summed in order by a second kernel (no atomics, deterministic).
+// Rows longer than 2048 elements are split into 2048-element chunks; the chunk
+// sums of a row are added in chunk order, inside the CTA for rows of up to
+// 16384 elements and by a second kernel beyond (no atomics, deterministic).
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -72,26 +73,32 @@ __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g,
   }
 }
 
-// A warp's work is a sequence of batches of kRows consecutive rows of one K
-// chunk.  The loads of the next batch are issued before the arithmetic of the
-// current one (two register buffers), and the first batch's loads before the
-// CTA quantizes X, so the weight stream starts at kernel entry.
+// A warp's task is kRows consecutive rows of one 2048-element K chunk.  Tasks
+// are ordered row-major (all chunks of a row batch are adjacent), so a CTA
+// streams whole rows.  With at most kWarps chunks per row, one CTA holds every
+// chunk of its row batches at once: the warps' chunk sums meet in shared
+// memory and are added in chunk order there.  Longer rows write fp32 chunk
+// sums [chunk][m][n] that a second kernel adds in the same order.  The loads
+// of the next task are issued before the arithmetic of the current one (two
+// register buffers), and the first task's loads before the CTA quantizes X,
+// so the weight stream starts at kernel entry.
+constexpr int kWarps = kGemvThreads / 32;
+
 struct GemvBatch {
   uint32_t c[kRows][8];   // 64 codes of each row for this lane
   uint32_t sf[kRows];     // the 4 block scales of this lane's 64 codes
-  int32_t n0, g4;         // first row of the batch; this lane's 64-element group (-1: none)
+  int32_t n0, g4;         // first row of the task; this lane's 64-element group (-1: none)
 };
 
-__device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t batch, int32_t nb_per_chunk,
-                                          int32_t g4_total, int lane, GemvBatch &B) {
-  const int32_t kc = batch / nb_per_chunk;
-  B.n0 = (batch - kc * nb_per_chunk) * kRows;
+__device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t n0, int32_t kc, int32_t g4_total,
+                                          int lane, GemvBatch &B) {
+  B.n0 = n0;
   const int32_t g4 = kc * (kGemvChunk / 64) + lane;
-  B.g4 = (g4 < g4_total && lane < kGemvChunk / 64) ? g4 : -1;
+  B.g4 = g4 < g4_total ? g4 : -1;
   const int64_t row_bytes = p.K / 2;
 #pragma unroll
   for (int j = 0; j < kRows; ++j) {
-    const int32_t n = B.n0 + j;
+    const int32_t n = n0 + j;
     if (B.g4 >= 0 && n < p.N) {
       asm volatile(
           "ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -104,21 +111,34 @@ __device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t batch, in
   }
 }
 
+// The chunk sums of the task's rows: on return lane m (< MX) holds row j's
+// sum for activation row m in out[j].  Blocks outer, rows inner: the lane's X
+// words of a block are read from shared memory once for all rows.
 template <int MX>
-__device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatch &B, int32_t batch,
-                                             int32_t nb_per_chunk, int nchunks, const uint32_t *xs,
-                                             const float *sxs, int64_t G4, int64_t nblk, float alpha,
-                                             int lane, float *partial) {
-  const int32_t kc = batch / nb_per_chunk;
+__device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatch &B, const uint32_t *xs,
+                                             const float *sxs, int64_t G4, int64_t nblk, int lane,
+                                             float (&out)[kRows]) {
+  float acc[kRows][MX];
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) {
-    const int32_t n = B.n0 + j;
-    float acc[MX];
+  for (int j = 0; j < kRows; ++j)
 #pragma unroll
-    for (int m = 0; m < MX; ++m) acc[m] = 0.0f;
-    if (B.g4 >= 0 && n < p.N) {
+    for (int m = 0; m < MX; ++m) acc[j][m] = 0.0f;
+  if (B.g4 >= 0) {
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
+    for (int bb = 0; bb < 4; ++bb) {
+      uint32_t pw[MX][4], nw[MX][4];
+      float sx[MX];
+#pragma unroll
+      for (int m = 0; m < MX; ++m) {
+        const uint4 *xq = reinterpret_cast<const uint4 *>(xs + m * (p.K / 2));
+        const uint4 xp = xq[(0 * 4 + bb) * G4 + B.g4], xn = xq[(1 * 4 + bb) * G4 + B.g4];
+        pw[m][0] = xp.x; pw[m][1] = xp.y; pw[m][2] = xp.z; pw[m][3] = xp.w;
+        nw[m][0] = xn.x; nw[m][1] = xn.y; nw[m][2] = xn.z; nw[m][3] = xn.w;
+        sx[m] = sxs[m * nblk + bb * G4 + B.g4];
+      }
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        if (B.n0 + j >= p.N) continue;
         const float sw = e4m3_to_f32((B.sf[j] >> (8 * bb)) & 0xFF);
         // per group of four codes: doubled magnitudes, and the selector that
         // takes +x or -x by the weight's sign
@@ -131,40 +151,58 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
         }
 #pragma unroll
         for (int m = 0; m < MX; ++m) {
-          const uint4 *xq = reinterpret_cast<const uint4 *>(xs + m * (p.K / 2));
-          const uint4 xp = xq[(0 * 4 + bb) * G4 + B.g4], xn = xq[(1 * 4 + bb) * G4 + B.g4];
-          const uint32_t pw[4] = {xp.x, xp.y, xp.z, xp.w}, nw[4] = {xn.x, xn.y, xn.z, xn.w};
           int isum = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) isum = __dp4a((int)mag[q], (int)__byte_perm(pw[q], nw[q], sel[q]), isum);
+          for (int q = 0; q < 4; ++q)
+            isum = __dp4a((int)mag[q], (int)__byte_perm(pw[m][q], nw[m][q], sel[q]), isum);
           const float dot = __fmul_rn(__int2float_rn(isum), 0.25f);   // exact: |isum| <= 2304
-          acc[m] = __fmaf_rn(dot, __fmul_rn(sw, sxs[m * nblk + bb * G4 + B.g4]), acc[m]);
+          acc[j][m] = __fmaf_rn(dot, __fmul_rn(sw, sx[m]), acc[j][m]);
         }
       }
     }
+  }
+#pragma unroll
+  for (int j = 0; j < kRows; ++j) {
 #pragma unroll
     for (int m = 0; m < MX; ++m)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-    if (n < p.N && lane < MX) {
-      float v = acc[0];
+      for (int o = 16; o > 0; o >>= 1) acc[j][m] += __shfl_xor_sync(0xffffffffu, acc[j][m], o);
+    float v = acc[j][0];
 #pragma unroll
-      for (int m = 1; m < MX; ++m)
-        if (lane == m) v = acc[m];
-      if (nchunks == 1) {
-        const float y = __fmul_rn(v, alpha);
-        if (p.out_fp32) reinterpret_cast<float *>(p.d)[lane * p.ldd + n] = y;
-        else reinterpret_cast<__nv_bfloat16 *>(p.d)[lane * p.ldd + n] = __float2bfloat16_rn(y);
-      } else {
-        partial[((int64_t)kc * MX + lane) * p.N + n] = v;
-      }
-    }
+    for (int m = 1; m < MX; ++m)
+      if (lane == m) v = acc[j][m];
+    out[j] = v;
   }
+}
+
+__device__ __forceinline__ void gemv_store(const GemvParams &p, int64_t m, int64_t n, float y) {
+  if (p.out_fp32) reinterpret_cast<float *>(p.d)[m * p.ldd + n] = y;
+  else reinterpret_cast<__nv_bfloat16 *>(p.d)[m * p.ldd + n] = __float2bfloat16_rn(y);
+}
+
+// Work units.  In-CTA mode (nchunks <= kWarps): a unit is rbu = kWarps / nchunks
+// row batches x nchunks chunks, warp w taking row batch w / nchunks, chunk
+// w % nchunks (warps past rbu * nchunks idle).  Global mode: a unit is one task.
+struct GemvPlan {
+  int32_t nchunks, rbu, units, g4_total;
+  bool in_cta;
+};
+
+__device__ __forceinline__ GemvPlan gemv_plan(const GemvParams &p, int nchunks) {
+  GemvPlan q;
+  q.nchunks = nchunks;
+  q.in_cta = nchunks <= kWarps;
+  const int32_t nb = (int32_t)((p.N + kRows - 1) / kRows);
+  q.rbu = q.in_cta ? kWarps / nchunks : 1;
+  q.units = q.in_cta ? (nb + q.rbu - 1) / q.rbu : nb * nchunks;
+  q.g4_total = (int32_t)(p.K / 64);
+  return q;
 }
 
 template <int MX>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
   extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ float red[2][kWarps][kRows][4];   // in-CTA chunk sums, double-buffered
   const int64_t K = p.K, nblk = K / 16;
   // Shared layout chosen so that the 32 lanes of a warp, which take 32
   // consecutive 64-element groups g4, read consecutive 16-byte words:
@@ -175,16 +213,29 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
 
-  const int lane = threadIdx.x & 31;
-  const int32_t warp = blockIdx.x * (kGemvThreads / 32) + (threadIdx.x >> 5);
-  const int32_t nwarps = gridDim.x * (kGemvThreads / 32);
-  const int32_t nb_per_chunk = (int32_t)((p.N + kRows - 1) / kRows);
-  const int32_t batches = nb_per_chunk * nchunks;
-  const int32_t g4_total = (int32_t)(K / 64);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const GemvPlan q = gemv_plan(p, nchunks);
+  // this warp's task in unit u (in-CTA) / task index (global)
+  const bool active = !q.in_cta || w < q.rbu * q.nchunks;
+  const int32_t my_kc = q.in_cta ? w % q.nchunks : 0, my_rb = q.in_cta ? w / q.nchunks : 0;
+  const int32_t ustep = q.in_cta ? (int32_t)gridDim.x : (int32_t)gridDim.x * kWarps;
+  int32_t u = q.in_cta ? (int32_t)blockIdx.x : (int32_t)blockIdx.x * kWarps + w;
+  auto task_of = [&](int32_t unit, int32_t &n0, int32_t &kc) {
+    if (q.in_cta) {
+      n0 = (unit * q.rbu + my_rb) * kRows;
+      kc = my_kc;
+    } else {
+      n0 = (unit / q.nchunks) * kRows;
+      kc = unit % q.nchunks;
+    }
+  };
 
   GemvBatch A, B;
-  int32_t b = warp;
-  if (b < batches) gemv_load(p, b, nb_per_chunk, g4_total, lane, A);   // weights in flight first
+  if (active && u < q.units) {   // weights in flight first
+    int32_t n0, kc;
+    task_of(u, n0, kc);
+    gemv_load(p, n0, kc, q.g4_total, lane, A);
+  }
 
   const float g = *p.g_x;
   const float t6g = __fmul_rn(6.0f, g);
@@ -204,16 +255,55 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   __syncthreads();
 
   const float alpha = __fmul_rn(g, *p.g_w);
-  while (b < batches) {
-    const int32_t b1 = b + nwarps;
-    if (b1 < batches) gemv_load(p, b1, nb_per_chunk, g4_total, lane, B);
-    gemv_compute<MX>(p, A, b, nb_per_chunk, nchunks, xs, sxs, G4, nblk, alpha, lane, partial);
-    b = b1;
-    if (b >= batches) break;
-    const int32_t b2 = b + nwarps;
-    if (b2 < batches) gemv_load(p, b2, nb_per_chunk, g4_total, lane, A);
-    gemv_compute<MX>(p, B, b, nb_per_chunk, nchunks, xs, sxs, G4, nblk, alpha, lane, partial);
-    b = b2;
+  int buf = 0;
+  // one unit: this warp's task (batch `cur`, prefetching the next unit into
+  // `nxt`), then the output of the unit
+  auto run_unit = [&](int32_t unit, const GemvBatch &cur, GemvBatch &nxt) {
+    const int32_t un = unit + ustep;
+    if (active && un < q.units) {
+      int32_t n0, kc;
+      task_of(un, n0, kc);
+      gemv_load(p, n0, kc, q.g4_total, lane, nxt);
+    }
+    float v[kRows];
+    if (active) gemv_compute<MX>(p, cur, xs, sxs, G4, nblk, lane, v);
+    if (!q.in_cta) {
+      const int32_t kc = unit % q.nchunks;
+#pragma unroll
+      for (int j = 0; j < kRows; ++j)
+        if (cur.n0 + j < p.N && lane < MX) partial[((int64_t)kc * MX + lane) * p.N + cur.n0 + j] = v[j];
+    } else if (q.nchunks == 1) {
+      if (active)
+#pragma unroll
+        for (int j = 0; j < kRows; ++j)
+          if (cur.n0 + j < p.N && lane < MX) gemv_store(p, lane, cur.n0 + j, __fmul_rn(v[j], alpha));
+    } else {
+      if (active && lane < MX)
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) red[buf][w][j][lane] = v[j];
+      __syncthreads();
+      // chunk sums of each output added in chunk order
+      const int t = threadIdx.x;
+      if (t < q.rbu * kRows * MX) {
+        const int rbl = t / (kRows * MX), j = (t / MX) % kRows, m = t % MX;
+        const int64_t n = (int64_t)(unit * q.rbu + rbl) * kRows + j;
+        if (n < p.N) {
+          float sum = 0.0f;
+          for (int kc = 0; kc < q.nchunks; ++kc) sum = __fadd_rn(sum, red[buf][rbl * q.nchunks + kc][j][m]);
+          gemv_store(p, m, n, __fmul_rn(sum, alpha));
+        }
+      }
+      buf ^= 1;
+    }
+  };
+  // units are CTA-uniform in in-CTA mode (every thread takes the same path
+  // to the barrier); in global mode they are per warp and no barrier is used
+  while (u < q.units) {
+    run_unit(u, A, B);
+    u += ustep;
+    if (u >= q.units) break;
+    run_unit(u, B, A);
+    u += ustep;
   }
 }
 
@@ -225,9 +315,7 @@ __global__ void k_gemv_reduce(const GemvParams p, int nchunks, int mx, const flo
     const int64_t m = i / p.N, n = i % p.N;
     float s = 0.0f;
     for (int kc = 0; kc < nchunks; ++kc) s = __fadd_rn(s, partial[(kc * mx + m) * p.N + n]);
-    const float y = __fmul_rn(s, alpha);
-    if (p.out_fp32) reinterpret_cast<float *>(p.d)[m * p.ldd + n] = y;
-    else reinterpret_cast<__nv_bfloat16 *>(p.d)[m * p.ldd + n] = __float2bfloat16_rn(y);
+    gemv_store(p, m, n, __fmul_rn(s, alpha));
   }
 }
 
@@ -236,13 +324,13 @@ size_t gemv_smem_bytes(int64_t M, int64_t K) { return (size_t)M * (K / 2) * 4 + 
 int gemv_chunks(int64_t K) { return (int)((K + kGemvChunk - 1) / kGemvChunk); }
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   const int c = gemv_chunks(K);
-  return c > 1 ? (size_t)c * M * N * sizeof(float) : 0;
+  return c > kWarps ? (size_t)c * M * N * sizeof(float) : 0;
 }
 
 template <int MX>
 static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {
   const size_t smem = gemv_smem_bytes(MX, p.K);
-  static size_t configured = 48 * 1024;
+  static size_t configured = 48 * 1024 - sizeof(float) * 2 * kWarps * kRows * 4;
   if (smem > configured) {
     cudaError_t e = cudaFuncSetAttribute(k_gemv<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -253,12 +341,13 @@ static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, 
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX>, kGemvThreads, smem);
   per_sm = std::max(1, std::min(per_sm, 8));
   // one wave of resident CTAs (or fewer when there is less work)
-  const int64_t batches = (p.N + kRows - 1) / kRows * nchunks;
-  const int64_t ctas_needed = (batches + kGemvThreads / 32 - 1) / (kGemvThreads / 32);
+  const int64_t nb = (p.N + kRows - 1) / kRows;
+  const int64_t ctas_needed = nchunks <= kWarps ? (nb + kWarps / nchunks - 1) / (kWarps / nchunks)
+                                                : (nb * nchunks + kWarps - 1) / kWarps;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, ctas_needed));
   k_gemv<MX><<<grid, kGemvThreads, smem, st>>>(p, nchunks, partial);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || nchunks == 1) return e;
+  if (e != cudaSuccess || nchunks <= kWarps) return e;
   k_gemv_reduce<<<num_sms, 256, 0, st>>>(p, nchunks, MX, partial);
   return cudaGetLastError();
 }

@@ -117,6 +117,23 @@ def test_decode_static_scale(M, K):
         assert_gemm_close(y, y_or, S, what=f"decode M{M}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 520, 6144), (2, 520, 10240), (4, 520, 16384), (3, 776, 2112),
+                                   (1, 264, 20480), (2, 264, 18432)])
+def test_decode_chunked_rows(M, N, K):
+    """Decode GEMV with rows of several 2048-element chunks: 3, 5, 8 and 2
+    chunks are summed inside one CTA (6, 5, 8 and 8 busy warps, ragged last
+    unit), 10 and 9 chunks through fp32 chunk sums and the ordered second pass."""
+    c = make_case("decode_q_b_proj", M=M, N=N, K=K)
+    static = 16.0 / 2688.0
+    wc, ws, wg = quant_dev(c["w"])
+    gx = torch.tensor([static], dtype=torch.float32, device="cuda")
+    y_or, S, _ = oracle_linear(c["x"], c["w"], xg=np.float32(static))
+    for od in (torch.bfloat16, torch.float32):
+        y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx,
+                          out_dtype=od)
+        assert_gemm_close(y, y_or, S, what=f"decode M{M} N{N} K{K}")
+
+
 @pytest.mark.parametrize("name", ["decode_q_b_proj", "decode_o_proj"])
 def test_decode_full_weights_sampled(name):
     c = make_case(name, M=1)
