@@ -11,9 +11,11 @@
 //     and the E4M3 block scales as fp32;
 //   * a warp reads 32 x 32 contiguous bytes of W codes (64 elements per lane)
 //     and the matching 4-byte group of swizzled scales;
-//   * four codes at a time become doubled magnitudes by one byte permute (a
-//     table lookup), the weight signs pick +x or -x by a second permute, and
-//     dp4a sums the four products: a 16-element block dot product is an exact
+//   * four codes at a time become the doubled magnitudes of the positive
+//     codes and, from the codes with their sign bits flipped, of the negative
+//     codes, each by one byte permute whose sign-replicate mode zeroes the
+//     other sign; two dp4a sum them against +x and -x: a 16-element block dot
+//     product is an exact
 //     integer (4x the E2M1 dot), sx_b*sw_b is exact in fp32 (two 4-bit
 //     significands) and so is their product with the block dot; only the fp32
 //     sum over blocks rounds.
@@ -34,6 +36,15 @@ constexpr int kRows = 4;           // units (rows) a warp has in flight
 // Doubled E2M1 magnitudes {0,1,2,3,4,6,8,12} as bytes of two words: byte c of
 // (lo, hi) is 2*E2M1(c) for c = 0..7 (a byte-permute lookup table).
 constexpr uint32_t kE2m1x2Lo = 0x03020100u, kE2m1x2Hi = 0x0C080604u;
+
+// Byte permute with the selector's high bit per byte honoured: a selector
+// nibble of 8..15 yields the sign of the selected byte replicated (0 for the
+// non-negative table entries here), 0..7 the byte itself.
+__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
 
 // Same block quantizer as the row packing (kept local: tiny X, static scale).
 // Writes the block's 16 values as signed bytes 2*E2M1 (xp, 4 words) and their
@@ -140,21 +151,26 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
       for (int j = 0; j < kRows; ++j) {
         if (B.n0 + j >= p.N) continue;
         const float sw = e4m3_to_f32((B.sf[j] >> (8 * bb)) & 0xFF);
-        // per group of four codes: doubled magnitudes, and the selector that
-        // takes +x or -x by the weight's sign
-        uint32_t mag[4], sel[4];
+        // per group of four codes: the doubled magnitudes of the positive
+        // codes (negative ones read 0) and of the negative codes (positive
+        // ones read 0), each by one table lookup in sign-replicate mode
+        uint32_t mpos[4], mneg[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t nib = B.c[j][2 * bb + (q >> 1)] >> (16 * (q & 1));
-          mag[q] = __byte_perm(kE2m1x2Lo, kE2m1x2Hi, nib & 0x7777u);
-          sel[q] = 0x3210u | ((nib >> 1) & 0x4444u);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t w = B.c[j][2 * bb + h], wn = w ^ 0x88888888u;
+          mpos[2 * h] = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, w);
+          mpos[2 * h + 1] = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, w >> 16);
+          mneg[2 * h] = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, wn);
+          mneg[2 * h + 1] = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, wn >> 16);
         }
 #pragma unroll
         for (int m = 0; m < MX; ++m) {
           int isum = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            isum = __dp4a((int)mag[q], (int)__byte_perm(pw[m][q], nw[m][q], sel[q]), isum);
+          for (int q = 0; q < 4; ++q) {
+            isum = __dp4a((int)mpos[q], (int)pw[m][q], isum);
+            isum = __dp4a((int)mneg[q], (int)nw[m][q], isum);
+          }
           const float dot = __fmul_rn(__int2float_rn(isum), 0.25f);   // exact: |isum| <= 2304
           acc[j][m] = __fmaf_rn(dot, __fmul_rn(sw, sx[m]), acc[j][m]);
         }
