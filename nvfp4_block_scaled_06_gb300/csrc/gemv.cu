@@ -171,8 +171,8 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
             isum = __dp4a((int)mpos[q], (int)pw[m][q], isum);
             isum = __dp4a((int)mneg[q], (int)nw[m][q], isum);
           }
-          const float dot = __fmul_rn(__int2float_rn(isum), 0.25f);   // exact: |isum| <= 2304
-          acc[j][m] = __fmaf_rn(dot, __fmul_rn(sw, sx[m]), acc[j][m]);
+          // isum/4 (the E2M1 dot) times sx*sw, both exact: one rounding in the fma
+          acc[j][m] = __fmaf_rn(__int2float_rn(isum), __fmul_rn(sw, sx[m]), acc[j][m]);
         }
       }
     }
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   // consecutive 64-element groups g4, read consecutive 16-byte words:
   //   xs  [m][h][bb][g4] = the 16 values of block 4*g4 + bb as signed bytes
   //                        2*E2M1 (h = 0) and their negations (h = 1)
-  //   sxs [m][bb][g4]    = E4M3 block scale as fp32
+  //   sxs [m][bb][g4]    = E4M3 block scale / 4 as fp32 (the values are doubled)
   const int64_t G4 = K / 64;
   uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
     uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2));
     dst[(0 * 4 + bb) * G4 + g4] = make_uint4(xpv[0], xpv[1], xpv[2], xpv[3]);
     dst[(1 * 4 + bb) * G4 + g4] = make_uint4(xnv[0], xnv[1], xnv[2], xnv[3]);
-    sxs[m * nblk + bb * G4 + g4] = sx;
+    sxs[m * nblk + bb * G4 + g4] = __fmul_rn(sx, 0.25f);   // with the 1/4 of the doubled values (exact)
   }
   __syncthreads();
 
