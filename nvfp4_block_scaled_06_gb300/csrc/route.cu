@@ -232,30 +232,67 @@ __global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, i
     inv[perm[i]] = (int32_t)i;
 }
 
+// A warp takes a token: its slots' row indices and weights are read once, and
+// for top_k <= 8 the 16-byte loads of all slots are in flight together before
+// the sums (which keep the slot order).
 __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__restrict__ d,
                                                      const int32_t *__restrict__ inv,
                                                      const float *__restrict__ w, int64_t tokens, int top_k,
                                                      int64_t N, __nv_bfloat16 *__restrict__ y) {
+  constexpr int kMaxK = 8;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t vecs = N / 8;                       // 16-byte vectors of a row
   for (int64_t t = warp; t < tokens; t += nwarps) {
-    for (int64_t v0 = 0; v0 < vecs; v0 += 32) {
-      const int64_t v = v0 + lane;
-      if (v >= vecs) break;
+    if (top_k <= kMaxK) {
+      const uint4 *rows[kMaxK];
+      float wj[kMaxK];
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        rows[j] = j < top_k ? reinterpret_cast<const uint4 *>(d + (int64_t)inv[t * top_k + j] * N) : nullptr;
+        wj[j] = j < top_k ? w[t * top_k + j] : 0.0f;
+      }
+      for (int64_t v = lane; v < vecs; v += 32) {
+        uint4 q[kMaxK];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) q[j] = j < top_k ? __ldg(rows[j] + v) : make_uint4(0, 0, 0, 0);
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+          if (j >= top_k) break;
+          const uint32_t qw[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = __fmaf_rn(wj[j], __uint_as_float(qw[i] << 16), acc[2 * i]);
+            acc[2 * i + 1] = __fmaf_rn(wj[j], __uint_as_float(qw[i] & 0xFFFF0000u), acc[2 * i + 1]);
+          }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+          o[i] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(y + t * N)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      continue;
+    }
+    for (int64_t v = lane; v < vecs; v += 32) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
       for (int j = 0; j < top_k; ++j) {
         const int64_t g = inv[t * top_k + j];
-        const float wj = w[t * top_k + j];
+        const float wv = w[t * top_k + j];
         const uint4 q = __ldg(reinterpret_cast<const uint4 *>(d + g * N) + v);
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = __fmaf_rn(wj, __uint_as_float(qw[i] << 16), acc[2 * i]);
-          acc[2 * i + 1] = __fmaf_rn(wj, __uint_as_float(qw[i] & 0xFFFF0000u), acc[2 * i + 1]);
+          acc[2 * i] = __fmaf_rn(wv, __uint_as_float(qw[i] << 16), acc[2 * i]);
+          acc[2 * i + 1] = __fmaf_rn(wv, __uint_as_float(qw[i] & 0xFFFF0000u), acc[2 * i + 1]);
         }
       }
       uint32_t o[4];
