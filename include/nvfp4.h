@@ -89,7 +89,9 @@ typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_FP32 = 1 } nvfp4_out_dtype;
  *   cols) and nvfp4_sf_bytes(rows, cols, sf_layout) (row packing), the same
  *   with rows and cols swapped for column packing.
  * Requirements: cols % 16 == 0 (row), rows % 16 == 0 (col); ld % 8 == 0 and
- *   src 16-byte aligned; code/scale pointers 16-byte aligned.
+ *   src 16-byte aligned; code/scale pointers 16-byte aligned.  rows, cols
+ *   <= 2^31 for the row packing alone, < 2^30 when the column packing is asked
+ *   for (else NVFP4_ERR_UNSUPPORTED_SHAPE).
  * Workspace: nvfp4_quantize_workspace_bytes(&args).
  * ------------------------------------------------------------------------ */
 typedef struct {

@@ -134,6 +134,8 @@ nvfp4_status validate_quantize(const nvfp4_quant_args *a) {
   if (a->cols % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (col && a->rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (a->rows > (1ll << 31) || a->cols > (1ll << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  // the tiled kernel (column packing) indexes rows and columns in 32 bits
+  if (col && (a->rows >= (1ll << 30) || a->cols >= (1ll << 30))) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned(a->src, 16) || a->ld % 8 != 0 || (a->batch > 1 && a->batch_stride % 8 != 0))
     return NVFP4_ERR_ALIGNMENT;
   for (const void *p : {(const void *)a->codes_row, (const void *)a->sf_row, (const void *)a->codes_col,
@@ -1096,6 +1098,18 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, const uint64_t (&dims)[3],
+                 const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3]) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void *>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 }  // namespace nvfp4
 

@@ -47,6 +47,9 @@ nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scr
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
+// 3-D tiled map (x = innermost), no swizzle, zero fill out of bounds.
+bool make_map_3d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, const uint64_t (&dims)[3],
+                 const uint64_t (&strides_bytes)[2], const uint32_t (&box)[3]);
 // NVFP4 -> bf16 (transpose: out[c][r]).
 cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *sf, int sf_swz, const float *g, int64_t rows,
                            int64_t cols, int transpose, __nv_bfloat16 *out, int64_t ldo, int num_sms,

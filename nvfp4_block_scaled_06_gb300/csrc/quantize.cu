@@ -521,126 +521,218 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
 }
 
 // ------------------------------------------------- tiled col (+row) packing --
-// A CTA quantizes 64 x 128 tiles of one matrix (grid-stride over tiles).  Each
-// thread loads two 16-element row blocks (64 contiguous bytes) and packs them
-// from registers (row packing); the tile is staged in shared memory, where each
-// thread reads two adjacent columns per 32-bit load and packs one 16-row block
-// of each (column packing).  Requires rows % 16 == 0 for the column packing.
-constexpr int kTR = 64, kTC = 128;
+// A CTA quantizes 64 x 256 tiles of one matrix (grid-stride over tiles).  The
+// tiles arrive by TMA (one 3-D box per tile, rows and columns past the matrix
+// zero-filled) into two shared-memory buffers, so that the next tile streams
+// in while this one is packed.  Every thread ends a tile with 32 contiguous
+// bytes of codes per packing (one full sector) and one word of scales:
+//   row role: thread t owns row t/4 of the tile and its 64-column quarter t%4,
+//     four whole 16-element blocks;
+//   column role: lanes 2i and 2i+1 read the column pair (two columns per
+//     32-bit word) of their warp's pair index over the upper and lower 32 rows,
+//     pack two 16-row blocks of both columns, and swap one column's half, so
+//     that each ends with the four blocks of one column.
+// Requires rows % 16 == 0 for the column packing.
+constexpr int kTR = 64, kTC = 256;
+constexpr int kTileBytes = kTR * kTC * 2;
+constexpr uint64_t kTileDrainNs = 200000000ull;
 
-__global__ void __launch_bounds__(256) k_quant_tiles(QuantParams p) {
+// quant16 with the block maximum taken by max.xorsign.abs (same magnitude).
+__device__ __forceinline__ uint64_t quant16_abs(const uint32_t (&w)[8], const BlockScale &s, uint32_t &sf_out) {
+  const uint32_t m2 = bmaxabs2(bmaxabs2(bmaxabs2(w[0], w[1]), bmaxabs2(w[2], w[3])),
+                               bmaxabs2(bmaxabs2(w[4], w[5]), bmaxabs2(w[6], w[7]))) &
+                      0x7FFF7FFFu;
+  const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
+  uint32_t sb = 0;
+  if (!s.gzero) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(mb << 16), s.t6g));
+  sf_out = sb;
+  if (sb == 0) return 0ull;
+  return encode16(w, s.senc[sb]);
+}
+
+// Stores the codes of blocks 0..nvalid-1 (8 bytes each) at dst: one 32-byte
+// store when all four are valid and dst is 32-byte aligned, else smaller ones.
+__device__ __forceinline__ void store_blocks4(uint8_t *dst, const uint64_t (&cd)[4], int nvalid) {
+  const uint32_t w[8] = {(uint32_t)cd[0], (uint32_t)(cd[0] >> 32), (uint32_t)cd[1], (uint32_t)(cd[1] >> 32),
+                         (uint32_t)cd[2], (uint32_t)(cd[2] >> 32), (uint32_t)cd[3], (uint32_t)(cd[3] >> 32)};
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+  if (nvalid == 4 && (a & 31) == 0) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+  } else if (nvalid == 4 && (a & 15) == 0) {
+    reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < nvalid) reinterpret_cast<uint2 *>(dst)[j] = make_uint2(w[2 * j], w[2 * j + 1]);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const __grid_constant__ CUtensorMap tm) {
+  extern __shared__ __align__(128) uint8_t qts[];           // two tiles [kTR][kTC] bf16, row-major
   __shared__ uint32_t scratch[32];
   __shared__ float senc_tab[128];
-  __shared__ __align__(16) uint32_t tile[kTR][kTC / 2];   // bf16 pairs
-  __shared__ __align__(16) uint8_t sfcol[kTC][4];
+  __shared__ __align__(8) uint64_t full[2];
   const int b = blockIdx.y;
-  const float g = resolve_global_scale(p, b, scratch);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && p.g_out) p.g_out[b] = g;
-  const BlockScale s = make_block_scale(g, senc_tab);
-
   const int t = threadIdx.x;
-  const int64_t tiles_r = (p.rows + kTR - 1) / kTR, tiles_c = (p.cols + kTC - 1) / kTC;
-  const __nv_bfloat16 *src = p.src + (int64_t)b * p.bstride;
+  if (t == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_barrier_init();
+  }
+  const float g = resolve_global_scale(p, b, scratch);
+  if (blockIdx.x == 0 && t == 0 && p.g_out) p.g_out[b] = g;
+  const BlockScale s = make_block_scale(g, senc_tab);   // synchronizes (barrier init visible)
+
+  const int32_t rows = (int32_t)p.rows, cols = (int32_t)p.cols;
+  const int32_t tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
+  const int32_t ntiles = tiles_r * tiles_c;
   const bool do_row = p.codes_row != nullptr, do_col = p.codes_col != nullptr;
-  const int64_t nblk_r = p.cols / 16, sfc_pad_r = (nblk_r + 3) & ~int64_t(3);
-  const int64_t nblk_c = p.rows / 16, sfc_pad_c = (nblk_c + 3) & ~int64_t(3);
+  const int32_t nblk_r = cols / 16, sfc_pad_r = (nblk_r + 3) & ~3;
+  const int32_t nblk_c = rows / 16, sfc_pad_c = (nblk_c + 3) & ~3;
   uint8_t *codes_r = do_row ? p.codes_row + (int64_t)b * p.codes_row_bstride : nullptr;
   uint8_t *sf_r = do_row ? p.sf_row + (int64_t)b * p.sf_row_bstride : nullptr;
   uint8_t *codes_c = do_col ? p.codes_col + (int64_t)b * p.codes_col_bstride : nullptr;
   uint8_t *sf_c = do_col ? p.sf_col + (int64_t)b * p.sf_col_bstride : nullptr;
-  // Row role: load slot i of warp w covers tile rows 16i + 2w + (lane >> 4);
-  // lane & 15 is the 8-element chunk of that 256-byte row, so a warp-wide
-  // 16-byte load reads two whole rows (fully coalesced).  Lanes 2j, 2j+1 hold
-  // the two halves of 16-element block j of the row.
-  const int warp = t >> 5, lane = t & 31;
-  const int chunk = lane & 15, blk_in_row = chunk >> 1;
-  const int cp = t & 63, crb = t >> 6;        // column role: column pair, 16-row block
+  const int rr = t >> 2, qd = t & 3;          // row role: tile row, 64-column quarter
+  const int cp = t >> 1, rh = t & 1;          // column role: column pair, 32-row half
 
-  for (int64_t tix = blockIdx.x; tix < tiles_r * tiles_c; tix += gridDim.x) {
-    const int64_t r0 = (tix / tiles_c) * kTR, c0 = (tix % tiles_c) * kTC;
-    const int64_t gc = c0 + 8 * chunk;
-    uint32_t w[4][4];
-    bool in[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int64_t gr = r0 + 16 * i + 2 * warp + (lane >> 4);
-      in[i] = gr < p.rows && gc < p.cols;
-      if (in[i]) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + gr * p.ld + gc));
-        w[i][0] = v.x; w[i][1] = v.y; w[i][2] = v.z; w[i][3] = v.w;
-      } else {
-        w[i][0] = w[i][1] = w[i][2] = w[i][3] = 0;
-      }
-    }
-    __syncthreads();   // the previous tile's column readers are done with `tile`
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      *reinterpret_cast<uint4 *>(&tile[16 * i + 2 * warp + (lane >> 4)][4 * chunk]) =
-          make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
-    if (do_row) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t gr = r0 + 16 * i + 2 * warp + (lane >> 4);
-        // block max over this lane's 8 values and its partner's
-        uint32_t m2 = bmax2(bmax2(w[i][0] & 0x7FFF7FFFu, w[i][1] & 0x7FFF7FFFu),
-                            bmax2(w[i][2] & 0x7FFF7FFFu, w[i][3] & 0x7FFF7FFFu));
-        m2 = bmax2(m2, __shfl_xor_sync(0xffffffffu, m2, 1));
-        const uint32_t mb = max(m2 & 0xFFFFu, m2 >> 16);
-        uint32_t sb = 0;
-        if (!s.gzero && in[i]) sb = cvt_e4m3(__fdiv_rn(__uint_as_float(mb << 16), s.t6g));
-        const uint32_t code = sb ? encode8(w[i], s.senc[sb]) : 0u;
-        if (in[i]) *reinterpret_cast<uint32_t *>(codes_r + gr * (p.cols / 2) + gc / 2) = code;
-        const int64_t blk = gc / 16;
-        if (p.sf_swizzled) {
-          // even lanes of each 8-lane group hold blocks 4g .. 4g+3 of the row
-          uint32_t v = sb;
-          v |= __shfl_down_sync(0xffffffffu, sb, 2) << 8;
-          v |= __shfl_down_sync(0xffffffffu, sb, 4) << 16;
-          v |= __shfl_down_sync(0xffffffffu, sb, 6) << 24;
-          if ((lane & 7) == 0 && gr < p.rows && blk < sfc_pad_r)
-            *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = v;
-        } else if (in[i] && (lane & 1) == 0) {
-          sf_r[gr * nblk_r + blk] = (uint8_t)sb;
-        }
-        (void)blk_in_row;
-      }
-    }
-    __syncthreads();
-    if (do_col) {
-      // columns 2cp, 2cp+1 of the tile, rows 16*crb .. 16*crb+15
-      uint32_t ca[8], cb[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w0 = tile[crb * 16 + 2 * i][cp], w1 = tile[crb * 16 + 2 * i + 1][cp];
-        ca[i] = __byte_perm(w0, w1, 0x5410);    // column 2cp: rows 2i, 2i+1
-        cb[i] = __byte_perm(w0, w1, 0x7632);    // column 2cp+1
-      }
-      const int64_t rr = r0 + 16 * crb;         // first input row of the block
-      const bool rin = rr < p.rows;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int64_t oc = c0 + 2 * cp + k;     // output row (= input column)
-        const bool cin = rin && oc < p.cols;
-        uint32_t sbc = 0;
-        const uint64_t cd = cin ? quant16(k ? cb : ca, s, sbc) : 0ull;
-        if (cin)
-          *reinterpret_cast<uint2 *>(codes_c + oc * (p.rows / 2) + rr / 2) =
-              make_uint2((uint32_t)cd, (uint32_t)(cd >> 32));
-        if (p.sf_swizzled) sfcol[2 * cp + k][crb] = (uint8_t)sbc;
-        else if (cin) sf_c[oc * nblk_c + rr / 16] = (uint8_t)sbc;
-      }
-      if (p.sf_swizzled) {
-        __syncthreads();
-        if (t < kTC) {
-          const int64_t oc2 = c0 + t;
-          const int64_t blk = r0 / 16;          // first of the tile's 4 column blocks
-          if (oc2 < p.cols && blk < sfc_pad_c)
-            *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc2, blk, sfc_pad_c)) =
-                *reinterpret_cast<const uint32_t *>(sfcol[t]);
-        }
-      }
-    }
+  // tile it of this CTA -> buffer it % 2 (thread 0)
+  int32_t issued = 0;
+  auto issue = [&](int32_t it) {
+    const int32_t tix = (int32_t)blockIdx.x + it * (int32_t)gridDim.x;
+    if (tix >= ntiles) return;
+    const int32_t tr = tix / tiles_c;
+    uint64_t *bar = &full[it & 1];
+    mbar_arrive_expect_tx(bar, kTileBytes);
+    tma_load_3d(qts + (it & 1) * kTileBytes, &tm, bar, (tix - tr * tiles_c) * kTC, tr * kTR, b);
+    issued = it + 1;
+  };
+  if (t == 0) {
+    issue(0);
+    issue(1);
   }
+  for (int32_t it = 0;; ++it) {
+    const int32_t tix = (int32_t)blockIdx.x + it * (int32_t)gridDim.x;
+    if (tix >= ntiles) break;
+    const int buf = it & 1;
+    const bool got = mbar_wait(&full[buf], (uint32_t)(it >> 1) & 1u, p.timeout_ns);
+    if (__syncthreads_or(!got)) {
+      if (t == 0) record_timeout(p.status);
+      break;
+    }
+    const uint32_t *tile = reinterpret_cast<const uint32_t *>(qts + buf * kTileBytes);   // [kTR][kTC/2] words
+    const int32_t tr = tix / tiles_c;
+    const int32_t r0 = tr * kTR, c0 = (tix - tr * tiles_c) * kTC;
+    if (do_row) {
+      const int32_t gr = r0 + rr, gq = c0 + 64 * qd;   // this thread's row and first column
+      if (gr < rows) {
+        // the 16-byte pairs are read in an order rotated by the quarter, so
+        // that the four quarters of a row hit different bank groups: w-block
+        // m holds block (m + qd) % 4 of the quarter
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int c = (k + 2 * qd) & 7;
+          const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr * (kTC / 2) + 32 * qd + 4 * c]);
+          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        }
+        const int nvalid = min(4, (cols - gq) / 16);
+        uint64_t cm[4];
+        uint32_t sm[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t(&wb)[8] = *reinterpret_cast<const uint32_t(*)[8]>(&w[8 * m]);
+          sm[m] = 0;
+          cm[m] = ((m + qd) & 3) < nvalid ? quant16_abs(wb, s, sm[m]) : 0ull;
+        }
+        // back to block order j = 0..3 (w-block (j - qd) % 4)
+        uint64_t cd[4];
+        uint32_t sbw = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int m0 = (j - qd) & 3;
+          cd[j] = m0 == 0 ? cm[0] : m0 == 1 ? cm[1] : m0 == 2 ? cm[2] : cm[3];
+          sbw |= (m0 == 0 ? sm[0] : m0 == 1 ? sm[1] : m0 == 2 ? sm[2] : sm[3]) << (8 * j);
+        }
+        store_blocks4(codes_r + (int64_t)gr * (cols / 2) + gq / 2, cd, nvalid);
+        const int32_t blk = gq / 16;
+        if (p.sf_swizzled) {
+          if (blk < sfc_pad_r) *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = sbw;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < nvalid) sf_r[(int64_t)gr * nblk_r + blk + j] = (uint8_t)(sbw >> (8 * j));
+        }
+      }
+    }
+    if (do_col) {
+      // rows 32*rh .. 32*rh+31 of columns 2cp, 2cp+1: blocks 2rh, 2rh+1 of each
+      uint64_t cda[2], cdb[2];
+      uint32_t sba[2], sbb[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int rb = 2 * rh + h2;               // 16-row block of the tile
+        uint32_t ca[8], cb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w0 = tile[(16 * rb + 2 * i) * (kTC / 2) + cp];
+          const uint32_t w1 = tile[(16 * rb + 2 * i + 1) * (kTC / 2) + cp];
+          ca[i] = __byte_perm(w0, w1, 0x5410);   // column 2cp: rows 2i, 2i+1
+          cb[i] = __byte_perm(w0, w1, 0x7632);   // column 2cp+1
+        }
+        const bool bin = r0 + 16 * rb < rows;
+        sba[h2] = sbb[h2] = 0;
+        cda[h2] = (bin && c0 + 2 * cp < cols) ? quant16_abs(ca, s, sba[h2]) : 0ull;
+        cdb[h2] = (bin && c0 + 2 * cp + 1 < cols) ? quant16_abs(cb, s, sbb[h2]) : 0ull;
+      }
+      // lane rh = 0 keeps column 2cp and receives its blocks 2, 3; lane rh = 1
+      // keeps column 2cp+1 and receives its blocks 0, 1
+      uint64_t keep[2], give[2];
+      uint32_t skeep[2], sgive[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        keep[h2] = rh ? cdb[h2] : cda[h2];
+        give[h2] = rh ? cda[h2] : cdb[h2];
+        skeep[h2] = rh ? sbb[h2] : sba[h2];
+        sgive[h2] = rh ? sba[h2] : sbb[h2];
+      }
+      uint64_t got2[2];
+      uint32_t sgot[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)give[h2], 1);
+        const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(give[h2] >> 32), 1);
+        got2[h2] = ((uint64_t)hi << 32) | lo;
+        sgot[h2] = __shfl_xor_sync(0xffffffffu, sgive[h2], 1);
+      }
+      const int32_t oc = c0 + 2 * cp + rh;        // this thread's output row (= input column)
+      if (oc < cols) {
+        const uint64_t cd[4] = {rh ? got2[0] : keep[0], rh ? got2[1] : keep[1], rh ? keep[0] : got2[0],
+                                rh ? keep[1] : got2[1]};
+        const uint32_t sbw = (rh ? sgot[0] : skeep[0]) | ((rh ? sgot[1] : skeep[1]) << 8) |
+                             ((rh ? skeep[0] : sgot[0]) << 16) | ((rh ? skeep[1] : sgot[1]) << 24);
+        const int nvalid = min(4, (rows - r0) / 16);
+        store_blocks4(codes_c + (int64_t)oc * (rows / 2) + r0 / 2, cd, nvalid);
+        const int32_t blk = r0 / 16;              // first of the tile's 4 column blocks
+        if (p.sf_swizzled) {
+          if (blk < sfc_pad_c) *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc, blk, sfc_pad_c)) = sbw;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < nvalid) sf_c[(int64_t)oc * nblk_c + blk + j] = (uint8_t)(sbw >> (8 * j));
+        }
+      }
+    }
+    __syncthreads();   // every read of this buffer is done
+    if (t == 0) issue(it + 2);
+  }
+  // tiles still in flight (only after a timeout) land before the CTA exits
+  if (t == 0)
+    for (int32_t it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
+      mbar_wait(&full[it & 1], (uint32_t)(it >> 1) & 1u, kTileDrainNs);
 }
 
 // ---------------------------------------------------------- grouped gather --
@@ -762,14 +854,28 @@ cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st
 }
 
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
+  // the source as [batch][rows][cols] bf16, one 256 x 64 x 1 box per tile
+  CUtensorMap tm;
+  const uint64_t dims[3] = {(uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)p.batch};
+  const uint64_t bstride = p.batch > 1 ? (uint64_t)p.bstride : (uint64_t)p.rows * (uint64_t)p.ld;
+  const uint64_t strides[2] = {(uint64_t)p.ld * 2, bstride * 2};
+  const uint32_t box[3] = {kTC, kTR, 1};
+  if (!make_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.src, dims, strides, box))
+    return cudaErrorInvalidValue;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_quant_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   const int64_t tiles = ((p.rows + kTR - 1) / kTR) * ((p.cols + kTC - 1) / kTC);
   int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 2 * kTileBytes);
   per_sm = std::max(per_sm, 1);
   // one wave of resident CTAs, shared by the matrices of the batch
   int64_t ctas = std::min<int64_t>(tiles, std::max<int64_t>(1, (int64_t)num_sms * per_sm / std::max<int64_t>(1, p.batch)));
   dim3 grid((unsigned)ctas, (unsigned)p.batch);
-  k_quant_tiles<<<grid, 256, 0, st>>>(p);
+  k_quant_tiles<<<grid, 256, 2 * kTileBytes, st>>>(p, tm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !p.sf_swizzled) return e;
   // rows beyond the matrix inside the last 128-row atom
