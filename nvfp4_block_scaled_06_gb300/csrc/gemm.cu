@@ -436,9 +436,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   dst[i2] = dst[i2] + f[i2];
                 }
             } else if (full_chunk) {
+              // whole 32-byte sectors per store where the row allows it
+              if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
 #pragma unroll
-              for (int i2 = 0; i2 < 32; i2 += 4)
-                *reinterpret_cast<float4 *>(dst + i2) = make_float4(f[i2], f[i2 + 1], f[i2 + 2], f[i2 + 3]);
+                for (int i2 = 0; i2 < 32; i2 += 8)
+                  st_global_v8(dst + i2, __float_as_uint(f[i2]), __float_as_uint(f[i2 + 1]),
+                               __float_as_uint(f[i2 + 2]), __float_as_uint(f[i2 + 3]), __float_as_uint(f[i2 + 4]),
+                               __float_as_uint(f[i2 + 5]), __float_as_uint(f[i2 + 6]), __float_as_uint(f[i2 + 7]));
+              } else {
+#pragma unroll
+                for (int i2 = 0; i2 < 32; i2 += 4)
+                  *reinterpret_cast<float4 *>(dst + i2) = make_float4(f[i2], f[i2 + 1], f[i2 + 2], f[i2 + 3]);
+              }
               if (p.sqnorm)
 #pragma unroll
                 for (int i2 = 0; i2 < 32; ++i2) sq += f[i2] * f[i2];
@@ -466,9 +475,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(f[2 * i2], f[2 * i2 + 1]);
                 w[i2] = *reinterpret_cast<const uint32_t *>(&h2);
               }
+              // whole 32-byte sectors per store where the row allows it
+              if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
+                st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+              } else {
 #pragma unroll
-              for (int i2 = 0; i2 < 16; i2 += 4)
-                *reinterpret_cast<uint4 *>(dst + 2 * i2) = make_uint4(w[i2], w[i2 + 1], w[i2 + 2], w[i2 + 3]);
+                for (int i2 = 0; i2 < 16; i2 += 4)
+                  *reinterpret_cast<uint4 *>(dst + 2 * i2) = make_uint4(w[i2], w[i2 + 1], w[i2 + 2], w[i2 + 3]);
+              }
               if (p.sqnorm)
 #pragma unroll
                 for (int i2 = 0; i2 < 32; ++i2) sq += f[i2] * f[i2];
