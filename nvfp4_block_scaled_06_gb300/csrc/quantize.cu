@@ -738,11 +738,13 @@ __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const 
 // ---------------------------------------------------------- grouped gather --
 // The expert-grouped, 128-padded A operand of the grouped GEMM from the token
 // rows quantized once (one tensor-wide g): destination row r takes the codes
-// and scales of token row_map[r]; rows with row_map < 0 (padding) are left
-// untouched.  Scales arrive in the linear [tokens][K/16] layout and leave in
-// the swizzled 128x4-atom layout (scale columns past K/16 inside the last
-// 4-column group are zero).  One warp per destination row: 16-byte copies of
-// the codes, one 4-scale word per lane step.
+// and scales of token row_map[r]; rows with row_map < 0 (padding) get no
+// codes and zero scales.  Scales arrive in the linear [tokens][K/16] layout and
+// leave in the swizzled 128x4-atom layout (scale columns past K/16 inside the
+// last 4-column group are zero).  One warp per group of four destination rows
+// r, r+32, r+64, r+96 of a 128-row group: their scale words share one 16-byte
+// slot of every atom, which the warp writes whole; each row's codes are copied
+// with up to eight 16-byte loads per lane in flight.
 __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict__ codes_src,
                                                        const uint8_t *__restrict__ sf_src,
                                                        const int32_t *__restrict__ row_map, int64_t rows,
@@ -752,36 +754,55 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t vec_per_row = K / 32;               // 16-byte vectors of codes
-  const int64_t nblk = K / 16, sfc_pad = (nblk + 3) & ~int64_t(3);
-  int64_t sr_next = warp < rows ? row_map[warp] : -1;
-  for (int64_t r = warp; r < rows; r += nwarps) {
-    const int64_t sr = sr_next;
-    if (r + nwarps < rows) sr_next = row_map[r + nwarps];   // prefetch the next row's source
-    if (sr < 0) continue;
-    const uint4 *cs = reinterpret_cast<const uint4 *>(codes_src + sr * (K / 2));
-    uint4 *cd = reinterpret_cast<uint4 *>(codes_dst + r * (K / 2));
-    // eight 16-byte loads in flight per lane before their stores
-    for (int64_t i0 = 0; i0 < vec_per_row; i0 += 256) {
-      uint4 v[8];
+  const int64_t nblk = K / 16, sfc_pad = (nblk + 3) & ~int64_t(3), ngrp = sfc_pad >> 2;
+  const int64_t quads = ((rows + 127) >> 7) * 32;
+  const bool word_sf = (nblk & 3) == 0;             // source scale rows are 4-byte aligned
+  for (int64_t qd = warp; qd < quads; qd += nwarps) {
+    const int64_t r0 = (qd >> 5) * 128 + (qd & 31);  // rows r0 + 32 i, i = 0..3
+    int64_t sr[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t i = i0 + 32 * j + lane;
-        if (i < vec_per_row) v[j] = __ldg(cs + i);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = r0 + 32 * i;
+      sr[i] = r < rows ? (int64_t)row_map[r] : -1;
+    }
+    // codes of the four rows, eight 16-byte loads per lane in flight
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int64_t i = i0 + 32 * j + lane;
-        if (i < vec_per_row) cd[i] = v[j];
+    for (int ri = 0; ri < 4; ++ri) {
+      if (sr[ri] < 0) continue;
+      const uint4 *cs = reinterpret_cast<const uint4 *>(codes_src + sr[ri] * (K / 2));
+      uint4 *cd = reinterpret_cast<uint4 *>(codes_dst + (r0 + 32 * ri) * (K / 2));
+      for (int64_t i0 = 0; i0 < vec_per_row; i0 += 256) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t i = i0 + 32 * j + lane;
+          if (i < vec_per_row) v[j] = __ldg(cs + i);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int64_t i = i0 + 32 * j + lane;
+          if (i < vec_per_row) cd[i] = v[j];
+        }
       }
     }
-    const uint8_t *ss = sf_src + sr * nblk;
-    uint8_t *sd = sf_dst + 16 * (r & 31) + 4 * ((r & 127) >> 5) + 512 * ((r >> 7) * (sfc_pad >> 2));
-    for (int64_t g = lane; g < (sfc_pad >> 2); g += 32) {
-      uint32_t w = 0;
+    // scales: slot 16 * (r0 % 32) of atom (r0 / 128, group) holds the four rows' words
+    uint8_t *sd = sf_dst + 512 * ((r0 >> 7) * ngrp) + 16 * (r0 & 31);
+    for (int64_t gI = lane; gI < ngrp; gI += 32) {
+      uint32_t w[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (4 * g + j < nblk) w |= (uint32_t)__ldg(ss + 4 * g + j) << (8 * j);
-      *reinterpret_cast<uint32_t *>(sd + 512 * g) = w;
+      for (int i = 0; i < 4; ++i) {
+        w[i] = 0;
+        if (sr[i] < 0) continue;
+        const uint8_t *ss = sf_src + sr[i] * nblk + 4 * gI;
+        if (word_sf) {
+          w[i] = __ldg(reinterpret_cast<const uint32_t *>(ss));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (4 * gI + j < nblk) w[i] |= (uint32_t)__ldg(ss + j) << (8 * j);
+        }
+      }
+      *reinterpret_cast<uint4 *>(sd + 512 * gI) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
@@ -789,7 +810,8 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
                                  int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
                                  cudaStream_t st) {
-  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms * 8));
+  const int64_t quads = ((rows + 127) / 128) * 32;   // one warp per four rows
+  const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((quads + 7) / 8, (int64_t)num_sms * 8));
   k_gather_packed<<<(unsigned)ctas, 256, 0, st>>>(codes_src, sf_src, row_map, rows, K, codes_dst, sf_dst);
   return cudaGetLastError();
 }
