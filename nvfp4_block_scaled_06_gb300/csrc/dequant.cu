@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(256) k_dequant_t(const uint8_t *__restrict__ c
   }
 }
 
-// Row-major: thread = (row, 64-column chunk), 128 bytes of bf16 out.
+// Row-major: thread = (row, 64-column chunk), 128 bytes of bf16 out as four
+// 32-byte stores where the row allows it.
 __global__ void __launch_bounds__(256) k_dequant_n(const uint8_t *__restrict__ codes,
                                                    const uint8_t *__restrict__ sf, int sf_swz,
                                                    const float *__restrict__ gp, int64_t rows, int64_t cols,
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(256) k_dequant_n(const uint8_t *__restrict__ c
     const uint4 c2[2] = {__ldg(src), __ldg(src + 1)};
     const uint32_t sw = scale_word(sf, sf_swz, r, ch * 4, nblk);
     uint4 *dst = reinterpret_cast<uint4 *>(out + r * ldo + ch * 64);
+    const bool whole = (reinterpret_cast<uintptr_t>(dst) & 31) == 0;   // 32-byte stores fill sectors
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       const float sd = __fmul_rn(e4m3_to_f32((sw >> (8 * b)) & 0xFF), g);
@@ -104,8 +106,12 @@ __global__ void __launch_bounds__(256) k_dequant_n(const uint8_t *__restrict__ c
         o[i] = bf16x2_bits(__fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF))), sd),
                            __fmul_rn(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))), sd));
       }
-      dst[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      if (whole) {
+        st_global_v8(dst + 2 * b, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+      } else {
+        dst[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
     }
   }
 }
