@@ -111,6 +111,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- helpers --
+def max_over_ranks(torch, ms, device, world):
+    """The slowest rank's time (every rank receives it), then a barrier."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return float(t)
+
+
+def job_value(world, flops_per_step, ms):
+    """Whole-job TFLOP/s: every rank runs the full step on its own GPU (weak
+    scaling), so the job does world x the step's FLOPs per ms of the slowest."""
+    return world * flops_per_step / (ms * 1e-3) / 1e12
+
+
 def ev_pairs(torch, n):
     return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(n)]
@@ -208,11 +224,7 @@ def run_main(args, torch, nv, device, rank, world):
         # event pair around the GEMM launch (an event between two launches
         # ends their programmatic overlap, so this run is not the headline)
         ms_prof = time_loop(torch, step, args.steps, 0, prof)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-        ms = float(t)
+    ms = max_over_ranks(torch, ms, device, world)
     gemm_ms = mean_ms(prof)
     flops = 2.0 * M * N * K
     # end to end: pinned host X in, host Y out, through the same C-ABI call
@@ -566,7 +578,7 @@ def main():
         return
 
     ms = main_res["ms"]
-    value = world * main_res["flops"] / (ms * 1e-3) / 1e12
+    value = job_value(world, main_res["flops"], ms)
     # the GEMM is timed inside a long run of steps: the sustained bf16 figure
     fp4_peak = pk["bf16_sustained"] * FP4_PER_BF16
     gemm_tflops = main_res["flops"] / (main_res["gemm_ms"] * 1e-3) / 1e12
@@ -590,11 +602,11 @@ def main():
                                 f"(nominal fp4:bf16)",
                       timing_note="CUDA events around each GEMM launch in a second run of the same "
                                   f"{args.steps} steps ({main_res['ms_prof']:.4f} ms/step with the events)"),
-        e2e=dict(value=world * main_res["flops"] / (e2e["ms"] * 1e-3) / 1e12, unit=UNIT,
+        e2e=dict(value=job_value(world, main_res["flops"], e2e["ms"]), unit=UNIT,
                  h2d_bytes_per_step=e2e["h2d"], d2h_bytes_per_step=e2e["d2h"],
                  overlap="steps pipelined: the input copy of step i+1 and the output copy of "
                          "step i-1 run during step i (two buffer sets, three streams)",
-                 serial_value=world * main_res["flops"] / (e2e["serial_ms"] * 1e-3) / 1e12),
+                 serial_value=job_value(world, main_res["flops"], e2e["serial_ms"])),
         gpu_launches=main_res["launches_per_step"] * args.steps,
         clocks=main_res["clocks"],
         secondary=sec,
