@@ -241,11 +241,14 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
   const float t_scale = p.t_f32 ? __fdiv_rn(p.lora_scale, acc_scale_of(g, *p.g_b)) : 0.0f;
   // last use of the source rows: let L2 drop them first
   const uint64_t pol = l2_policy_evict_first();
-  for (int64_t r = warp; r < rows_out; r += nwarps) {
+  // work item = (row, chunk of 128 blocks): short rows keep every warp busy
+  const int64_t nch = (sfc_pad + 127) / 128;
+  for (int64_t wi = warp; wi < rows_out * nch; wi += nwarps) {
+    const int64_t r = wi / nch, ch = wi - r * nch;
     int64_t sr = -1;
     if (r < p.dst_rows) sr = p.row_map ? (int64_t)p.row_map[r] : r;
     if (p.row_map && sr < 0) continue;   // unmapped (padding) rows are left untouched
-    if (p.t_f32 && r < p.dst_rows) {
+    if (p.t_f32 && r < p.dst_rows && ch == 0) {
       // LoRA hand-off: the down-projection's fp32 row, scaled and rounded once to bf16
       for (int j = lane; j < p.rank; j += 32) {
         float t = p.t_f32[r * p.rank + j];
@@ -254,7 +257,8 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
       }
     }
     const __nv_bfloat16 *srow = src + sr * p.ld;
-    for (int64_t blk0 = 0; blk0 < sfc_pad; blk0 += 128) {
+    {
+      const int64_t blk0 = ch * 128;
       uint32_t w[4][8];
       uint64_t c[4];
       uint32_t sb[4];
@@ -862,9 +866,13 @@ cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st
   // bulk copies need 16-byte aligned rows and segments
   const bool staged = ((reinterpret_cast<uintptr_t>(p.src) & 15) == 0) && (p.ld % 8 == 0) &&
                       (p.bstride % 8 == 0) && (p.cols % 16 == 0);
-  if (staged) return launch_quant_rows_staged(p, num_sms, st);
+  // a few rows (decode activations) take the plain kernel: the staged ring's
+  // set-up would outweigh the work
+  const bool tiny = p.dst_rows <= 64 && p.batch == 1 && !p.row_map;
+  if (staged && !tiny) return launch_quant_rows_staged(p, num_sms, st);
   const int64_t rows_out = p.sf_swizzled ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
-  int64_t ctas = (rows_out + 7) / 8;      // 8 warps per CTA, one row each per pass
+  const int64_t nch = ((p.cols / 16 + 3) / 4 * 4 + 127) / 128;
+  int64_t ctas = (rows_out * nch + 7) / 8;      // 8 warps per CTA, one (row, chunk) each per pass
   const int64_t cap = (int64_t)num_sms * 8 / std::max<int64_t>(1, p.batch);
   ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, std::max<int64_t>(cap, 1)));
   dim3 grid((unsigned)ctas, (unsigned)p.batch);
