@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) k_dequant_t(const uint8_t *__restrict__ c
                                                    const uint8_t *__restrict__ sf, int sf_swz,
                                                    const float *__restrict__ gp, int64_t rows, int64_t cols,
                                                    __nv_bfloat16 *__restrict__ out, int64_t ldo) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const float g = *gp;
   const int64_t pairs = rows / 2, chunks = cols / 64, nblk = cols / 16;
   const int64_t total = pairs * chunks;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(256) k_dequant_n(const uint8_t *__restrict__ c
                                                    const uint8_t *__restrict__ sf, int sf_swz,
                                                    const float *__restrict__ gp, int64_t rows, int64_t cols,
                                                    __nv_bfloat16 *__restrict__ out, int64_t ldo) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const float g = *gp;
   const int64_t chunks = cols / 64, nblk = cols / 16;
   const int64_t total = rows * chunks;
@@ -122,10 +126,9 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *sf, int sf_swz, 
   const int64_t work = transpose ? (rows / 2) * (cols / 64) : rows * (cols / 64);
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, (int64_t)num_sms * 8));
   if (transpose)
-    k_dequant_t<<<(unsigned)ctas, 256, 0, st>>>(codes, sf, sf_swz, g, rows, cols, out, ldo);
+    return launch_pdl(k_dequant_t, dim3((unsigned)ctas), dim3(256), 0, st, codes, sf, sf_swz, g, rows, cols, out, ldo);
   else
-    k_dequant_n<<<(unsigned)ctas, 256, 0, st>>>(codes, sf, sf_swz, g, rows, cols, out, ldo);
-  return cudaGetLastError();
+    return launch_pdl(k_dequant_n, dim3((unsigned)ctas), dim3(256), 0, st, codes, sf, sf_swz, g, rows, cols, out, ldo);
 }
 
 }  // namespace nvfp4

@@ -864,6 +864,8 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
 
 // ----------------------------------------------------------- split-K sum --
 __global__ void k_splitk_reduce(const GemmParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const int64_t total = p.M * p.N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -878,8 +880,7 @@ __global__ void k_splitk_reduce(const GemmParams p) {
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st) {
   const int64_t total = p.M * p.N;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 4));
-  k_splitk_reduce<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_splitk_reduce, dim3(grid), dim3(256), 0, st, p);
 }
 
 // ----------------------------------------------------------------- launch --

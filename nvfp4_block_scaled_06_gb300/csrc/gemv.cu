@@ -217,6 +217,8 @@ __device__ __forceinline__ GemvPlan gemv_plan(const GemvParams &p, int nchunks) 
 
 template <int MX>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[2][kWarps][kRows][4];   // in-CTA chunk sums, double-buffered
   const int64_t K = p.K, nblk = K / 16;
@@ -324,6 +326,8 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
 }
 
 __global__ void k_gemv_reduce(const GemvParams p, int nchunks, int mx, const float *partial) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const float alpha = __fmul_rn(*p.g_x, *p.g_w);
   const int64_t total = (int64_t)mx * p.N;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -361,11 +365,9 @@ static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, 
   const int64_t ctas_needed = nchunks <= kWarps ? (nb + kWarps / nchunks - 1) / (kWarps / nchunks)
                                                 : (nb * nchunks + kWarps - 1) / kWarps;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, ctas_needed));
-  k_gemv<MX><<<grid, kGemvThreads, smem, st>>>(p, nchunks, partial);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_gemv<MX>, dim3(grid), dim3(kGemvThreads), smem, st, p, nchunks, partial);
   if (e != cudaSuccess || nchunks <= kWarps) return e;
-  k_gemv_reduce<<<num_sms, 256, 0, st>>>(p, nchunks, MX, partial);
-  return cudaGetLastError();
+  return launch_pdl(k_gemv_reduce, dim3(num_sms), dim3(256), 0, st, p, nchunks, (int)MX, (const float *)partial);
 }
 
 cudaError_t launch_gemv_ws(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {

@@ -179,6 +179,8 @@ __device__ __forceinline__ void load16(const __nv_bfloat16 *src, uint32_t (&w)[8
 // Grid (nparts, batch).  Part i of matrix b reduces rows i, i+nparts, ... and
 // writes max |bf16| magnitude bits to amax_part[b*nparts + i].
 __global__ void __launch_bounds__(256) k_amax_partial(QuantParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ uint32_t scratch[32];
   const int b = blockIdx.y;
   const __nv_bfloat16 *base = p.src + (int64_t)b * p.bstride;
@@ -220,6 +222,8 @@ __global__ void __launch_bounds__(256) k_amax_partial(QuantParams p) {
 // written (zeros outside the matrix).
 template <bool kV8>
 __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ uint32_t scratch[32];
   __shared__ float senc_tab[128];
   const int b = blockIdx.y;
@@ -575,6 +579,8 @@ __device__ __forceinline__ void store_blocks4(uint8_t *dst, const uint64_t (&cd)
 }
 
 __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const __grid_constant__ CUtensorMap tm) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ __align__(128) uint8_t qts[];           // two tiles [kTR][kTC] bf16, row-major
   __shared__ uint32_t scratch[32];
   __shared__ float senc_tab[128];
@@ -754,6 +760,8 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
                                                        const int32_t *__restrict__ row_map, int64_t rows,
                                                        int64_t K, uint8_t *__restrict__ codes_dst,
                                                        uint8_t *__restrict__ sf_dst) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -816,14 +824,16 @@ cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src
                                  cudaStream_t st) {
   const int64_t quads = ((rows + 127) / 128) * 32;   // one warp per four rows
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((quads + 7) / 8, (int64_t)num_sms * 8));
-  k_gather_packed<<<(unsigned)ctas, 256, 0, st>>>(codes_src, sf_src, row_map, rows, K, codes_dst, sf_dst);
-  return cudaGetLastError();
+  return launch_pdl(k_gather_packed, dim3((unsigned)ctas), dim3(256), 0, st, codes_src, sf_src, row_map, rows, K,
+                    codes_dst, sf_dst);
 }
 
 // Zero the swizzled padding of a scale buffer that the tile kernel does not
 // reach: rows in [rows, pad128(rows)) of every matrix.  Columns beyond the
 // matrix inside a reached row are written by the kernels themselves.
 __global__ void k_zero_sf_pad_rows(uint8_t *sf, int64_t bstride, int64_t rows, int64_t sf_cols) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   const int b = blockIdx.y;
   const int64_t sfc_pad = (sf_cols + 3) & ~int64_t(3);
   const int64_t prow = (rows + 127) & ~int64_t(127);
@@ -841,8 +851,7 @@ int amax_parts_for(int64_t rows) { return (int)std::min<int64_t>(rows, 512); }
 
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st) {
   dim3 grid(p.nparts, (unsigned)p.batch);
-  k_amax_partial<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_amax_partial, grid, dim3(256), 0, st, p);
 }
 
 static cudaError_t launch_quant_rows_staged(const QuantParams &p, int num_sms, cudaStream_t st) {
@@ -878,9 +887,8 @@ cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st
   dim3 grid((unsigned)ctas, (unsigned)p.batch);
   const bool v8 = ((reinterpret_cast<uintptr_t>(p.src) & 31) == 0) && (p.ld % 16 == 0) &&
                   (p.bstride % 16 == 0);
-  if (v8) k_quant_rows<true><<<grid, 256, 0, st>>>(p);
-  else k_quant_rows<false><<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  if (v8) return launch_pdl(k_quant_rows<true>, grid, dim3(256), 0, st, p);
+  return launch_pdl(k_quant_rows<false>, grid, dim3(256), 0, st, p);
 }
 
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
@@ -905,17 +913,20 @@ cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t s
   // one wave of resident CTAs, shared by the matrices of the batch
   int64_t ctas = std::min<int64_t>(tiles, std::max<int64_t>(1, (int64_t)num_sms * per_sm / std::max<int64_t>(1, p.batch)));
   dim3 grid((unsigned)ctas, (unsigned)p.batch);
-  k_quant_tiles<<<grid, 256, 2 * kTileBytes, st>>>(p, tm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_quant_tiles, grid, dim3(256), 2 * kTileBytes, st, p, tm);
   if (e != cudaSuccess || !p.sf_swizzled) return e;
   // rows beyond the matrix inside the last 128-row atom
   if (p.codes_row && (p.rows % 128) != 0) {
-    k_zero_sf_pad_rows<<<dim3(4, (unsigned)p.batch), 256, 0, st>>>(p.sf_row, p.sf_row_bstride,
-                                                                  p.rows, p.cols / 16);
+    if (cudaError_t e2 = launch_pdl(k_zero_sf_pad_rows, dim3(4, (unsigned)p.batch), dim3(256), 0, st, p.sf_row,
+                                    p.sf_row_bstride, p.rows, p.cols / 16);
+        e2 != cudaSuccess)
+      return e2;
   }
   if (p.codes_col && (p.cols % 128) != 0) {
-    k_zero_sf_pad_rows<<<dim3(4, (unsigned)p.batch), 256, 0, st>>>(p.sf_col, p.sf_col_bstride,
-                                                                  p.cols, p.rows / 16);
+    if (cudaError_t e2 = launch_pdl(k_zero_sf_pad_rows, dim3(4, (unsigned)p.batch), dim3(256), 0, st, p.sf_col,
+                                    p.sf_col_bstride, p.cols, p.rows / 16);
+        e2 != cudaSuccess)
+      return e2;
   }
   return cudaGetLastError();
 }

@@ -18,6 +18,8 @@ namespace nvfp4 {
 constexpr int kRouteChunk = 1024;
 
 __global__ void __launch_bounds__(1024) k_route_hist(const RouteParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ int32_t sh_hist[];   // [E]
   for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x) sh_hist[e] = 0;
   __syncthreads();
@@ -59,6 +61,8 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t *scra
 }
 
 __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ int32_t scratch[64];
   const int e = threadIdx.x;
   const bool act = e < p.num_experts;
@@ -107,6 +111,8 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
 }
 
 __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ int32_t sh_base[];   // [E] first grouped position of this chunk's pairs
   const int E = p.num_experts;
   uint16_t *sh_cnt = reinterpret_cast<uint16_t *>(sh_base + E);   // [32 warps][E]
@@ -139,11 +145,9 @@ __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
 }
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
-  k_route_hist<<<p.nchunks, kRouteChunk, p.num_experts * sizeof(int32_t), st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_route_hist, dim3(p.nchunks), dim3(kRouteChunk), p.num_experts * sizeof(int32_t), st, p);
   if (e != cudaSuccess) return e;
-  k_route_scan<<<1, 1024, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(k_route_scan, dim3(1), dim3(1024), 0, st, p);
   if (e != cudaSuccess) return e;
   const size_t sm = (size_t)p.num_experts * sizeof(int32_t) + (size_t)32 * p.num_experts * sizeof(uint16_t);
   static size_t configured = 48 * 1024;
@@ -152,8 +156,7 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = sm;
   }
-  k_route_scatter<<<p.nchunks, kRouteChunk, sm, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_route_scatter, dim3(p.nchunks), dim3(kRouteChunk), sm, st, p);
 }
 
 // ------------------------------------------- layout from given expert offsets --
@@ -164,6 +167,8 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
 __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restrict__ offsets, int E,
                                                          int32_t *poffsets, GroupTile *gtiles,
                                                          int32_t *gnum_mtiles) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ int32_t scratch[64];
   const int e = threadIdx.x;
   const bool act = e < E;
@@ -194,6 +199,8 @@ __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restri
 __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ offsets,
                                       const int32_t *__restrict__ poffsets, int E, int64_t rows,
                                       int32_t *row_map) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
        r += (int64_t)gridDim.x * blockDim.x) {
     int32_t v = -1;
@@ -214,12 +221,11 @@ __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ offsets,
 cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t padded_rows_max,
                                        int32_t *poffsets, GroupTile *gtiles, int32_t *gnum_mtiles,
                                        int32_t *row_map, int num_sms, cudaStream_t st) {
-  k_offsets_layout<<<1, 1024, 0, st>>>(offsets, E, poffsets, gtiles, gnum_mtiles);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_offsets_layout, dim3(1), dim3(1024), 0, st, offsets, E, poffsets, gtiles, gnum_mtiles);
   if (e != cudaSuccess) return e;
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((padded_rows_max + 255) / 256, (int64_t)num_sms * 4));
-  k_rowmap_from_offsets<<<(unsigned)ctas, 256, 0, st>>>(offsets, poffsets, E, padded_rows_max, row_map);
-  return cudaGetLastError();
+  return launch_pdl(k_rowmap_from_offsets, dim3((unsigned)ctas), dim3(256), 0, st, offsets,
+                    (const int32_t *)poffsets, E, padded_rows_max, row_map);
 }
 
 // ----------------------------------------------------------------- combine --
@@ -227,6 +233,8 @@ cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pa
 // accumulation (one fused multiply-add per slot), rounded once to bf16, where
 // g(t, j) is the grouped row of pair t*top_k + j (the inverse of perm).
 __global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, int32_t *inv) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pairs;
        i += (int64_t)gridDim.x * blockDim.x)
     inv[perm[i]] = (int32_t)i;
@@ -239,6 +247,8 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
                                                      const int32_t *__restrict__ inv,
                                                      const float *__restrict__ w, int64_t tokens, int top_k,
                                                      int64_t N, __nv_bfloat16 *__restrict__ y) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
   constexpr int kMaxK = 8;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -311,12 +321,11 @@ cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int3
                                cudaStream_t st) {
   const int64_t pairs = tokens * top_k;
   const int64_t c1 = std::max<int64_t>(1, std::min<int64_t>((pairs + 255) / 256, (int64_t)num_sms * 4));
-  k_invert_perm<<<(unsigned)c1, 256, 0, st>>>(perm, pairs, inv);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_invert_perm, dim3((unsigned)c1), dim3(256), 0, st, perm, pairs, inv);
   if (e != cudaSuccess) return e;
   const int64_t c2 = std::max<int64_t>(1, std::min<int64_t>((tokens + 7) / 8, (int64_t)num_sms * 8));
-  k_moe_combine<<<(unsigned)c2, 256, 0, st>>>(d, inv, w, tokens, top_k, N, y);
-  return cudaGetLastError();
+  return launch_pdl(k_moe_combine, dim3((unsigned)c2), dim3(256), 0, st, d, (const int32_t *)inv, w, tokens, top_k,
+                    N, y);
 }
 
 }  // namespace nvfp4
