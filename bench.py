@@ -9,12 +9,19 @@ FP4 GEMM with the fused LoRA up-projection), bf16 out.  value = FP4 TFLOP/s
 
 Also measured in the same run (the "secondary" object): the expert-weight
 quantization sweep (32 x [2048,6144], row + column packings, GB/s), the decode
-projections (q_b_proj, o_proj at M = 1, 8, 32: weight GB/s) and the grouped MoE
-up-projection (4096 tokens, top-8 of 256 experts, LoRA r64: TFLOP/s and GB/s).
+projections (q_b_proj, o_proj at M = 1, 8, 32: weight GB/s), the grouped MoE
+up-projection (4096 tokens, top-8 of 256 experts, LoRA r64: TFLOP/s and GB/s),
+the backward of the prefill linear (both Dgrad forms and the FP4 Wgrad) and the
+MoE down-projection with the gate-weighted combine.
 
 Timing: CUDA events on the launching stream, after >= 3 warm-up steps;
 inputs rotate over buffers whose total exceeds L2, so no step reads its input
-from L2.  N > 1 (torchrun): every rank runs the same workload on its own GPU
+from L2.  value comes from steps with nothing recorded between the launches;
+the GEMM kernel's launch durations (roofline.achieved) from a second run of
+the same steps with the library's event pair around the GEMM launch.  e2e
+moves every step's X in from pinned host memory and its Y back out, steps
+pipelined over two buffer sets and three streams (serial_value: one after
+another).  N > 1 (torchrun): every rank runs the same workload on its own GPU
 (replicas; the layer has no data-path exchange on one GPU per replica); the
 time is the max over ranks and value is the total over ranks.
 
