@@ -67,9 +67,18 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
   const int e = threadIdx.x;
   const bool act = e < p.num_experts;
   int32_t count = 0;
-  if (act) {
-    // eight independent loads in flight per step (the chunk bases are formed
-    // by the scatter kernel)
+  // up to 32 chunks: every chunk count of this expert in registers at once,
+  // and after the scan each chunk's first grouped position is written back
+  // over its count; more chunks: eight loads in flight per step, and the
+  // scatter kernel forms the chunk bases itself
+  const bool few = p.nchunks <= 32;
+  int32_t hv[32];
+  if (act && few) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) hv[j] = j < p.nchunks ? p.hist[(int64_t)j * p.num_experts + e] : 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) count += hv[j];
+  } else if (act) {
     int c = 0;
     for (; c + 8 <= p.nchunks; c += 8) {
       int32_t v[8];
@@ -86,6 +95,14 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
   const int32_t off = block_exclusive_scan(count, scratch, total);
   const int32_t poff = block_exclusive_scan(padded, scratch, ptotal);
   const int32_t moff = block_exclusive_scan(mt, scratch, mtotal);
+  if (act && few) {
+    int32_t b = off;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j < p.nchunks) p.hist[(int64_t)j * p.num_experts + e] = b;
+      b += hv[j];
+    }
+  }
   if (act) {
     p.counts[e] = count;
     p.offsets[e] = off;
@@ -118,9 +135,13 @@ __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
   uint16_t *sh_cnt = reinterpret_cast<uint16_t *>(sh_base + E);   // [32 warps][E]
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) sh_cnt[i] = 0;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t b = p.offsets[e];
-    for (int c = 0; c < (int)blockIdx.x; ++c) b += p.hist[(int64_t)c * E + e];
-    sh_base[e] = b;
+    if (p.nchunks <= 32) {
+      sh_base[e] = p.hist[(int64_t)blockIdx.x * E + e];   // written by the scan kernel
+    } else {
+      int32_t b = p.offsets[e];
+      for (int c = 0; c < (int)blockIdx.x; ++c) b += p.hist[(int64_t)c * E + e];
+      sh_base[e] = b;
+    }
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
