@@ -733,6 +733,7 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   q.sf_swizzled = 1;
   q.row_map = pl.row_map;
   q.dst_rows = pl.prow_max;
+  q.num_mtiles = pl.nmt;   // rows past the routed layout are never read
   q.status = status;
   q.timeout_ns = tmo;
   if (!a->h_global_scale) {

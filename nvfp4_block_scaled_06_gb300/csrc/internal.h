@@ -28,6 +28,7 @@ struct QuantParams {
   int sf_swizzled;
   const int32_t *row_map;             // optional gather: dst row -> src row (<0: skip)
   int64_t dst_rows;                   // rows written by the row packing
+  const int32_t *num_mtiles;          // optional (device, batch 1): only rows < 128 x this are in use
   // optional LoRA hand-off: T' = bf16(T * (lora_scale / (g * g_b))) per row
   const float *t_f32;                 // [t_splits][dst_rows][rank], summed in order
   int t_splits;

@@ -387,8 +387,10 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
   griddep_launch_dependents();
   griddep_wait();   // inputs of this kernel come from the previous one in the stream
 
-  const int64_t rows_out =
-      (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  int64_t rows_out = (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
+  // a layout whose used size is known only on the device: split the rows in
+  // use evenly (the rest are never read)
+  if (p.num_mtiles && p.batch == 1) rows_out = min(rows_out, (int64_t)128 * (int64_t)*p.num_mtiles);
   const int64_t per_b = rows_out * nseg, U = per_b * p.batch;
   const int64_t W = (int64_t)gridDim.x * kQWarps, gw = (int64_t)blockIdx.x * kQWarps + warp;
   // an even split: every warp gets floor(U/W) or ceil(U/W) consecutive units
