@@ -623,7 +623,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
     if (cudaError_t e_ = launch_amax(q, st); e_ != cudaSuccess) return cuda_status(e_);
   }
   if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
-  if (cudaError_t e_ = launch_gather_packed(pl.xq_tok, pl.xsf_tok, pl.row_map, pl.prow_max, a->K, pl.xq,
+  if (cudaError_t e_ = launch_gather_packed(pl.xq_tok, pl.xsf_tok, pl.row_map, pl.prow_max, pl.nmt, a->K, pl.xq,
                                             pl.xsf, sms, st);
       e_ != cudaSuccess)
     return cuda_status(e_);

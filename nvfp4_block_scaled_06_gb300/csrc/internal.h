@@ -57,7 +57,7 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *sf, int sf_swz, 
                            cudaStream_t st);
 // Token-row codes + linear scales -> expert-grouped rows + swizzled scales.
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
-                                 int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
+                                 int64_t rows, const int32_t *num_mtiles, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
                                  cudaStream_t st);
 
 // --------------------------------------------------------------------- GEMM --

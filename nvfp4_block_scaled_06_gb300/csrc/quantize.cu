@@ -760,7 +760,8 @@ __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const 
 __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict__ codes_src,
                                                        const uint8_t *__restrict__ sf_src,
                                                        const int32_t *__restrict__ row_map, int64_t rows,
-                                                       int64_t K, uint8_t *__restrict__ codes_dst,
+                                                       const int32_t *__restrict__ num_mtiles, int64_t K,
+                                                       uint8_t *__restrict__ codes_dst,
                                                        uint8_t *__restrict__ sf_dst) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
@@ -769,6 +770,8 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t vec_per_row = K / 32;               // 16-byte vectors of codes
   const int64_t nblk = K / 16, sfc_pad = (nblk + 3) & ~int64_t(3), ngrp = sfc_pad >> 2;
+  // only the rows of the routed layout (128 x its m-tile count) are read later
+  if (num_mtiles) rows = min(rows, (int64_t)128 * (int64_t)*num_mtiles);
   const int64_t quads = ((rows + 127) >> 7) * 32;
   const bool word_sf = (nblk & 3) == 0;             // source scale rows are 4-byte aligned
   for (int64_t qd = warp; qd < quads; qd += nwarps) {
@@ -822,12 +825,12 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
 }
 
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
-                                 int64_t rows, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
+                                 int64_t rows, const int32_t *num_mtiles, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
                                  cudaStream_t st) {
   const int64_t quads = ((rows + 127) / 128) * 32;   // one warp per four rows
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((quads + 7) / 8, (int64_t)num_sms * 8));
-  return launch_pdl(k_gather_packed, dim3((unsigned)ctas), dim3(256), 0, st, codes_src, sf_src, row_map, rows, K,
-                    codes_dst, sf_dst);
+  return launch_pdl(k_gather_packed, dim3((unsigned)ctas), dim3(256), 0, st, codes_src, sf_src, row_map, rows,
+                    num_mtiles, K, codes_dst, sf_dst);
 }
 
 // Zero the swizzled padding of a scale buffer that the tile kernel does not
