@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
     if (p.offsets_out) p.offsets_out[p.num_experts] = total;
     *p.gnum_mtiles = mtotal;
   }
-  for (int64_t r = ptotal + threadIdx.x; r < p.padded_rows_max; r += blockDim.x) p.row_map[r] = -1;
+  // rows past ptotal (= 128 x the m-tile count) are never read: every user of
+  // the layout is bounded by the m-tile count
 }
 
 __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
