@@ -31,7 +31,6 @@ namespace nvfp4 {
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lanes x 64
-constexpr int kRows = 4;           // units (rows) a warp has in flight
 
 // Doubled E2M1 magnitudes {0,1,2,3,4,6,8,12} as bytes of two words: byte c of
 // (lo, hi) is 2*E2M1(c) for c = 0..7 (a byte-permute lookup table).
@@ -84,7 +83,8 @@ __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g,
   }
 }
 
-// A warp's task is kRows consecutive rows of one 2048-element K chunk.  Tasks
+// A warp's task is R consecutive rows of one 2048-element K chunk (R = 2 when
+// a row is one chunk, so twice the tasks are in flight; R = 4 otherwise).  Tasks
 // are ordered row-major (all chunks of a row batch are adjacent), so a CTA
 // streams whole rows.  With at most kWarps chunks per row, one CTA holds every
 // chunk of its row batches at once: the warps' chunk sums meet in shared
@@ -95,20 +95,22 @@ __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g,
 // so the weight stream starts at kernel entry.
 constexpr int kWarps = kGemvThreads / 32;
 
+template <int R>
 struct GemvBatch {
-  uint32_t c[kRows][8];   // 64 codes of each row for this lane
-  uint32_t sf[kRows];     // the 4 block scales of this lane's 64 codes
-  int32_t n0, g4;         // first row of the task; this lane's 64-element group (-1: none)
+  uint32_t c[R][8];   // 64 codes of each row for this lane
+  uint32_t sf[R];     // the 4 block scales of this lane's 64 codes
+  int32_t n0, g4;     // first row of the task; this lane's 64-element group (-1: none)
 };
 
+template <int R>
 __device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t n0, int32_t kc, int32_t g4_total,
-                                          int lane, GemvBatch &B) {
+                                          int lane, GemvBatch<R> &B) {
   B.n0 = n0;
   const int32_t g4 = kc * (kGemvChunk / 64) + lane;
   B.g4 = g4 < g4_total ? g4 : -1;
   const int64_t row_bytes = p.K / 2;
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) {
+  for (int j = 0; j < R; ++j) {
     const int32_t n = n0 + j;
     if (B.g4 >= 0 && n < p.N) {
       asm volatile(
@@ -125,13 +127,13 @@ __device__ __forceinline__ void gemv_load(const GemvParams &p, int32_t n0, int32
 // The chunk sums of the task's rows: on return lane m (< MX) holds row j's
 // sum for activation row m in out[j].  Blocks outer, rows inner: the lane's X
 // words of a block are read from shared memory once for all rows.
-template <int MX>
-__device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatch &B, const uint32_t *xs,
+template <int MX, int R>
+__device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatch<R> &B, const uint32_t *xs,
                                              const float *sxs, int64_t G4, int64_t nblk, int lane,
-                                             float (&out)[kRows]) {
-  float acc[kRows][MX];
+                                             float (&out)[R]) {
+  float acc[R][MX];
 #pragma unroll
-  for (int j = 0; j < kRows; ++j)
+  for (int j = 0; j < R; ++j)
 #pragma unroll
     for (int m = 0; m < MX; ++m) acc[j][m] = 0.0f;
   if (B.g4 >= 0) {
@@ -148,7 +150,7 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
         sx[m] = sxs[m * nblk + bb * G4 + B.g4];
       }
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) {
+      for (int j = 0; j < R; ++j) {
         if (B.n0 + j >= p.N) continue;
         const float sw = e4m3_to_f32((B.sf[j] >> (8 * bb)) & 0xFF);
         // per group of four codes: the doubled magnitudes of the positive
@@ -178,7 +180,7 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
     }
   }
 #pragma unroll
-  for (int j = 0; j < kRows; ++j) {
+  for (int j = 0; j < R; ++j) {
 #pragma unroll
     for (int m = 0; m < MX; ++m)
 #pragma unroll
@@ -204,23 +206,24 @@ struct GemvPlan {
   bool in_cta;
 };
 
+template <int R>
 __device__ __forceinline__ GemvPlan gemv_plan(const GemvParams &p, int nchunks) {
   GemvPlan q;
   q.nchunks = nchunks;
   q.in_cta = nchunks <= kWarps;
-  const int32_t nb = (int32_t)((p.N + kRows - 1) / kRows);
+  const int32_t nb = (int32_t)((p.N + R - 1) / R);
   q.rbu = q.in_cta ? kWarps / nchunks : 1;
   q.units = q.in_cta ? (nb + q.rbu - 1) / q.rbu : nb * nchunks;
   q.g4_total = (int32_t)(p.K / 64);
   return q;
 }
 
-template <int MX>
+template <int MX, int R>
 __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ float red[2][kWarps][kRows][4];   // in-CTA chunk sums, double-buffered
+  __shared__ float red[2][kWarps][R][4];   // in-CTA chunk sums, double-buffered
   const int64_t K = p.K, nblk = K / 16;
   // Shared layout chosen so that the 32 lanes of a warp, which take 32
   // consecutive 64-element groups g4, read consecutive 16-byte words:
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const GemvPlan q = gemv_plan(p, nchunks);
+  const GemvPlan q = gemv_plan<R>(p, nchunks);
   // this warp's task in unit u (in-CTA) / task index (global)
   const bool active = !q.in_cta || w < q.rbu * q.nchunks;
   const int32_t my_kc = q.in_cta ? w % q.nchunks : 0, my_rb = q.in_cta ? w / q.nchunks : 0;
@@ -240,15 +243,15 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   int32_t u = q.in_cta ? (int32_t)blockIdx.x : (int32_t)blockIdx.x * kWarps + w;
   auto task_of = [&](int32_t unit, int32_t &n0, int32_t &kc) {
     if (q.in_cta) {
-      n0 = (unit * q.rbu + my_rb) * kRows;
+      n0 = (unit * q.rbu + my_rb) * R;
       kc = my_kc;
     } else {
-      n0 = (unit / q.nchunks) * kRows;
+      n0 = (unit / q.nchunks) * R;
       kc = unit % q.nchunks;
     }
   };
 
-  GemvBatch A, B;
+  GemvBatch<R> A, B;
   if (active && u < q.units) {   // weights in flight first
     int32_t n0, kc;
     task_of(u, n0, kc);
@@ -276,35 +279,35 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   int buf = 0;
   // one unit: this warp's task (batch `cur`, prefetching the next unit into
   // `nxt`), then the output of the unit
-  auto run_unit = [&](int32_t unit, const GemvBatch &cur, GemvBatch &nxt) {
+  auto run_unit = [&](int32_t unit, const GemvBatch<R> &cur, GemvBatch<R> &nxt) {
     const int32_t un = unit + ustep;
     if (active && un < q.units) {
       int32_t n0, kc;
       task_of(un, n0, kc);
       gemv_load(p, n0, kc, q.g4_total, lane, nxt);
     }
-    float v[kRows];
-    if (active) gemv_compute<MX>(p, cur, xs, sxs, G4, nblk, lane, v);
+    float v[R];
+    if (active) gemv_compute<MX, R>(p, cur, xs, sxs, G4, nblk, lane, v);
     if (!q.in_cta) {
       const int32_t kc = unit % q.nchunks;
 #pragma unroll
-      for (int j = 0; j < kRows; ++j)
+      for (int j = 0; j < R; ++j)
         if (cur.n0 + j < p.N && lane < MX) partial[((int64_t)kc * MX + lane) * p.N + cur.n0 + j] = v[j];
     } else if (q.nchunks == 1) {
       if (active)
 #pragma unroll
-        for (int j = 0; j < kRows; ++j)
+        for (int j = 0; j < R; ++j)
           if (cur.n0 + j < p.N && lane < MX) gemv_store(p, lane, cur.n0 + j, __fmul_rn(v[j], alpha));
     } else {
       if (active && lane < MX)
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) red[buf][w][j][lane] = v[j];
+        for (int j = 0; j < R; ++j) red[buf][w][j][lane] = v[j];
       __syncthreads();
       // chunk sums of each output added in chunk order
       const int t = threadIdx.x;
-      if (t < q.rbu * kRows * MX) {
-        const int rbl = t / (kRows * MX), j = (t / MX) % kRows, m = t % MX;
-        const int64_t n = (int64_t)(unit * q.rbu + rbl) * kRows + j;
+      if (t < q.rbu * R * MX) {
+        const int rbl = t / (R * MX), j = (t / MX) % R, m = t % MX;
+        const int64_t n = (int64_t)(unit * q.rbu + rbl) * R + j;
         if (n < p.N) {
           float sum = 0.0f;
           for (int kc = 0; kc < q.nchunks; ++kc) sum = __fadd_rn(sum, red[buf][rbl * q.nchunks + kc][j][m]);
@@ -347,25 +350,32 @@ size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   return c > kWarps ? (size_t)c * M * N * sizeof(float) : 0;
 }
 
-template <int MX>
-static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {
+template <int MX, int R>
+static cudaError_t launch_mxr(const GemvParams &p, int nchunks, int num_sms, cudaStream_t st, float *partial) {
   const size_t smem = gemv_smem_bytes(MX, p.K);
-  static size_t configured = 48 * 1024 - sizeof(float) * 2 * kWarps * kRows * 4;
+  static size_t configured = 48 * 1024 - sizeof(float) * 2 * kWarps * R * 4;
   if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<MX, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  const int nchunks = gemv_chunks(p.K);
   int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX>, kGemvThreads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX, R>, kGemvThreads, smem);
   per_sm = std::max(1, std::min(per_sm, 8));
   // one wave of resident CTAs (or fewer when there is less work)
-  const int64_t nb = (p.N + kRows - 1) / kRows;
+  const int64_t nb = (p.N + R - 1) / R;
   const int64_t ctas_needed = nchunks <= kWarps ? (nb + kWarps / nchunks - 1) / (kWarps / nchunks)
                                                 : (nb * nchunks + kWarps - 1) / kWarps;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)num_sms * per_sm, ctas_needed));
-  cudaError_t e = launch_pdl(k_gemv<MX>, dim3(grid), dim3(kGemvThreads), smem, st, p, nchunks, partial);
+  return launch_pdl(k_gemv<MX, R>, dim3(grid), dim3(kGemvThreads), smem, st, p, nchunks, partial);
+}
+
+template <int MX>
+static cudaError_t launch_mx(const GemvParams &p, int num_sms, cudaStream_t st, float *partial) {
+  const int nchunks = gemv_chunks(p.K);
+  // rows of one chunk: two-row tasks (twice the tasks in flight); longer rows: four
+  cudaError_t e = nchunks == 1 ? launch_mxr<MX, 2>(p, nchunks, num_sms, st, partial)
+                               : launch_mxr<MX, 4>(p, nchunks, num_sms, st, partial);
   if (e != cudaSuccess || nchunks <= kWarps) return e;
   return launch_pdl(k_gemv_reduce, dim3(num_sms), dim3(256), 0, st, p, nchunks, (int)MX, (const float *)partial);
 }
