@@ -35,6 +35,7 @@ constexpr int kGemvChunk = 2048;   // K elements per (row, chunk) unit = 32 lane
 // Doubled E2M1 magnitudes {0,1,2,3,4,6,8,12} as bytes of two words: byte c of
 // (lo, hi) is 2*E2M1(c) for c = 0..7 (a byte-permute lookup table).
 constexpr uint32_t kE2m1x2Lo = 0x03020100u, kE2m1x2Hi = 0x0C080604u;
+constexpr int kMagic = 0x4B400000;   // fp32 bits of 1.5 * 2^23
 
 // Byte permute with the selector's high bit per byte honoured: a selector
 // nibble of 8..15 yields the sign of the selected byte replicated (0 for the
@@ -48,13 +49,9 @@ __device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t sel
 // Same block quantizer as the row packing (kept local: tiny X, static scale).
 // Writes the block's 16 values as signed bytes 2*E2M1 (xp, 4 words) and their
 // negations (xn), and the E4M3 scale as fp32.
-__device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g, float t6g,
+__device__ __forceinline__ void quant_x_block(const uint4 (&raw)[2], float g, float t6g,
                                               uint32_t (&xp)[4], uint32_t (&xn)[4], float &sx) {
-  uint32_t w[8];
-  const uint4 a = __ldg(reinterpret_cast<const uint4 *>(src));
-  const uint4 b = __ldg(reinterpret_cast<const uint4 *>(src) + 1);
-  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-  w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
   uint32_t m2 = 0;
 #pragma unroll
   for (int i = 0; i < 8; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
@@ -66,19 +63,26 @@ __device__ __forceinline__ void quant_x_block(const __nv_bfloat16 *src, float g,
   for (int i = 0; i < 4; ++i) xp[i] = xn[i] = 0;
   if (sb == 0) return;
   const float senc = fminf(__frcp_rn(__fmul_rn(sx, g)), 3.402823466e38f);
+  uint32_t cc[8];   // byte i: the codes of elements 2i (low nibble) and 2i + 1
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    // two codes (elements 2i, 2i+1) -> two signed doubled values
-    const uint32_t cc = cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc));
+  for (int i = 0; i < 8; ++i)
+    cc[i] = cvt_e2m1x2(__fmul_rn(bf16lo(w[i]), senc), __fmul_rn(bf16hi(w[i]), senc));
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t c = (cc >> (4 * h)) & 0xF;
-      const uint32_t mag = __byte_perm(kE2m1x2Lo, kE2m1x2Hi, c & 7);   // byte 0
-      const uint32_t v = (c & 8) ? ((0u - (mag & 0xFF)) & 0xFF) : (mag & 0xFF);
-      const uint32_t nv = (0u - v) & 0xFF;
-      const int e = 2 * i + h;             // element index in the block
-      xp[e >> 2] |= v << (8 * (e & 3));
-      xn[e >> 2] |= nv << (8 * (e & 3));
+  for (int hw = 0; hw < 2; ++hw) {
+    // the eight codes of elements 8hw .. 8hw + 7, element k in nibble k
+    const uint32_t c8 = __byte_perm(__byte_perm(cc[4 * hw], cc[4 * hw + 1], 0x0040),
+                                    __byte_perm(cc[4 * hw + 2], cc[4 * hw + 3], 0x0040), 0x5410);
+    const uint32_t c8n = c8 ^ 0x88888888u;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      // doubled magnitudes of the positive codes (mp) and of the negative ones
+      // (mn); per byte one of them is zero, so the byte-wise differences mp - mn
+      // and mn - mp need no borrow between bytes: with the minuend biased by
+      // 0x80 the subtraction stays inside the byte, and the bias is toggled off
+      const uint32_t mp = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, c8 >> (16 * hh));
+      const uint32_t mn = prmt_sx(kE2m1x2Lo, kE2m1x2Hi, c8n >> (16 * hh));
+      xp[2 * hw + hh] = ((mp | 0x80808080u) - mn) ^ 0x80808080u;
+      xn[2 * hw + hh] = ((mn | 0x80808080u) - mp) ^ 0x80808080u;
     }
   }
 }
@@ -152,7 +156,10 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         if (B.n0 + j >= p.N) continue;
-        const float sw = e4m3_to_f32((B.sf[j] >> (8 * bb)) & 0xFF);
+        // the E4M3 scale byte shifted into fp32 bits 20..27 reads as its value
+        // times 2^-120 (a subnormal for exponent 0, still exact); the X scales
+        // carry the 2^120 back, so no conversion instruction is needed
+        const float sw = __uint_as_float(((B.sf[j] >> (8 * bb)) & 0xFFu) << 20);
         // per group of four codes: the doubled magnitudes of the positive
         // codes (negative ones read 0) and of the negative codes (positive
         // ones read 0), each by one table lookup in sign-replicate mode
@@ -167,14 +174,17 @@ __device__ __forceinline__ void gemv_compute(const GemvParams &p, const GemvBatc
         }
 #pragma unroll
         for (int m = 0; m < MX; ++m) {
-          int isum = 0;
+          // two independent chains; the first starts at the bits of 1.5 * 2^23,
+          // so their sum read as fp32 is 1.5 * 2^23 + isum (|isum| <= 2304)
+          int ipos = kMagic, ineg = 0;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            isum = __dp4a((int)mpos[q], (int)pw[m][q], isum);
-            isum = __dp4a((int)mneg[q], (int)nw[m][q], isum);
+            ipos = __dp4a((int)mpos[q], (int)pw[m][q], ipos);
+            ineg = __dp4a((int)mneg[q], (int)nw[m][q], ineg);
           }
+          const float fsum = __fsub_rn(__int_as_float(ipos + ineg), 12582912.0f);   // isum, exact
           // isum/4 (the E2M1 dot) times sx*sw, both exact: one rounding in the fma
-          acc[j][m] = __fmaf_rn(__int2float_rn(isum), __fmul_rn(sw, sx[m]), acc[j][m]);
+          acc[j][m] = __fmaf_rn(fsum, __fmul_rn(sw, sx[m]), acc[j][m]);
         }
       }
     }
@@ -218,8 +228,12 @@ __device__ __forceinline__ GemvPlan gemv_plan(const GemvParams &p, int nchunks) 
   return q;
 }
 
+// resident CTAs per SM the register budget is held to: three for the
+// one-row-of-X two-row tasks, two up to two X rows (at most 128 registers)
+constexpr int gemv_min_ctas(int mx, int r) { return mx == 1 && r == 2 ? 3 : mx <= 2 ? 2 : 1; }
+
 template <int MX, int R>
-__global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int nchunks, float *partial) {
+__global__ void __launch_bounds__(kGemvThreads, gemv_min_ctas(MX, R)) k_gemv(const GemvParams p, int nchunks, float *partial) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ __align__(16) uint8_t smem[];
@@ -229,7 +243,8 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   // consecutive 64-element groups g4, read consecutive 16-byte words:
   //   xs  [m][h][bb][g4] = the 16 values of block 4*g4 + bb as signed bytes
   //                        2*E2M1 (h = 0) and their negations (h = 1)
-  //   sxs [m][bb][g4]    = E4M3 block scale / 4 as fp32 (the values are doubled)
+  //   sxs [m][bb][g4]    = E4M3 block scale * 2^118 as fp32 (1/4: the values are
+  //                        doubled; 2^120: the weight scales' bit placement)
   const int64_t G4 = K / 64;
   uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
@@ -261,17 +276,37 @@ __global__ void __launch_bounds__(kGemvThreads) k_gemv(const GemvParams p, int n
   const float g = *p.g_x;
   const float t6g = __fmul_rn(6.0f, g);
   const int32_t nb32 = (int32_t)nblk;
-  for (int32_t i = threadIdx.x; i < MX * nb32; i += blockDim.x) {
-    const int32_t m = i / nb32;
-    const int32_t bk = i - m * nb32;
-    uint32_t xpv[4], xnv[4];
-    float sx;
-    quant_x_block(p.x + m * p.ldx + (int64_t)bk * 16, g, t6g, xpv, xnv, sx);
-    const int64_t g4 = bk >> 2, bb = bk & 3;
-    uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2));
-    dst[(0 * 4 + bb) * G4 + g4] = make_uint4(xpv[0], xpv[1], xpv[2], xpv[3]);
-    dst[(1 * 4 + bb) * G4 + g4] = make_uint4(xnv[0], xnv[1], xnv[2], xnv[3]);
-    sxs[m * nblk + bb * G4 + g4] = __fmul_rn(sx, 0.25f);   // with the 1/4 of the doubled values (exact)
+  // a thread's X blocks: all loads first, then the arithmetic (one L2
+  // round trip instead of one per block)
+  constexpr int kXDepth = 4;
+  for (int32_t i0 = threadIdx.x; i0 < MX * nb32; i0 += kXDepth * blockDim.x) {
+    uint4 raw[kXDepth][2];
+#pragma unroll
+    for (int r = 0; r < kXDepth; ++r) {
+      const int32_t i = i0 + r * (int32_t)blockDim.x;
+      if (i < MX * nb32) {
+        const int32_t m = i / nb32, bk = i - m * nb32;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + m * p.ldx + (int64_t)bk * 16);
+        raw[r][0] = __ldg(src);
+        raw[r][1] = __ldg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kXDepth; ++r) {
+      const int32_t i = i0 + r * (int32_t)blockDim.x;
+      if (i < MX * nb32) {
+        const int32_t m = i / nb32, bk = i - m * nb32;
+        uint32_t xpv[4], xnv[4];
+        float sx;
+        quant_x_block(raw[r], g, t6g, xpv, xnv, sx);
+        const int64_t g4 = bk >> 2, bb = bk & 3;
+        uint4 *dst = reinterpret_cast<uint4 *>(xs + m * (K / 2));
+        dst[(0 * 4 + bb) * G4 + g4] = make_uint4(xpv[0], xpv[1], xpv[2], xpv[3]);
+        dst[(1 * 4 + bb) * G4 + g4] = make_uint4(xnv[0], xnv[1], xnv[2], xnv[3]);
+        // with the 1/4 of the doubled values and the 2^120 of the weight scales (exact)
+        sxs[m * nblk + bb * G4 + g4] = __fmul_rn(sx, 0x1p118f);
+      }
+    }
   }
   __syncthreads();
 
