@@ -15,10 +15,9 @@
 //     codes and, from the codes with their sign bits flipped, of the negative
 //     codes, each by one byte permute whose sign-replicate mode zeroes the
 //     other sign; two dp4a sum them against +x and -x: a 16-element block dot
-//     product is an exact
-//     integer (4x the E2M1 dot), sx_b*sw_b is exact in fp32 (two 4-bit
-//     significands) and so is their product with the block dot; only the fp32
-//     sum over blocks rounds.
+//     product is an exact integer (4x the E2M1 dot), sx_b*sw_b is exact in
+//     fp32 (two 4-bit significands) and so is their product with the block
+//     dot; only the fp32 sum over blocks rounds.
 // Rows longer than 2048 elements are split into 2048-element chunks; the chunk
 // sums of a row are added in chunk order, inside the CTA for rows of up to
 // 16384 elements and by a second kernel beyond (no atomics, deterministic).
