@@ -1,7 +1,11 @@
 """Host logic of bench.py that needs no GPU: the multi-rank aggregation (two
-gloo ranks on CPU), the whole-job value and the clock-record summary."""
+gloo ranks on CPU), the whole-job value, the clock-record summary and the
+reference arm (the oracle on the host cores)."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -66,3 +70,35 @@ def test_clock_summary_reasons_and_median():
     assert s["reasons"] == ["sw_power_cap"]
     c.lines = ["0, 1500, 2070, 1400, 0x40, Not Active, Active, Not Active, Not Active"]
     assert bench.ClockSampler.summary(c)["reasons"] == ["hw_thermal_slowdown"]
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run_reference(env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--steps", "1", "--warmup", "0"],
+                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run_reference({"RANK": "0", "WORLD_SIZE": "1"})
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] > 0
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"]
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
