@@ -11,6 +11,8 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "../../include/nvfp4.h"
 #include "internal.h"
@@ -1089,6 +1091,24 @@ nvfp4_status run_wgrad(const nvfp4_wgrad_args *a, const WgradPlan &pl, int sms, 
 }  // namespace
 
 namespace nvfp4 {
+cudaError_t ensure_dynamic_smem(const void *func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  thread_local std::vector<std::pair<const void *, size_t>> done[kMaxDevices];
+  for (auto &f : done[dev])
+    if (f.first == func) {
+      if (f.second >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (e == cudaSuccess) f.second = bytes;
+      return e;
+    }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done[dev].emplace_back(func, bytes);
+  return e;
+}
+
 bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
                  uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();

@@ -888,13 +888,7 @@ cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t 
 template <int BN>
 static cudaError_t launch_bn(const GemmParams &p, const GemmMaps &m, int num_sms, cudaStream_t st) {
   using C = GemmCfg<BN>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_gemm_fp4<BN>, C::kSmemBytes); e != cudaSuccess) return e;
   int64_t tiles = (int64_t)p.tiles_n * (p.gtiles ? 0 : p.tiles_m) * std::max(1, p.ksplit);
   int grid = num_sms;
 #ifdef NVFP4_WAIT_STATS
@@ -918,12 +912,7 @@ cudaError_t launch_lora_down(const LoraDownParams &p, const LoraDownMaps &m, int
                              cudaStream_t st) {
   const int stages = lora_stages_for(p.rank);
   const int smem = lora_smem_bytes(p.rank, stages);
-  static int configured_bytes = 0;
-  if (configured_bytes < smem) {
-    cudaError_t e = cudaFuncSetAttribute(k_lora_down, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured_bytes = smem;
-  }
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_lora_down, smem); e != cudaSuccess) return e;
   int grid = num_sms;
   if (!p.gtiles) grid = std::min(p.tiles_m * std::max(1, p.ksplit), num_sms);
   if (grid <= 0) return cudaSuccess;

@@ -387,12 +387,7 @@ size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 template <int MX, int R>
 static cudaError_t launch_mxr(const GemvParams &p, int nchunks, int num_sms, cudaStream_t st, float *partial) {
   const size_t smem = gemv_smem_bytes(MX, p.K);
-  static size_t configured = 48 * 1024 - sizeof(float) * 2 * kWarps * R * 4;
-  if (smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemv<MX, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
-  }
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_gemv<MX, R>, smem); e != cudaSuccess) return e;
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_gemv<MX, R>, kGemvThreads, smem);
   per_sm = std::max(1, std::min(per_sm, 8));

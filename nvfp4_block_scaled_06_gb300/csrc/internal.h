@@ -186,6 +186,12 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
 // Launch with programmatic stream serialization: the kernel may begin (its
 // setup) while the previous kernel in the stream drains; every kernel launched
 // this way calls griddep_wait() before touching global memory.
+// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute is per device; each host thread remembers
+// what it has set per device and function (setting it again from another
+// thread is harmless), so concurrent callers and several devices are safe.
+cudaError_t ensure_dynamic_smem(const void *func, size_t bytes);
+
 template <class... KArgs, class... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t st, Args &&...args) {

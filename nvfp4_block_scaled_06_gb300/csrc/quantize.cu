@@ -861,13 +861,7 @@ cudaError_t launch_amax(const QuantParams &p, cudaStream_t st) {
 
 static cudaError_t launch_quant_rows_staged(const QuantParams &p, int num_sms, cudaStream_t st) {
   const StagedCfg c = staged_cfg(p.cols);
-  static size_t configured = 48 * 1024;
-  if (c.smem > configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_quant_rows_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)c.smem);
-    if (e != cudaSuccess) return e;
-    configured = c.smem;
-  }
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_quant_rows_staged, c.smem); e != cudaSuccess) return e;
   const int64_t rows_out =
       (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
   const int64_t units = rows_out * c.nseg * p.batch;
@@ -905,12 +899,7 @@ cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t s
   const uint32_t box[3] = {kTC, kTR, 1};
   if (!make_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.src, dims, strides, box))
     return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k_quant_tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * kTileBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_quant_tiles, 2 * kTileBytes); e != cudaSuccess) return e;
   const int64_t tiles = ((p.rows + kTR - 1) / kTR) * ((p.cols + kTC - 1) / kTC);
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 2 * kTileBytes);

@@ -172,12 +172,7 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
   e = launch_pdl(k_route_scan, dim3(1), dim3(1024), 0, st, p);
   if (e != cudaSuccess) return e;
   const size_t sm = (size_t)p.num_experts * sizeof(int32_t) + (size_t)32 * p.num_experts * sizeof(uint16_t);
-  static size_t configured = 48 * 1024;
-  if (sm > configured) {
-    e = cudaFuncSetAttribute(k_route_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    if (e != cudaSuccess) return e;
-    configured = sm;
-  }
+  if ((e = ensure_dynamic_smem((const void *)k_route_scatter, sm)) != cudaSuccess) return e;
   return launch_pdl(k_route_scatter, dim3(p.nchunks), dim3(kRouteChunk), sm, st, p);
 }
 
