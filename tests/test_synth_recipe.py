@@ -71,3 +71,28 @@ def test_grouped_case_routing_shape():
     ex = c["expert_ids"]
     assert ex.shape == (256, c["topk"]) and ex.dtype == np.int32
     assert ex.min() >= 0 and ex.max() < 16
+
+
+# ---- the device-side generators of the benchmark inputs (run here on the CPU)
+
+def test_torch_case_same_recipe_on_cpu():
+    import torch
+    from synth import torch_case
+    a = torch_case("prefill", seed=3, device="cpu", M=256, N=256, K=1024)
+    b = torch_case("prefill", seed=3, device="cpu", M=256, N=256, K=1024)
+    for k, sigma in (("x", 1.0), ("w", 0.02), ("lora_a", 0.01), ("lora_b", 0.01)):
+        assert torch.equal(a[k], b[k]), k
+        assert a[k].dtype == torch.bfloat16
+        v = a[k].double()
+        assert abs(v.std().item() / sigma - 1.0) < 0.03, (k, v.std().item())
+    q = torch_case("quantize", seed=0, device="cpu", E=2, N=64)
+    w = q["w"].float().reshape(-1, q["K"])
+    assert bool((w.abs().amax(dim=1) > 0.2).all())
+    g = torch_case("grouped", seed=0, device="cpu", T=2048, E=64, N=128, K=256, rank=32)
+    ex = g["expert_ids"]
+    assert ex.dtype == torch.int32 and ex.shape == (2048, 8)
+    assert all(len(set(r.tolist())) == 8 for r in ex)
+    load = torch.bincount(ex.reshape(-1).long(), minlength=64)
+    assert load.max().item() > 3 * load.float().mean().item()
+    m = torch_case("moe_down", seed=0, device="cpu", T=256, E=16, N=128, K=256, rank=32)
+    assert torch.allclose(m["route_weights"].sum(dim=1), torch.ones(256), atol=1e-6)
