@@ -36,15 +36,20 @@ struct QuantParams {
   int rank;
   float lora_scale;
   const float *g_b;
-  // in-kernel waits (the staged packing kernel): budget and status word
+  // in-kernel waits (the staged and tiled packing kernels): budget and status word
   int *status;
   uint64_t timeout_ns;
+  int stall_probe;                    // test hook: first wait on a barrier nothing arrives at
 };
 
 int amax_parts_for(int64_t rows);
-// The quantize path with caller-supplied amax scratch of `words` 32-bit words.
+// The quantize path with caller-supplied amax scratch of `words` 32-bit words
+// and the device status word its bounded waits write.
 nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scratch, size_t words,
-                                        cudaStream_t st);
+                                        int *status, cudaStream_t st);
+// Device address (current device) of the status word of the workspace-free
+// quantize entry point.
+nvfp4_status noalloc_status_word(int **out);
 cudaError_t launch_amax(const QuantParams &p, cudaStream_t st);
 cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st);
@@ -183,15 +188,17 @@ bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint6
                  uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner,
                  uint32_t box_rows, CUtensorMapSwizzle sw);
 
+// Raises `func`'s dynamic shared-memory limit on the current device to at
+// least `bytes`.  The attribute is one value per device and function for the
+// whole process, so the library keeps one record of it per device and
+// function under a lock and only ever raises it (to the largest size asked
+// for so far): a smaller request from any thread never lowers a limit that a
+// concurrent larger launch relies on.
+cudaError_t ensure_dynamic_smem(const void *func, size_t bytes);
+
 // Launch with programmatic stream serialization: the kernel may begin (its
 // setup) while the previous kernel in the stream drains; every kernel launched
 // this way calls griddep_wait() before touching global memory.
-// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the
-// current device.  The attribute is per device; each host thread remembers
-// what it has set per device and function (setting it again from another
-// thread is harmless), so concurrent callers and several devices are safe.
-cudaError_t ensure_dynamic_smem(const void *func, size_t bytes);
-
 template <class... KArgs, class... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t st, Args &&...args) {
