@@ -123,18 +123,22 @@ size_t nvfp4_quantize_workspace_bytes(const nvfp4_quant_args *args);
  * layout with no slot for per-call scratch.
  *
  * Same arguments, results and requirements as nvfp4_quantize, except that
- * `workspace` and `workspace_bytes` are ignored and nothing is allocated: the
- * scratch the dynamic global scale needs (one 32-bit word per (matrix, part),
- * min(rows, 512) parts per matrix) lives in a 64 KiB array inside the library
- * (16384 words), present on every GPU that loads the library until the
- * process exits.  Returns NVFP4_ERR_WORKSPACE, before any device work, when
- * batch * min(rows, 512) exceeds 16384 (static global scales need none).
+ * `workspace` and `workspace_bytes` are ignored (never read or written) and
+ * nothing is allocated: the scratch the dynamic global scale needs (one 32-bit
+ * word per (matrix, part), min(rows, 512) parts per matrix) lives in a 64 KiB
+ * array inside the library (16384 words), present on every GPU that loads the
+ * library until the process exits.  Returns NVFP4_ERR_WORKSPACE, before any
+ * device work, when batch * min(rows, 512) exceeds 16384 (static global scales
+ * need none).  The same array holds this entry point's own device status word
+ * (in place of the workspace's first word): an expired in-kernel wait records
+ * NVFP4_ERR_TIMEOUT there, and nvfp4_read_device_status(NULL, stream) reads
+ * and clears it for the current device.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  All calls
  * on a device share the array and it keeps the last call's contents (every
- * word a call reads is first written by that call, so nothing needs
- * clearing); calls that overlap on the GPU (different streams, no ordering)
- * race on it.
+ * amax word a call reads is first written by that call, and the status word
+ * is cleared only by reading it); calls that overlap on the GPU (different
+ * streams, no ordering) race on it.
  * ------------------------------------------------------------------------ */
 nvfp4_status nvfp4_quantize_noalloc(const nvfp4_quant_args *args, nvfp4_stream stream);
 
@@ -411,13 +415,16 @@ const char *nvfp4_status_string(nvfp4_status s);
  * Library diagnostics only: the pages have no counterpart. */
 const char *nvfp4_last_cuda_error(void);
 /* Synchronizes `stream`, reads (and clears) the device status word at the
- * start of `workspace` and returns it (NVFP4_OK when no wait expired). */
+ * start of `workspace` and returns it (NVFP4_OK when no wait expired).
+ * workspace = NULL reads the status word of nvfp4_quantize_noalloc on the
+ * current device instead. */
 nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream);
 /* Bound, in nanoseconds, of every in-kernel wait launched afterwards by this
  * process (default 2e9).  Returns the previous value.  0 is a test hook: each
- * GEMM kernel launched afterwards first waits on a barrier that nothing
- * arrives at, so its expiry path (status word NVFP4_ERR_TIMEOUT, drain of its
- * own copies and MMAs, TMEM freed, early return) runs without any hang. */
+ * GEMM kernel, and each packing kernel of nvfp4_quantize(_noalloc), launched
+ * afterwards first waits on a barrier that nothing arrives at, so its expiry
+ * path (status word NVFP4_ERR_TIMEOUT, drain of its own copies and MMAs, TMEM
+ * freed, early return) runs without any hang. */
 uint64_t nvfp4_set_wait_timeout_ns(uint64_t ns);
 /* Library version, e.g. 0x000100 for 0.1.0. */
 int32_t nvfp4_version(void);

@@ -56,7 +56,9 @@ def set_wait_timeout_ns(ns: int) -> int:
     return int(load().nvfp4_set_wait_timeout_ns(int(ns)))
 
 
-def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+def read_device_status(workspace, stream=None) -> int:
+    """Status word of a workspace (synchronizes the stream, clears the word);
+    workspace=None reads the workspace-free quantize call's own status word."""
     return int(load().nvfp4_read_device_status(_p(workspace), _stream(stream)))
 
 

@@ -146,7 +146,9 @@ nvfp4_status validate_quantize(const nvfp4_quant_args *a) {
   return NVFP4_OK;
 }
 
-nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int sms, cudaStream_t st) {
+// `status`: the device status word that the packing kernels' bounded waits
+// write (the workspace's first word, or the workspace-free entry point's own).
+nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int *status, int sms, cudaStream_t st) {
   QuantParams p{};
   p.src = static_cast<const __nv_bfloat16 *>(a->src);
   p.rows = a->rows;
@@ -173,8 +175,9 @@ nvfp4_status run_quantize(const nvfp4_quant_args *a, const QuantPlan &pl, int sm
     p.sf_col_bstride = (int64_t)nvfp4_sf_bytes(a->cols, a->rows, a->sf_layout);
   }
   p.dst_rows = a->rows;
-  p.status = static_cast<int *>(a->workspace);
+  p.status = status;
   p.timeout_ns = g_timeout_ns.load();
+  p.stall_probe = p.timeout_ns == 0;
   if (!a->global_scale_in) {
     cudaError_t e = launch_amax(p, st);
     if (e != cudaSuccess) return cuda_status(e);
@@ -1079,9 +1082,9 @@ nvfp4_status run_wgrad(const nvfp4_wgrad_args *a, const WgradPlan &pl, int sms, 
   nvfp4_status s;
   QuantPlan qp;
   plan_quantize(&qd, &qp);
-  if ((s = run_quantize(&qd, qp, sms, st)) != NVFP4_OK) return s;
+  if ((s = run_quantize(&qd, qp, static_cast<int *>(qd.workspace), sms, st)) != NVFP4_OK) return s;
   plan_quantize(&qx, &qp);
-  if ((s = run_quantize(&qx, qp, sms, st)) != NVFP4_OK) return s;
+  if ((s = run_quantize(&qx, qp, static_cast<int *>(qx.workspace), sms, st)) != NVFP4_OK) return s;
   const nvfp4_gemm_args g = wgrad_gemm(a, pl);
   GemmPlan gp;
   plan_gemm(&g, &gp);
@@ -1096,7 +1099,12 @@ cudaError_t ensure_dynamic_smem(const void *func, size_t bytes) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  thread_local std::vector<std::pair<const void *, size_t>> done[kMaxDevices];
+  // one record per (device, function) for the whole process; the lock is held
+  // across the attribute call so that two threads never race a smaller value
+  // past a larger one
+  static std::mutex mu;
+  static std::vector<std::pair<const void *, size_t>> done[kMaxDevices];
+  std::lock_guard<std::mutex> lk(mu);
   for (auto &f : done[dev])
     if (f.first == func) {
       if (f.second >= bytes) return cudaSuccess;
@@ -1138,7 +1146,7 @@ namespace nvfp4 {
 // nvfp4_quantize with the amax scratch supplied by the caller of this function
 // (the workspace-free entry point); `words` is the scratch capacity.
 nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scratch, size_t words,
-                                        cudaStream_t st) {
+                                        int *status, cudaStream_t st) {
   nvfp4_status s = validate_quantize(a);
   if (s != NVFP4_OK) return s;
   DevInfo d;
@@ -1149,7 +1157,7 @@ nvfp4_status quantize_with_amax_scratch(const nvfp4_quant_args *a, uint32_t *scr
     if ((size_t)a->batch * (size_t)pl.nparts > words) return NVFP4_ERR_WORKSPACE;
     pl.amax = scratch;
   }
-  return run_quantize(a, pl, d.sms, st);
+  return run_quantize(a, pl, status, d.sms, st);
 }
 }  // namespace nvfp4
 
@@ -1188,7 +1196,12 @@ int32_t nvfp4_version(void) { return 0x000100; }
 uint64_t nvfp4_set_wait_timeout_ns(uint64_t ns) { return g_timeout_ns.exchange(ns); }
 
 nvfp4_status nvfp4_read_device_status(void *workspace, nvfp4_stream stream) {
-  if (!workspace) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace) {
+    // the status word of nvfp4_quantize_noalloc on the current device
+    int *w = nullptr;
+    if (nvfp4_status s = noalloc_status_word(&w); s != NVFP4_OK) return s;
+    workspace = w;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int v = 0;
   if (cudaError_t e_ = cudaStreamSynchronize(st); e_ != cudaSuccess) return cuda_status(e_);
@@ -1216,7 +1229,7 @@ nvfp4_status nvfp4_quantize(const nvfp4_quant_args *a, nvfp4_stream stream) {
   QuantPlan pl;
   plan_quantize(a, &pl);
   if ((s = check_workspace(a->workspace, a->workspace_bytes, pl.ws)) != NVFP4_OK) return s;
-  return run_quantize(a, pl, d.sms, reinterpret_cast<cudaStream_t>(stream));
+  return run_quantize(a, pl, static_cast<int *>(a->workspace), d.sms, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t nvfp4_gemm_workspace_bytes(const nvfp4_gemm_args *a) {

@@ -386,6 +386,12 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
   __syncwarp();
   griddep_launch_dependents();
   griddep_wait();   // inputs of this kernel come from the previous one in the stream
+  if (p.stall_probe) {
+    // test hook: wait on a slot barrier before any copy is armed, so the wait
+    // expires and the expiry path (status word, early return) runs
+    if (lane == 0 && !mbar_wait(&full[0], 0, p.timeout_ns)) record_timeout(p.status);
+    return;
+  }
 
   int64_t rows_out = (p.sf_swizzled && !p.row_map) ? ((p.dst_rows + 127) & ~int64_t(127)) : p.dst_rows;
   // a layout whose used size is known only on the device: split the rows in
@@ -587,16 +593,23 @@ __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const 
   __shared__ uint32_t scratch[32];
   __shared__ float senc_tab[128];
   __shared__ __align__(8) uint64_t full[2];
+  __shared__ __align__(8) uint64_t never;   // test hook: a barrier nothing arrives at
   const int b = blockIdx.y;
   const int t = threadIdx.x;
   if (t == 0) {
     mbar_init(&full[0], 1);
     mbar_init(&full[1], 1);
+    mbar_init(&never, 1);
     fence_barrier_init();
   }
   const float g = resolve_global_scale(p, b, scratch);
   if (blockIdx.x == 0 && t == 0 && p.g_out) p.g_out[b] = g;
   const BlockScale s = make_block_scale(g, senc_tab);   // synchronizes (barrier init visible)
+  if (p.stall_probe) {
+    // test hook: the expiry path (status word, early return) before any copy is issued
+    if (t == 0 && !mbar_wait(&never, 0, p.timeout_ns)) record_timeout(p.status);
+    return;
+  }
 
   const int32_t rows = (int32_t)p.rows, cols = (int32_t)p.cols;
   const int32_t tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
