@@ -136,21 +136,28 @@ def test_decode_chunked_rows(M, N, K):
 
 @pytest.mark.parametrize("name", ["decode_q_b_proj", "decode_o_proj"])
 def test_decode_full_weights_sampled(name):
-    c = make_case(name, M=1)
+    """The decode projections at their real shapes and M = 1, 8, 32: the GEMV
+    for M = 1, the tcgen05 GEMM with X quantized in the call for M = 8 and 32
+    (for o_proj, K = 16384, with the K ranges summed by the split-K pass)."""
+    c = make_case(name, M=32)
     N, K = c["N"], c["K"]
     static = np.float32(16.0 / 2688.0)
     wc, ws, wg = quant_dev(c["w"])
     gx = torch.tensor([float(static)], dtype=torch.float32, device="cuda")
-    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx,
-                      out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    cols = np.random.default_rng(2).choice(N, 256, replace=False)
-    xq = o.quantize(c["x"], static)
+    cols = np.unique(np.concatenate([[0, 127, 128, 255, 256, N - 1],
+                                     np.random.default_rng(2).choice(N, 250, replace=False)]))
     # the sampled rows of W, quantized with the whole tensor's global scale
     wq = o.quantize(c["w"][cols], o.global_scale(c["w"]))
-    y_or = o.linear_fp64(xq, wq)
-    S = o.error_scale(xq, wq)
-    assert_gemm_close(y[:, torch.from_numpy(cols).cuda()], y_or, S, what=name)
+    for M in (1, 8, 32):
+        x = np.ascontiguousarray(c["x"][:M])
+        for od in (torch.float32, torch.bfloat16):
+            y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(x), a_global_scale=gx,
+                              out_dtype=od)
+            torch.cuda.synchronize()
+            xq = o.quantize(x, static)
+            y_or = o.linear_fp64(xq, wq)
+            S = o.error_scale(xq, wq)
+            assert_gemm_close(y[:, torch.from_numpy(cols).cuda()], y_or, S, what=f"{name} M{M} {od}")
 
 
 @pytest.mark.parametrize("ydtype", [torch.bfloat16, torch.float32])
