@@ -215,8 +215,14 @@ struct GemmPlan {
   float *t32 = nullptr;         // T [lsplit][M][rank] fp32 (dynamic X with LoRA: amax in the same pass)
   int lsplit = 1;
   int bn = 256, ksplit = 1;
+  bool pair = false;            // dense product on CTA pairs (256 x 256 tiles)
   float *partial = nullptr;     // split-K partials [ksplit][M][N]
 };
+
+// The pair kernel serves every dense product with at least one full 256-row
+// pair tile and no K split (the small-M decode products keep the 1-SM kernel,
+// whose 128-row tiles waste less).
+bool use_pair(int64_t M, int ksplit) { return M >= 256 && ksplit == 1; }
 
 // K is split when the output has too few tiles to occupy the SMs (small-M
 // decode); the caller's SM count is taken from the device at plan time.
@@ -269,6 +275,7 @@ nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
   const int sms = plan_sms();
   pl->bn = pick_bn(a->M, a->N, sms);
   pl->ksplit = pick_ksplit(a->M, a->N, a->K, pl->bn, sms, a->lora_a != nullptr);
+  pl->pair = use_pair(a->M, pl->ksplit);
   if (pl->ksplit > 1) pl->partial = c.take<float>((size_t)pl->ksplit * a->M * a->N * 4);
   pl->ws = c.off;
   return NVFP4_OK;
@@ -331,6 +338,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   const float *g_a = a->a_global_scale;
   const void *xb = a->lora_x ? a->lora_x : a->a_bf16;
   const int bn = pl.bn;
+  const int b_box = pl.pair ? 128 : bn;   // a CTA of a pair loads half of the 256-row B tile
   GemmMaps maps;
   int lora_steps = 0;
   LoraDownMaps lm;
@@ -339,7 +347,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     if (!map2d(&lm.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xb, a->K, a->M, a->lda * 2, 64, 128) ||
         !map2d(&lm.a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_a, a->K, a->rank, a->K * 2, 64, a->rank) ||
         !map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pl.t, a->rank, a->M, a->rank * 2, 64, 128) ||
-        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, bn))
+        !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N, a->rank * 2, 64, b_box))
       return NVFP4_ERR_CUDA;
     lp.M = a->M;
     lp.K = a->K;
@@ -397,7 +405,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
   }
   if (!map2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, a->K / 2, a->M, a->K / 2, 128, 128) ||
-      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, bn))
+      !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, b_box))
     return NVFP4_ERR_CUDA;
   if (!a->lora_a) {
     maps.t = maps.a;
@@ -427,8 +435,9 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
+  if (pl.pair) p.tiles_n = (int)ceil_div(a->N, 256);
   if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
-  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  cudaError_t e = pl.pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess && pl.ksplit > 1) e = launch_splitk_reduce(p, sms, st);
   if (e == cudaSuccess) e = mark(a->prof_end, st);
   return cuda_status(e);
@@ -871,9 +880,10 @@ nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, i
                            void *prof_end, int sms, cudaStream_t st) {
   const uint64_t tmo = g_timeout_ns.load();
   const int bn = pick_bn(M, Nout, sms);
+  const bool pair = use_pair(M, 1);
   GemmMaps maps;
   if (!map2d(&maps.t, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, Kc, M, lda * 2, 64, 128) ||
-      !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, Kc, Nout, ldb * 2, 64, bn))
+      !map2d(&maps.lb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, Kc, Nout, ldb * 2, 64, pair ? 128 : bn))
     return NVFP4_ERR_CUDA;
   maps.a = maps.t;
   maps.b = maps.lb;
@@ -888,13 +898,13 @@ nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, i
   p.out_fp32 = out_fp32;
   p.lora_steps = (int)ceil_div(Kc, 64);
   p.tiles_m = (int)ceil_div(M, 128);
-  p.tiles_n = (int)ceil_div(Nout, bn);
+  p.tiles_n = (int)ceil_div(Nout, pair ? 256 : bn);
   p.ksplit = 1;
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
   if (cudaError_t e_ = mark(prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
-  cudaError_t e = launch_gemm_fp4(p, maps, bn, sms, st);
+  cudaError_t e = pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess) e = mark(prof_end, st);
   return cuda_status(e);
 }

@@ -103,6 +103,10 @@ struct GemmMaps {
 
 cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, int num_sms,
                             cudaStream_t st);
+// The dense product on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2):
+// p.tiles_n = ceil(N / 256); maps.b and maps.lb with 128-row boxes (each CTA
+// loads its half of the B tile); no grouped tiles, split-K or accumulation.
+cudaError_t launch_gemm_fp4_pair(const GemmParams &p, const GemmMaps &maps, int num_sms, cudaStream_t st);
 // Sums split-K partials in order: D = sum_s partial[s] (bf16 or fp32 out).
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st);
 
