@@ -47,10 +47,10 @@ UNIT = "TFLOP/s"
 PREFILL = dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0)
 L2_BYTES = 129 * 1024 * 1024
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
-# DRAM bytes of one k_gemm_fp4<256> launch on the prefill workload, from one ncu
-# capture of the current kernel (36.79 MB read + 4.44 MB written); set to None
-# whenever the kernel changes until it is captured again.
-GEMM_TRAFFIC_BYTES = 41228800
+# DRAM bytes (read + write) of one GEMM launch on the prefill workload, from
+# one ncu capture of the current kernel; None until the current kernel has
+# been captured.
+GEMM_TRAFFIC_BYTES = None
 
 
 def peaks():
@@ -157,6 +157,16 @@ def arm(C, args, pr):
 
 def mean_ms(pairs):
     return sum(a.elapsed_time(b) for a, b in pairs) / max(1, len(pairs))
+
+
+def plain_and_kernel(torch, fn, steps, warmup, prof):
+    """The per-call time with nothing recorded between the calls (an event
+    between two launches ends their programmatic overlap), then the main
+    kernel's launch durations from a second run with the library's event pair
+    around it.  Returns (ms per call, ms per call when instrumented, kernel ms)."""
+    ms = time_loop(torch, fn, steps, warmup, None)
+    ms_prof = time_loop(torch, fn, steps, 0, prof)
+    return ms, ms_prof, mean_ms(prof)
 
 
 def time_loop(torch, fn, steps, warmup, prof=None, queue_ahead=True):
@@ -324,13 +334,14 @@ def run_quantize_sweep(torch, nv, device, steps, warmup, pk):
     def step(i, pr):
         arm(C, call.args, pr)
         call()
-    ms = time_loop(torch, step, steps, warmup, prof)
+    ms, ms_prof, kms = plain_and_kernel(torch, step, steps, warmup, prof)
     elems = E * N * K
     alg = elems * (2 + 2 * 0.5625)             # one bf16 read, two NVFP4 packings written
-    kms = mean_ms(prof)
     del c, out
     return dict(workload="32 x W[2048,6144] bf16 -> row + column NVFP4 packings, swizzled scales, dynamic g",
-                ms=ms, elements_per_s=elems / (ms * 1e-3), gbs=alg / (ms * 1e-3) / 1e9,
+                ms=ms, ms_instrumented=ms_prof, kernel_ms=kms,
+                elements_per_s=elems / (ms * 1e-3), gbs=alg / (ms * 1e-3) / 1e9,
+                frac_call=alg / (ms * 1e-3) / 1e9 / pk["hbm"],
                 kernel_gbs=alg / (kms * 1e-3) / 1e9, algorithmic_bytes=alg,
                 frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
                 note="amax pass + packing pass (2 reads of the 805 MB input); frac uses the packing kernel's time with the algorithmic one-read bytes")
@@ -358,11 +369,11 @@ def run_decode(torch, nv, device, steps, warmup, pk):
                 cl = calls[i % len(calls)]
                 arm(C, cl.args, pr)
                 cl()
-            ms = time_loop(torch, step, steps, warmup, prof)
-            kms = mean_ms(prof)
+            ms, ms_prof, kms = plain_and_kernel(torch, step, steps, warmup, prof)
             alg = wbytes + M * K * 2 + M * N * 2
             res[f"{name[7:]}_M{M}"] = dict(
-                ms=ms, kernel_ms=kms, weight_gbs=wbytes / (ms * 1e-3) / 1e9,
+                ms=ms, ms_instrumented=ms_prof, kernel_ms=kms,
+                weight_gbs=wbytes / (ms * 1e-3) / 1e9, frac_call=alg / (ms * 1e-3) / 1e9 / pk["hbm"],
                 kernel_gbs=alg / (kms * 1e-3) / 1e9, frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
                 path="cuda-core GEMV" if M <= 4 else "tcgen05 GEMM")
         del wqs, c
@@ -387,8 +398,7 @@ def run_grouped(torch, nv, device, steps, warmup, pk):
     def step(i, pr):
         arm(C, call.args, pr)
         call()
-    ms = time_loop(torch, step, steps, warmup, prof)
-    kms = mean_ms(prof)
+    ms, ms_prof, kms = plain_and_kernel(torch, step, steps, warmup, prof)
     counts = torch.bincount(c["expert_ids"].reshape(-1).long(), minlength=E).cpu()
     active = int((counts > 0).sum())
     P = T * topk
@@ -397,8 +407,8 @@ def run_grouped(torch, nv, device, steps, warmup, pk):
     lbytes = active * (c["rank"] * K + N * c["rank"]) * 2
     alg = wbytes + lbytes + T * K * 2 + P * N * 2
     return dict(workload=f"{T} tokens x top-{topk} of {E} experts W_e[{N},{K}] + LoRA r{c['rank']}",
-                ms=ms, tflops=flops / (ms * 1e-3) / 1e12, kernel_ms=kms,
-                kernel_tflops=flops / (kms * 1e-3) / 1e12,
+                ms=ms, ms_instrumented=ms_prof, tflops=flops / (ms * 1e-3) / 1e12, kernel_ms=kms,
+                kernel_tflops=flops / (kms * 1e-3) / 1e12, gbs=alg / (ms * 1e-3) / 1e9,
                 kernel_gbs=alg / (kms * 1e-3) / 1e9, active_experts=active,
                 max_rows=int(counts.max()), hbm_frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
                 tensor_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16"] * FP4_PER_BF16))
@@ -423,10 +433,9 @@ def run_dgrad(torch, nv, device, steps, warmup, pk):
         def step(i, pr, call=call):
             arm(C, call.args, pr)
             call()
-        ms = time_loop(torch, step, steps, warmup, prof)
-        kms = mean_ms(prof)
-        peak = pk["bf16_sustained"] * (1.0 if name == "dequant_bf16" else FP4_PER_BF16)
-        out[name] = dict(ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+        ms, ms_prof, kms = plain_and_kernel(torch, step, steps, warmup, prof)
+        peak = pk["bf16"] * (1.0 if name == "dequant_bf16" else FP4_PER_BF16)
+        out[name] = dict(ms=ms, ms_instrumented=ms_prof, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
                          gemm_tflops=flops / (kms * 1e-3) / 1e12,
                          gemm_frac=flops / (kms * 1e-3) / 1e12 / peak,
                          pre_ms=ms - kms)
@@ -438,16 +447,15 @@ def run_dgrad(torch, nv, device, steps, warmup, pk):
     def wstep(i, pr):
         arm(C, call.args, pr)
         call()
-    ms = time_loop(torch, wstep, steps, warmup, prof)
-    kms = mean_ms(prof)
-    out["wgrad_fp4"] = dict(ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+    ms, ms_prof, kms = plain_and_kernel(torch, wstep, steps, warmup, prof)
+    out["wgrad_fp4"] = dict(ms=ms, ms_instrumented=ms_prof, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
                             gemm_tflops=flops / (kms * 1e-3) / 1e12,
-                            gemm_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16_sustained"] * FP4_PER_BF16),
+                            gemm_frac=flops / (kms * 1e-3) / 1e12 / (pk["bf16"] * FP4_PER_BF16),
                             pre_ms=ms - kms)
     out["workload"] = (f"dX[{M},{K}] = dY[{M},{N}] W[{N},{K}] and dW[{N},{K}] = dY^T X[{M},{K}] "
                        f"(prefill linear backward), bf16 out")
     out["note"] = ("pre_ms = dequantization (bf16 mode) or the in-call quantizations (fp4 modes); "
-                   "gemm_frac against the sustained bf16 / 6x bf16 peak")
+                   "gemm_frac against the burst bf16 / 6x bf16 peak")
     return out
 
 
@@ -474,63 +482,93 @@ def run_moe_down(torch, nv, device, steps, warmup, pk):
     def step(i, pr):
         arm(C, call.args, pr)
         call()
-    ms = time_loop(torch, step, steps, warmup, prof)
-    kms = mean_ms(prof)
+    ms, ms_prof, kms = plain_and_kernel(torch, step, steps, warmup, prof)
     active = int((counts > 0).sum())
     P = T * k
     flops = 2.0 * P * N * K
     wbytes = active * N * K * 0.5625
     return dict(workload=f"{T} tokens x top-{k}: down-projection of {E} experts W2_e[{N},{K}] + LoRA "
                          f"r{c['rank']} + gate-weighted combine -> y[{T},{N}]",
-                ms=ms, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
+                ms=ms, ms_instrumented=ms_prof, tflops=flops / (ms * 1e-3) / 1e12, gemm_ms=kms,
                 gemm_tflops=flops / (kms * 1e-3) / 1e12,
                 gemm_weight_gbs=wbytes / (kms * 1e-3) / 1e9, active_experts=active)
 
 
 # ----------------------------------------------------------- CPU baseline --
-def cpu_baseline(rows: int = 8192):
-    """The oracle on the headline workload (all 8192 rows by default) on the
-    host cores.  The oracle is numpy: its elementwise steps run on one
-    thread, its fp64 matmul on the BLAS threads; `cores` is the CPU time the
-    process used divided by the wall time (the average number of busy cores)."""
-    import numpy as np
-    from oracle import nvfp4_oracle as o
-    from synth import make_case
-    c = make_case("prefill", M=rows)
+CPU_ROWS = 256          # rows of X per oracle step (both CPU legs)
+
+
+class OracleStep:
+    """The oracle on the headline workload, as the GPU arm runs it: W is
+    quantized once outside the timed region; one step quantizes `rows` rows of
+    X (dynamic scale) and forms their W4A4 product + LoRA in fp64.  Both CPU
+    legs (cpu_baseline and --impl reference) time exactly this step, so their
+    rates measure the same work per row."""
+
+    def __init__(self, rows: int = CPU_ROWS):
+        from oracle import nvfp4_oracle as o
+        from synth import make_case
+        self.o = o
+        c = make_case("prefill", M=rows)
+        self.c = c
+        self.rows = rows
+        self.wq = o.quantize(c["w"])
+        self.lora = (c["lora_a"], c["lora_b"], PREFILL["alpha"])
+        self.flops = 2.0 * rows * PREFILL["N"] * PREFILL["K"]
+
+    def __call__(self):
+        xq = self.o.quantize(self.c["x"])
+        return self.o.linear_fp64(xq, self.wq, self.c["x"], self.lora)
+
+
+def timed_oracle_steps(step, n):
+    """Run n oracle steps; return (seconds per step, average busy cores)."""
     c0, t0 = time.process_time(), time.perf_counter()
-    xq = o.quantize(c["x"])
-    wq = o.quantize(c["w"])
-    o.linear_fp64(xq, wq, c["x"], (c["lora_a"], c["lora_b"], 128.0))
+    for _ in range(n):
+        step()
     dt = time.perf_counter() - t0
-    busy = (time.process_time() - c0) / dt
-    flops = 2.0 * rows * PREFILL["N"] * PREFILL["K"]
-    what = "all" if rows == PREFILL["M"] else "a sample of"
-    return dict(value=flops / dt / 1e12, unit=UNIT, cores=round(busy, 1), kind="oracle",
+    return dt / n, (time.process_time() - c0) / dt
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle timed on this host's cores for about `budget_s` seconds of
+    steps (a bounded sample of the headline workload).  The oracle is numpy:
+    its elementwise steps run on one thread, its fp64 matmul on the BLAS
+    threads; `cores` is the CPU time the process used divided by the wall time
+    (the average number of busy cores)."""
+    step = OracleStep()
+    step()                                   # warm-up (and first-touch of W)
+    one, _ = timed_oracle_steps(step, 1)
+    n = max(1, int(budget_s / max(one, 1e-3)))
+    sec, busy = timed_oracle_steps(step, n)
+    return dict(value=step.flops / sec / 1e12, unit=UNIT, cores=round(busy, 1), kind="oracle",
                 host_cores=os.cpu_count(),
-                sample=f"{what} {rows} rows of X through quantize + dequantized fp64 GEMM + LoRA "
-                       f"(W quantized each call, as the oracle stands); {dt:.2f} s, "
-                       f"{busy:.1f} cores busy on average of {os.cpu_count()}",
-                seconds=dt)
+                sample=f"{n} steps of {step.rows} rows of X [of 8192] through quantize + dequantized "
+                       f"fp64 W4A4 product + LoRA, W quantized once outside the timing (as the GPU "
+                       f"arm); {sec * n:.1f} s, {busy:.1f} cores busy on average of {os.cpu_count()}",
+                rows_per_step=step.rows, seconds=sec * n)
 
 
 def reference_arm(args):
-    steps, warm = args.steps, args.warmup
-    rows = 24
-    for _ in range(warm):
-        cpu_baseline(rows)
-    runs = [cpu_baseline(rows) for _ in range(steps)]
-    ts = [r["seconds"] for r in runs]
-    cores = round(sum(r["cores"] for r in runs) / len(runs), 1)
-    ms = 1e3 * sum(ts) / len(ts)
-    flops = 2.0 * rows * PREFILL["N"] * PREFILL["K"]
-    v = flops / (ms * 1e-3) / 1e12
+    """--impl reference: the oracle (there is no reference code: the pages hold
+    none) on the host cores, each step the same bounded sample that
+    cpu_baseline times."""
+    step = OracleStep()
+    for _ in range(args.warmup):
+        step()
+    sec, busy = timed_oracle_steps(step, args.steps)
+    ms = 1e3 * sec
+    v = step.flops / sec / 1e12
     line = dict(impl="reference", metric=METRIC, value=v, unit=UNIT, n_gpus=args.gpus,
-                steps=steps, warmup=warm, ms_per_step=ms, higher_is_better=True,
+                steps=args.steps, warmup=args.warmup, ms_per_step=ms, higher_is_better=True,
                 scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-                config=dict(workload="prefill QLoRA linear, CPU oracle on a 24-row sample",
-                            M_sample=rows, N=PREFILL["N"], K=PREFILL["K"], rank=64),
-                cpu_baseline=dict(value=v, unit=UNIT, cores=cores, kind="oracle",
-                                  sample=f"{rows} rows of X per step"),
+                config=dict(workload="prefill QLoRA linear (X[8192,6144] bf16, NVFP4 W[2048,6144], "
+                                     "LoRA r64), CPU oracle on a row sample per step",
+                            M=PREFILL["M"], M_sample=step.rows, N=PREFILL["N"], K=PREFILL["K"],
+                            rank=64),
+                cpu_baseline=dict(value=v, unit=UNIT, cores=round(busy, 1), kind="oracle",
+                                  sample=f"{step.rows} rows of X per step, W quantized once before "
+                                         f"the timed steps"),
                 e2e=dict(value=v, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line))
 
@@ -595,8 +633,8 @@ def main():
 
     ms = main_res["ms"]
     value = job_value(world, main_res["flops"], ms)
-    # the GEMM is timed inside a long run of steps: the sustained bf16 figure
-    fp4_peak = pk["bf16_sustained"] * FP4_PER_BF16
+    # the GEMM launches are timed over a few ms of steps: the burst bf16 figure
+    fp4_peak = pk["bf16"] * FP4_PER_BF16
     gemm_tflops = main_res["flops"] / (main_res["gemm_ms"] * 1e-3) / 1e12
     e2e = main_res["e2e"]
     line = dict(
@@ -609,13 +647,13 @@ def main():
                     M=PREFILL["M"], N=PREFILL["N"], K=PREFILL["K"], rank=64, alpha=128.0,
                     l2="X rotates over 4 buffers (403 MB > 129 MB L2)",
                     parallelism=f"replicas x{world}"),
-        roofline=dict(bound="tensor", kernel="k_gemm_fp4<256>", achieved=gemm_tflops,
+        roofline=dict(bound="tensor", kernel="k_gemm_fp4_pair", achieved=gemm_tflops,
                       peak=fp4_peak, unit="TFLOP/s", frac=gemm_tflops / fp4_peak,
                       traffic=GEMM_TRAFFIC_BYTES,
                       traffic_note="dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu "
-                                   "capture (profiles/k_gemm_fp4_prefill_M8192_N2048_K6144.md)",
-                      peak_note=f"{pk['source']} bf16 sustained {pk['bf16_sustained']} TFLOP/s x 6 "
-                                f"(nominal fp4:bf16)",
+                                   "capture of this kernel on this workload (M8192 N2048 K6144)",
+                      peak_note=f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x 6 "
+                                f"(nominal fp4:bf16), of {pk['source']}",
                       timing_note="CUDA events around each GEMM launch in a second run of the same "
                                   f"{args.steps} steps ({main_res['ms_prof']:.4f} ms/step with the events)"),
         e2e=dict(value=job_value(world, main_res["flops"], e2e["ms"]), unit=UNIT,
