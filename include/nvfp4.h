@@ -194,16 +194,31 @@ size_t nvfp4_gemm_workspace_bytes(const nvfp4_gemm_args *args);
  *
  * 256 routed experts with 8 per token ("GLM-5.2-NVFP4" card); a LoRA per
  * expert over the FP4 experts ("A model no kernel wanted to serve").
- *   expert_ids: device int32 [num_tokens*top_k], pair p = token*top_k + slot.
+ * Routing, one of:
+ *   expert_ids: device int32 [num_tokens*top_k], pair p = token*top_k + slot
+ *     (grouped on the device: rows of expert e contiguous, ordered by p);
+ *   offsets_in [E+1] + perm_in [num_tokens*top_k] (device int32, expert_ids
+ *     NULL): the grouping already made -- grouped row i holds pair perm_in[i],
+ *     rows offsets_in[e] .. offsets_in[e+1]-1 belong to expert e.  Device data
+ *     the host cannot check: the kernels clamp counts to [0, P] cumulatively
+ *     and treat pair indices outside [0, P) as padding, so inconsistent
+ *     routing gives wrong rows, never an access outside the buffers.
+ * Activations, one of:
  *   x_bf16 [num_tokens][K]: quantized once with one tensor-wide global scale
- *     (x_global_scale static, or NULL = dynamic amax).
+ *     (x_global_scale static, or NULL = dynamic amax);
+ *   x_codes [num_tokens][K/2] + x_sf linear [num_tokens][K/16] (x_bf16 may
+ *     be NULL without LoRA): token rows already quantized with the global
+ *     scale x_global_scale (required) -- scaled_fp4_mm's input of "Kernel
+ *     choice" on the "vroomfondel/glm-5.2-reap-504B-v2-W4A4" card.  The LoRA
+ *     branch still reads the unquantized x_bf16.
  *   Weights of all experts stacked: w_codes [E][N][K/2] and w_sf [E][swizzled
  *     N x K/16], w_global_scale device float[E].
  *   Optional per-expert LoRA: lora_a bf16 [E][rank][K], lora_b bf16 [E][N][rank].
- *   Output d bf16 [num_tokens*top_k][N] in expert-grouped order: rows of
- *   expert e are contiguous, ordered by pair index; perm_out[i] = the pair
- *   index of grouped row i; expert_offsets_out (optional) int32 [E+1].
- * Requirements: N % 256 == 0, K % 32 == 0, E <= 1024, as nvfp4_gemm otherwise.
+ *   Output d [num_tokens*top_k][N], bf16 or fp32 (out_dtype), in the grouped
+ *   order; perm_out[i] = the pair index of grouped row i (required with
+ *   expert_ids, optional with perm_in); expert_offsets_out (optional) [E+1].
+ * Requirements: N % 256 == 0, K % 32 == 0, E <= 1024, as nvfp4_gemm otherwise;
+ *   x_codes, x_sf, offsets_in, perm_in 16-byte aligned.
  * Workspace: nvfp4_grouped_workspace_bytes(&args).
  * ------------------------------------------------------------------------ */
 typedef struct {
@@ -223,6 +238,11 @@ typedef struct {
   size_t workspace_bytes;
   /* Optional cudaEvent_t pair recorded around the grouped GEMM kernel. */
   void *prof_begin, *prof_end;
+  /* Pre-quantized activations (see above); NULL = quantize x_bf16. */
+  const uint8_t *x_codes, *x_sf;
+  /* Precomputed routing (see above); NULL = route expert_ids. */
+  const int32_t *offsets_in, *perm_in;
+  int32_t out_dtype;             /* nvfp4_out_dtype of d (0 = bf16) */
 } nvfp4_grouped_args;
 
 nvfp4_status nvfp4_grouped_gemm(const nvfp4_grouped_args *args, nvfp4_stream stream);

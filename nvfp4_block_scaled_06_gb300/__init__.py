@@ -183,21 +183,40 @@ def nvfp4_gemm(b_codes, b_sf, b_global_scale, N, K, *, a_codes=None, a_sf=None,
 # ------------------------------------------------------------------ grouped --
 
 def prepare_grouped(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N: int, K: int,
-                    num_experts: int, x_global_scale=None, lora=None):
+                    num_experts: int, x_global_scale=None, lora=None, *, x_packed=None,
+                    routing=None, top_k: int | None = None, out_dtype=torch.bfloat16):
+    """Routing: expert_ids [T, k], or routing = (offsets [E+1], perm [T*k]) with
+    top_k.  Activations: x_bf16 [T, K], or x_packed = (codes [T, K/2], linear sf
+    [T, K/16]) with x_global_scale (x_bf16 still needed for a LoRA)."""
     lib = load()
-    dev = x_bf16.device
-    T, topk = expert_ids.shape
+    dev = w_codes.device
+    if expert_ids is not None:
+        T, topk = expert_ids.shape
+    else:
+        if routing is None or top_k is None:
+            raise ValueError("routing=(offsets, perm) and top_k are needed without expert_ids")
+        topk = int(top_k)
+        T = routing[1].numel() // topk
     P = T * topk
-    d = torch.empty((P, N), dtype=torch.bfloat16, device=dev)
-    perm = torch.empty(P, dtype=torch.int32, device=dev)
+    d = torch.empty((P, N), dtype=out_dtype, device=dev)
     offs = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(P, dtype=torch.int32, device=dev) if routing is None else routing[1]
     a = GroupedArgs(num_tokens=T, top_k=topk, num_experts=num_experts, N=N, K=K,
-                    expert_ids=expert_ids.data_ptr(), x_bf16=x_bf16.data_ptr(),
+                    x_bf16=None if x_bf16 is None else x_bf16.data_ptr(),
                     x_global_scale=None if x_global_scale is None else x_global_scale.data_ptr(),
                     w_codes=w_codes.data_ptr(), w_sf=w_sf.data_ptr(),
                     w_global_scale=w_global_scale.data_ptr(), d=d.data_ptr(),
-                    perm_out=perm.data_ptr(), expert_offsets_out=offs.data_ptr())
+                    expert_offsets_out=offs.data_ptr(),
+                    out_dtype=OUT_FP32 if out_dtype == torch.float32 else OUT_BF16)
     keep = [expert_ids, x_bf16, w_codes, w_sf, w_global_scale, x_global_scale, d, perm, offs]
+    if routing is None:
+        a.expert_ids, a.perm_out = expert_ids.data_ptr(), perm.data_ptr()
+    else:
+        a.offsets_in, a.perm_in = routing[0].data_ptr(), routing[1].data_ptr()
+        keep += list(routing)
+    if x_packed is not None:
+        a.x_codes, a.x_sf = x_packed[0].data_ptr(), x_packed[1].data_ptr()
+        keep += list(x_packed)
     if lora is not None:
         a.lora_a, a.lora_b = lora["a"].data_ptr(), lora["b"].data_ptr()
         a.rank, a.alpha = lora["a"].shape[1], float(lora["alpha"])
@@ -211,11 +230,12 @@ def prepare_grouped(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N: int, K
 
 
 def nvfp4_grouped_gemm(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N, K, num_experts,
-                       x_global_scale=None, lora=None, stream=None):
+                       x_global_scale=None, lora=None, stream=None, **forms):
     """Routed-expert W4A4 GEMM.  Returns (d [T*k, N] grouped by expert,
-    perm [T*k] grouped row -> pair index, offsets [E+1])."""
+    perm [T*k] grouped row -> pair index, offsets [E+1]).  `forms` takes
+    prepare_grouped's keyword inputs (x_packed, routing + top_k, out_dtype)."""
     call, res = prepare_grouped(expert_ids, x_bf16, w_codes, w_sf, w_global_scale, N, K,
-                                num_experts, x_global_scale, lora)
+                                num_experts, x_global_scale, lora, **forms)
     call(stream)
     return res
 

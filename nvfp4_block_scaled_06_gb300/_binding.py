@@ -74,6 +74,9 @@ class GroupedArgs(C.Structure):
         ("d", C.c_void_p), ("perm_out", C.c_void_p), ("expert_offsets_out", C.c_void_p),
         ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t),
         ("prof_begin", C.c_void_p), ("prof_end", C.c_void_p),
+        ("x_codes", C.c_void_p), ("x_sf", C.c_void_p),
+        ("offsets_in", C.c_void_p), ("perm_in", C.c_void_p),
+        ("out_dtype", C.c_int32),
     ]
 
 

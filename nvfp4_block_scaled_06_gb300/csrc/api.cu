@@ -448,7 +448,7 @@ struct GroupedPlan {
   size_t ws = 0;
   int nchunks = 0;
   int64_t prow_max = 0;
-  int32_t *hist = nullptr, *counts = nullptr, *offsets = nullptr, *poffsets = nullptr;
+  int32_t *hist = nullptr, *counts = nullptr, *offsets = nullptr, *poffsets = nullptr, *goffsets = nullptr;
   int32_t *row_map = nullptr, *nmt = nullptr;
   GroupTile *gtiles = nullptr;
   uint32_t *amax = nullptr;
@@ -464,31 +464,47 @@ nvfp4_status plan_grouped(const nvfp4_grouped_args *a, GroupedPlan *pl) {
   const int64_t P = a->num_tokens * a->top_k;
   pl->nchunks = (int)ceil_div(P, 1024);
   pl->prow_max = pad_up(P + a->num_experts * 127, 128);
-  pl->hist = c.take<int32_t>((size_t)pl->nchunks * a->num_experts * 4);
-  pl->counts = c.take<int32_t>((size_t)a->num_experts * 4);
-  pl->offsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  if (a->expert_ids) {
+    pl->hist = c.take<int32_t>((size_t)pl->nchunks * a->num_experts * 4);
+    pl->counts = c.take<int32_t>((size_t)a->num_experts * 4);
+    pl->offsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  } else {
+    pl->goffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
+  }
   pl->poffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
   pl->row_map = c.take<int32_t>((size_t)pl->prow_max * 4);
   pl->gtiles = c.take<GroupTile>((size_t)(pl->prow_max / 128) * sizeof(GroupTile));
   pl->nmt = c.take<int32_t>(4);
-  if (!a->x_global_scale) {
-    pl->nparts = amax_parts_for(a->num_tokens);
-    pl->amax = c.take<uint32_t>((size_t)pl->nparts * 4);
+  if (!a->x_codes) {
+    if (!a->x_global_scale) {
+      pl->nparts = amax_parts_for(a->num_tokens);
+      pl->amax = c.take<uint32_t>((size_t)pl->nparts * 4);
+    }
+    pl->g_x = c.take<float>(4);
+    pl->xq_tok = c.take<uint8_t>((size_t)a->num_tokens * a->K / 2);
+    pl->xsf_tok = c.take<uint8_t>((size_t)a->num_tokens * (a->K / 16));
   }
-  pl->g_x = c.take<float>(4);
   pl->xq = c.take<uint8_t>((size_t)pl->prow_max * a->K / 2);
   pl->xsf = c.take<uint8_t>(sf_swizzled_bytes(pl->prow_max, a->K));
-  pl->xq_tok = c.take<uint8_t>((size_t)a->num_tokens * a->K / 2);
-  pl->xsf_tok = c.take<uint8_t>((size_t)a->num_tokens * (a->K / 16));
   if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)pl->prow_max * a->rank * 2);
   pl->ws = c.off;
   return NVFP4_OK;
 }
 
 nvfp4_status validate_grouped(const nvfp4_grouped_args *a) {
-  if (!a || !a->expert_ids || !a->x_bf16 || !a->w_codes || !a->w_sf || !a->w_global_scale || !a->d ||
-      !a->perm_out)
+  if (!a || !a->w_codes || !a->w_sf || !a->w_global_scale || !a->d) return NVFP4_ERR_INVALID_ARG;
+  // routing: expert ids (grouped here, perm_out required) or offsets + perm given
+  const bool ids = a->expert_ids != nullptr, given = a->offsets_in && a->perm_in;
+  if (ids == given || (!given && (a->offsets_in || a->perm_in))) return NVFP4_ERR_INVALID_ARG;
+  if (ids && !a->perm_out) return NVFP4_ERR_INVALID_ARG;
+  // activations: bf16 rows, or packed rows with their global scale
+  if (a->x_codes || a->x_sf) {
+    if (!a->x_codes || !a->x_sf || !a->x_global_scale) return NVFP4_ERR_INVALID_ARG;
+  } else if (!a->x_bf16) {
     return NVFP4_ERR_INVALID_ARG;
+  }
+  if ((a->lora_a || a->lora_b) && !a->x_bf16) return NVFP4_ERR_INVALID_ARG;
+  if (a->out_dtype != NVFP4_OUT_BF16 && a->out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_INVALID_ARG;
   if (a->num_tokens < 1 || a->top_k < 1 || a->num_experts < 1 || a->N < 1 || a->K < 1)
     return NVFP4_ERR_INVALID_ARG;
   if (a->num_experts > 1024 || a->top_k > a->num_experts) return NVFP4_ERR_UNSUPPORTED_SHAPE;
@@ -500,8 +516,9 @@ nvfp4_status validate_grouped(const nvfp4_grouped_args *a) {
     if (a->rank < 32 || a->rank > 256 || a->rank % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (!aligned(a->lora_a, 16) || !aligned(a->lora_b, 16)) return NVFP4_ERR_ALIGNMENT;
   }
-  if (!aligned(a->x_bf16, 16) || !aligned(a->w_codes, 16) || !aligned(a->w_sf, 16) || !aligned(a->d, 16))
-    return NVFP4_ERR_ALIGNMENT;
+  const void *ptrs[] = {a->x_bf16, a->w_codes, a->w_sf, a->d, a->x_codes, a->x_sf, a->offsets_in, a->perm_in};
+  for (const void *q : ptrs)
+    if (q && !aligned(q, 16)) return NVFP4_ERR_ALIGNMENT;
   return NVFP4_OK;
 }
 
@@ -523,7 +540,8 @@ struct GroupedProducts {
   int32_t rank;
   float alpha;
   __nv_bfloat16 *t;               // [prow_max][rank] T' scratch
-  void *d;                        // bf16 [P][N]
+  void *d;                        // [P][N], bf16 or fp32
+  int out_fp32;
   void *prof_begin, *prof_end;
 };
 
@@ -578,7 +596,7 @@ nvfp4_status run_grouped_products(const GroupedProducts &g, int *status, uint64_
   p.g_b = g.w_g;
   p.d = g.d;
   p.ldd = g.N;
-  p.out_fp32 = 0;
+  p.out_fp32 = g.out_fp32;
   p.lora_steps = lora_steps;
   p.tiles_n = (int)(g.N / bn);
   p.gtiles = g.gtiles;
@@ -596,24 +614,72 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   int *status = static_cast<int *>(a->workspace);
   const uint64_t tmo = g_timeout_ns.load();
   const int64_t P = a->num_tokens * a->top_k;
-  RouteParams r{};
-  r.expert_ids = a->expert_ids;
-  r.pairs = P;
-  r.top_k = (int)a->top_k;
-  r.num_experts = (int)a->num_experts;
-  r.chunk = 1024;
-  r.nchunks = pl.nchunks;
-  r.hist = pl.hist;
-  r.counts = pl.counts;
-  r.offsets = pl.offsets;
-  r.poffsets = pl.poffsets;
-  r.perm = a->perm_out;
-  r.row_map = pl.row_map;
-  r.padded_rows_max = pl.prow_max;
-  r.gtiles = pl.gtiles;
-  r.gnum_mtiles = pl.nmt;
-  r.offsets_out = a->expert_offsets_out;
-  if (cudaError_t e_ = launch_route(r, st); e_ != cudaSuccess) return cuda_status(e_);
+  if (a->expert_ids) {
+    RouteParams r{};
+    r.expert_ids = a->expert_ids;
+    r.pairs = P;
+    r.top_k = (int)a->top_k;
+    r.num_experts = (int)a->num_experts;
+    r.chunk = 1024;
+    r.nchunks = pl.nchunks;
+    r.hist = pl.hist;
+    r.counts = pl.counts;
+    r.offsets = pl.offsets;
+    r.poffsets = pl.poffsets;
+    r.perm = a->perm_out;
+    r.row_map = pl.row_map;
+    r.padded_rows_max = pl.prow_max;
+    r.gtiles = pl.gtiles;
+    r.gnum_mtiles = pl.nmt;
+    r.offsets_out = a->expert_offsets_out;
+    if (cudaError_t e_ = launch_route(r, st); e_ != cudaSuccess) return cuda_status(e_);
+  } else {
+    // the caller's grouping: padded layout from its offsets, row_map -> token through its perm
+    if (cudaError_t e_ = launch_layout_from_offsets(a->offsets_in, (int)a->num_experts, P, pl.prow_max, pl.goffsets,
+                                                    pl.poffsets, pl.gtiles, pl.nmt, pl.row_map, a->perm_in,
+                                                    (int)a->top_k, sms, st);
+        e_ != cudaSuccess)
+      return cuda_status(e_);
+    if (a->perm_out && a->perm_out != a->perm_in &&
+        cudaMemcpyAsync(a->perm_out, a->perm_in, (size_t)P * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+    if (a->expert_offsets_out && cudaMemcpyAsync(a->expert_offsets_out, pl.goffsets, (size_t)(a->num_experts + 1) * 4,
+                                                 cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return NVFP4_ERR_CUDA;
+  }
+  if (a->x_codes) {
+    // activations already quantized per token row (linear scales) with x_global_scale
+    if (cudaError_t e_ = launch_gather_packed(a->x_codes, a->x_sf, pl.row_map, pl.prow_max, pl.nmt, a->K, pl.xq,
+                                              pl.xsf, sms, st);
+        e_ != cudaSuccess)
+      return cuda_status(e_);
+    GroupedProducts gp;
+    gp.E = a->num_experts;
+    gp.N = a->N;
+    gp.K = a->K;
+    gp.prow_max = pl.prow_max;
+    gp.aq = pl.xq;
+    gp.asf = pl.xsf;
+    gp.g_a = a->x_global_scale;
+    gp.row_map = pl.row_map;
+    gp.gtiles = pl.gtiles;
+    gp.nmt = pl.nmt;
+    gp.x_src = a->x_bf16;
+    gp.x_rows = a->num_tokens;
+    gp.w_codes = a->w_codes;
+    gp.w_sf = a->w_sf;
+    gp.w_g = a->w_global_scale;
+    gp.lora_a = a->lora_a;
+    gp.lora_b = a->lora_b;
+    gp.rank = a->rank;
+    gp.alpha = a->alpha;
+    gp.t = pl.t;
+    gp.d = a->d;
+    gp.out_fp32 = a->out_dtype == NVFP4_OUT_FP32;
+    gp.prof_begin = a->prof_begin;
+    gp.prof_end = a->prof_end;
+    return run_grouped_products(gp, status, tmo, sms, st);
+  }
 
   QuantParams q{};
   q.src = static_cast<const __nv_bfloat16 *>(a->x_bf16);
@@ -663,6 +729,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   gp.alpha = a->alpha;
   gp.t = pl.t;
   gp.d = a->d;
+  gp.out_fp32 = a->out_dtype == NVFP4_OUT_FP32;
   gp.prof_begin = a->prof_begin;
   gp.prof_end = a->prof_end;
   return run_grouped_products(gp, status, tmo, sms, st);
@@ -672,7 +739,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
 struct MoeDownPlan {
   size_t ws = 0;
   int64_t prow_max = 0;
-  int32_t *poffsets = nullptr, *row_map = nullptr, *nmt = nullptr, *inv = nullptr;
+  int32_t *goffsets = nullptr, *poffsets = nullptr, *row_map = nullptr, *nmt = nullptr, *inv = nullptr;
   GroupTile *gtiles = nullptr;
   uint32_t *amax = nullptr;
   int nparts = 0;
@@ -685,6 +752,7 @@ void plan_moe_down(const nvfp4_moe_down_args *a, MoeDownPlan *pl) {
   Carve c(a->workspace);
   const int64_t P = a->num_tokens * a->top_k;
   pl->prow_max = pad_up(P + a->num_experts * 127, 128);
+  pl->goffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
   pl->poffsets = c.take<int32_t>((size_t)(a->num_experts + 1) * 4);
   pl->row_map = c.take<int32_t>((size_t)pl->prow_max * 4);
   pl->gtiles = c.take<GroupTile>((size_t)(pl->prow_max / 128) * sizeof(GroupTile));
@@ -726,8 +794,9 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   int *status = static_cast<int *>(a->workspace);
   const uint64_t tmo = g_timeout_ns.load();
   const int64_t P = a->num_tokens * a->top_k;
-  if (cudaError_t e_ = launch_layout_from_offsets(a->expert_offsets, (int)a->num_experts, pl.prow_max,
-                                                  pl.poffsets, pl.gtiles, pl.nmt, pl.row_map, sms, st);
+  if (cudaError_t e_ = launch_layout_from_offsets(a->expert_offsets, (int)a->num_experts, P, pl.prow_max,
+                                                  pl.goffsets, pl.poffsets, pl.gtiles, pl.nmt, pl.row_map,
+                                                  nullptr, 0, sms, st);
       e_ != cudaSuccess)
     return cuda_status(e_);
   // h is quantized once (one tensor-wide g) straight into the padded layout:
@@ -776,6 +845,7 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   gp.alpha = a->alpha;
   gp.t = pl.t;
   gp.d = pl.d;
+  gp.out_fp32 = 0;
   gp.prof_begin = a->prof_begin;
   gp.prof_end = a->prof_end;
   nvfp4_status s = run_grouped_products(gp, status, tmo, sms, st);

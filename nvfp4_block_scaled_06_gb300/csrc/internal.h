@@ -176,11 +176,13 @@ struct RouteParams {
   int32_t *offsets_out;       // optional copy of offsets for the caller
 };
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
-// Padded grouped layout (poffsets, m-tiles, row_map -> grouped row) of rows
+// Padded grouped layout (goffsets = the clamped offsets rebuilt, poffsets,
+// m-tiles, row_map -> grouped row, or -> token through perm / top_k) of rows
 // that arrive already grouped with the given expert offsets.
-cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t padded_rows_max,
-                                       int32_t *poffsets, GroupTile *gtiles, int32_t *gnum_mtiles,
-                                       int32_t *row_map, int num_sms, cudaStream_t st);
+cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pairs, int64_t padded_rows_max,
+                                       int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
+                                       int32_t *gnum_mtiles, int32_t *row_map, const int32_t *perm, int top_k,
+                                       int num_sms, cudaStream_t st);
 // y[t] = sum_j w[t][j] d[inverse perm (t*top_k + j)] (bf16 rows, fp32 sums).
 cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int32_t *inv, const float *w,
                                int64_t tokens, int top_k, int64_t N, __nv_bfloat16 *y, int num_sms,

@@ -60,6 +60,36 @@ __device__ __forceinline__ int32_t block_exclusive_scan(int32_t v, int32_t *scra
   return before + x - v;
 }
 
+// The same scan with every partial sum capped at `cap` (inputs in [0, cap]):
+// min(a + b, cap) is associative on such values, so the result is the exact
+// prefix sum clamped to cap, and nothing overflows.
+__device__ __forceinline__ int32_t block_exclusive_scan_capped(int32_t v, int32_t cap, int32_t *scratch) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = min(x, cap - y) + y;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int32_t s = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s = min(s, cap - y) + y;
+    }
+    scratch[32 + lane] = s;
+  }
+  const int32_t prev = __shfl_up_sync(0xffffffffu, x, 1);
+  const int32_t in_warp = lane > 0 ? prev : 0;   // capped exclusive prefix within the warp
+  __syncthreads();
+  const int32_t before = w > 0 ? scratch[32 + w - 1] : 0;
+  return min(in_warp, cap - before) + before;
+}
+
 __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
@@ -178,43 +208,56 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
 
 // ------------------------------------------- layout from given expert offsets --
 // The grouped operand's padded layout when the rows already arrive grouped
-// (the down-projection input, in the order of the up-projection's output):
-// per expert e, rows offsets[e] .. offsets[e+1]-1 keep their order and start
-// at the 128-aligned padded offset.
-__global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restrict__ offsets, int E,
-                                                         int32_t *poffsets, GroupTile *gtiles,
+// (the down-projection input, in the order of the up-projection's output, or
+// a caller's precomputed routing): per expert e, its rows keep their order
+// and start at the 128-aligned padded offset.  The offsets are the caller's
+// device data, so the counts are clamped to [0, pairs] cumulatively and the
+// layout is rebuilt from the clamped counts (goffsets): consistent offsets
+// give back the same offsets, inconsistent ones can never index past the
+// grouped rows or the padded bound.
+__global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restrict__ offsets, int E, int64_t pairs,
+                                                         int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
                                                          int32_t *gnum_mtiles) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ int32_t scratch[64];
   const int e = threadIdx.x;
   const bool act = e < E;
-  const int32_t count = act ? offsets[e + 1] - offsets[e] : 0;
+  const int64_t diff = act ? (int64_t)offsets[e + 1] - (int64_t)offsets[e] : 0;
+  int32_t count = (int32_t)(diff < 0 ? 0 : diff > pairs ? pairs : diff);
+  const int32_t before = block_exclusive_scan_capped(count, (int32_t)pairs, scratch);
+  count = min(count, (int32_t)pairs - before);
   const int32_t padded = (count + 127) & ~127;
   const int32_t mt = padded / 128;
-  int32_t ptotal, mtotal;
+  int32_t ctotal, ptotal, mtotal;
+  const int32_t off = block_exclusive_scan(count, scratch, ctotal);
   const int32_t poff = block_exclusive_scan(padded, scratch, ptotal);
   const int32_t moff = block_exclusive_scan(mt, scratch, mtotal);
   if (act) {
+    goffsets[e] = off;
     poffsets[e] = poff;
     for (int j = 0; j < mt; ++j) {
       GroupTile g;
       g.expert = e;
       g.a_row0 = poff + 128 * j;
       g.valid_rows = min(128, count - 128 * j);
-      g.out_row0 = offsets[e] + 128 * j;
+      g.out_row0 = off + 128 * j;
       gtiles[moff + j] = g;
     }
   }
   if (threadIdx.x == 0) {
+    goffsets[E] = ctotal;
     poffsets[E] = ptotal;
     *gnum_mtiles = mtotal;
   }
 }
 
-// row_map[r] = the grouped row that padded row r holds, or -1 (padding).
-__global__ void k_rowmap_from_offsets(const int32_t *__restrict__ offsets,
+// row_map[r] = the grouped row that padded row r holds, or -1 (padding); with
+// perm given, the token of that row's pair instead (perm[row] / top_k; pair
+// indices outside [0, pairs) count as padding).
+__global__ void k_rowmap_from_offsets(const int32_t *__restrict__ goffsets,
                                       const int32_t *__restrict__ poffsets, int E, int64_t rows,
+                                      const int32_t *__restrict__ perm, int top_k, int64_t pairs,
                                       int32_t *row_map) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
@@ -229,32 +272,50 @@ __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ offsets,
         else hi = mid - 1;
       }
       const int64_t i = r - poffsets[lo];
-      if (i < offsets[lo + 1] - offsets[lo]) v = (int32_t)(offsets[lo] + i);
+      if (i < goffsets[lo + 1] - goffsets[lo]) {
+        v = (int32_t)(goffsets[lo] + i);
+        if (perm) {
+          const int32_t pr = perm[v];
+          v = (pr >= 0 && pr < pairs) ? pr / top_k : -1;
+        }
+      }
     }
     row_map[r] = v;
   }
 }
 
-cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t padded_rows_max,
-                                       int32_t *poffsets, GroupTile *gtiles, int32_t *gnum_mtiles,
-                                       int32_t *row_map, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_pdl(k_offsets_layout, dim3(1), dim3(1024), 0, st, offsets, E, poffsets, gtiles, gnum_mtiles);
+cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pairs, int64_t padded_rows_max,
+                                       int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
+                                       int32_t *gnum_mtiles, int32_t *row_map, const int32_t *perm, int top_k,
+                                       int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_pdl(k_offsets_layout, dim3(1), dim3(1024), 0, st, offsets, E, pairs, goffsets, poffsets,
+                             gtiles, gnum_mtiles);
   if (e != cudaSuccess) return e;
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((padded_rows_max + 255) / 256, (int64_t)num_sms * 4));
-  return launch_pdl(k_rowmap_from_offsets, dim3((unsigned)ctas), dim3(256), 0, st, offsets,
-                    (const int32_t *)poffsets, E, padded_rows_max, row_map);
+  return launch_pdl(k_rowmap_from_offsets, dim3((unsigned)ctas), dim3(256), 0, st, (const int32_t *)goffsets,
+                    (const int32_t *)poffsets, E, padded_rows_max, perm, top_k, pairs, row_map);
 }
 
 // ----------------------------------------------------------------- combine --
 // y[t][n] = sum over slots j (in order) of w[t][j] * d[g(t, j)][n], fp32
 // accumulation (one fused multiply-add per slot), rounded once to bf16, where
 // g(t, j) is the grouped row of pair t*top_k + j (the inverse of perm).
+// perm is the caller's device data: entries outside [0, pairs) are skipped,
+// and inv is first filled with -1 so that a pair no entry names reads nothing.
 __global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, int32_t *inv) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pairs;
-       i += (int64_t)gridDim.x * blockDim.x)
-    inv[perm[i]] = (int32_t)i;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t q = perm[i];
+    if (q >= 0 && q < pairs) inv[q] = (int32_t)i;
+  }
+}
+__global__ void k_fill_i32(int32_t *p, int64_t n, int32_t v) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = v;
 }
 
 // A warp takes a token: its slots' row indices and weights are read once, and
@@ -277,13 +338,14 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
       float wj[kMaxK];
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        rows[j] = j < top_k ? reinterpret_cast<const uint4 *>(d + (int64_t)inv[t * top_k + j] * N) : nullptr;
-        wj[j] = j < top_k ? w[t * top_k + j] : 0.0f;
+        const int32_t g = j < top_k ? inv[t * top_k + j] : -1;
+        rows[j] = g >= 0 ? reinterpret_cast<const uint4 *>(d + (int64_t)g * N) : nullptr;
+        wj[j] = g >= 0 ? w[t * top_k + j] : 0.0f;
       }
       for (int64_t v = lane; v < vecs; v += 32) {
         uint4 q[kMaxK];
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) q[j] = j < top_k ? __ldg(rows[j] + v) : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kMaxK; ++j) q[j] = rows[j] ? __ldg(rows[j] + v) : make_uint4(0, 0, 0, 0);
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -313,6 +375,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
       for (int j = 0; j < top_k; ++j) {
         const int64_t g = inv[t * top_k + j];
+        if (g < 0) continue;
         const float wv = w[t * top_k + j];
         const uint4 q = __ldg(reinterpret_cast<const uint4 *>(d + g * N) + v);
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
@@ -338,7 +401,9 @@ cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int3
                                cudaStream_t st) {
   const int64_t pairs = tokens * top_k;
   const int64_t c1 = std::max<int64_t>(1, std::min<int64_t>((pairs + 255) / 256, (int64_t)num_sms * 4));
-  cudaError_t e = launch_pdl(k_invert_perm, dim3((unsigned)c1), dim3(256), 0, st, perm, pairs, inv);
+  cudaError_t e = launch_pdl(k_fill_i32, dim3((unsigned)c1), dim3(256), 0, st, inv, pairs, (int32_t)-1);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_invert_perm, dim3((unsigned)c1), dim3(256), 0, st, perm, pairs, inv);
   if (e != cudaSuccess) return e;
   const int64_t c2 = std::max<int64_t>(1, std::min<int64_t>((tokens + 7) / 8, (int64_t)num_sms * 8));
   return launch_pdl(k_moe_combine, dim3((unsigned)c2), dim3(256), 0, st, d, (const int32_t *)inv, w, tokens, top_k,

@@ -96,3 +96,110 @@ def test_grouped_full_size_sampled():
     term = np.stack([lora_bf16_term(xb[perm_or[i] // topk][None], la[flat[perm_or[i]]],
                                     lb[flat[perm_or[i]]], t["alpha"])[0] for i in rows])
     assert_gemm_close(d[torch.from_numpy(rows).cuda()], y_or, S, term, what="grouped full")
+
+
+def test_grouped_input_forms_identical():
+    """The three input forms of the grouped call give the same bits: bf16 rows
+    with a static global scale; the same rows packed beforehand (codes + linear
+    scales, the quantizer's output) with that scale; and the grouping passed in
+    as offsets + perm instead of expert ids."""
+    c = make_case("grouped", T=200, E=24, N=512, K=512, rank=32)
+    E, N, K, topk = c["E"], c["N"], c["K"], c["topk"]
+    wc, ws, wg = quant_experts(c["w"])
+    ids = torch.from_numpy(c["expert_ids"]).cuda()
+    x = dev_bf16(c["x"])
+    q = nv.nvfp4_quantize(x, pack="row", sf_layout="linear")
+    g = q["global_scale"]
+    d1, perm1, offs1 = nv.nvfp4_grouped_gemm(ids, x, wc, ws, wg, N, K, E, x_global_scale=g)
+    d2, perm2, offs2 = nv.nvfp4_grouped_gemm(ids, None, wc, ws, wg, N, K, E, x_global_scale=g,
+                                             x_packed=(q["codes_row"], q["sf_row"]))
+    d3, perm3, offs3 = nv.nvfp4_grouped_gemm(None, None, wc, ws, wg, N, K, E, x_global_scale=g,
+                                             x_packed=(q["codes_row"], q["sf_row"]),
+                                             routing=(offs1, perm1), top_k=topk)
+    torch.cuda.synchronize()
+    assert torch.equal(perm1, perm2) and torch.equal(offs1, offs2)
+    assert torch.equal(perm3, perm1) and torch.equal(offs3, offs1)
+    assert torch.equal(d1.view(torch.int16), d2.view(torch.int16))
+    assert torch.equal(d1.view(torch.int16), d3.view(torch.int16))
+    # and the packed form against the oracle (the static scale is the tensor's own)
+    counts, offsets, perm_or = o.group_rows(c["expert_ids"], E)
+    assert np.array_equal(perm1.cpu().numpy(), perm_or)
+    xq = o.quantize(c["x"])
+    wq = {e: o.quantize(c["w"][e]) for e in range(E)}
+    rows = np.arange(perm_or.size)
+    y_or, S = o.grouped_linear_rows(rows, c["x"], xq, {e: wq[e][0] for e in wq},
+                                    {e: wq[e][1] for e in wq}, {e: wq[e][2] for e in wq}, perm_or,
+                                    c["expert_ids"], topk, None)
+    assert_gemm_close(d2, y_or, S, None, what="grouped packed input")
+
+
+@pytest.mark.parametrize("with_lora", [False, True])
+def test_grouped_fp32_output(with_lora):
+    """out_dtype fp32 within the fp32 tolerance of the oracle; the bf16 output
+    is that fp32 result rounded to nearest even."""
+    c = make_case("grouped", T=96, E=16, N=256, K=512, rank=64)
+    E, N, K = c["E"], c["N"], c["K"]
+    wc, ws, wg = quant_experts(c["w"])
+    ids = torch.from_numpy(c["expert_ids"]).cuda()
+    x = dev_bf16(c["x"])
+    lora = dict(a=dev_bf16(c["lora_a"]), b=dev_bf16(c["lora_b"]), alpha=c["alpha"]) if with_lora else None
+    d32, perm, _ = nv.nvfp4_grouped_gemm(ids, x, wc, ws, wg, N, K, E, lora=lora,
+                                         out_dtype=torch.float32)
+    d16, _, _ = nv.nvfp4_grouped_gemm(ids, x, wc, ws, wg, N, K, E, lora=lora)
+    torch.cuda.synchronize()
+    assert d32.dtype == torch.float32
+    assert torch.equal(d32.to(torch.bfloat16).view(torch.int16), d16.view(torch.int16))
+    counts, offsets, perm_or = o.group_rows(c["expert_ids"], E)
+    xq = o.quantize(c["x"])
+    wq = {e: o.quantize(c["w"][e]) for e in range(E)}
+    rows = np.arange(perm_or.size)
+    lo = (c["lora_a"], c["lora_b"], c["alpha"]) if with_lora else None
+    y_or, S = o.grouped_linear_rows(rows, c["x"], xq, {e: wq[e][0] for e in wq},
+                                    {e: wq[e][1] for e in wq}, {e: wq[e][2] for e in wq}, perm_or,
+                                    c["expert_ids"], c["topk"], lo)
+    term = None
+    if with_lora:
+        flat = c["expert_ids"].reshape(-1)
+        term = np.stack([lora_bf16_term(c["x"][perm_or[i] // c["topk"]][None],
+                                        c["lora_a"][flat[perm_or[i]]], c["lora_b"][flat[perm_or[i]]],
+                                        c["alpha"])[0] for i in rows])
+    assert_gemm_close(d32, y_or, S, term, what="grouped fp32")
+
+
+def test_grouped_given_routing_inconsistent():
+    """Given routing is device data the host cannot check: offsets that step
+    backwards or past the pair count, and perm entries outside [0, P), are
+    clamped (counts cumulatively to P, such pairs as padding).  The call
+    succeeds, the sanitized offsets come back, and the rows the clamped layout
+    does hold are computed as usual."""
+    c = make_case("grouped", T=64, E=8, N=256, K=256, rank=32)
+    E, N, K, topk = c["E"], c["N"], c["K"], c["topk"]
+    P = c["T"] * topk
+    wc, ws, wg = quant_experts(c["w"])
+    ids = torch.from_numpy(c["expert_ids"]).cuda()
+    x = dev_bf16(c["x"])
+    d_ref, perm_ref, offs_ref = nv.nvfp4_grouped_gemm(ids, x, wc, ws, wg, N, K, E)
+    bad_offs = offs_ref.clone()
+    bad_offs[3] = bad_offs[2] - 7            # expert 2 count negative -> 0
+    bad_offs[E] = P + 1000                   # last expert past the end
+    bad_perm = perm_ref.clone()
+    bad_perm[0] = -3
+    bad_perm[1] = P + 5
+    d, perm, offs = nv.nvfp4_grouped_gemm(None, x, wc, ws, wg, N, K, E,
+                                          routing=(bad_offs, bad_perm), top_k=topk)
+    torch.cuda.synchronize()
+    # the sanitized layout: counts of the given offsets clamped to [0, P] cumulatively
+    given = bad_offs.cpu().numpy().astype(np.int64)
+    cnt = np.clip(np.diff(given), 0, P)
+    want = np.zeros(E + 1, np.int64)
+    for e in range(E):
+        want[e + 1] = min(want[e] + cnt[e], P)
+    assert np.array_equal(offs.cpu().numpy(), want)
+    # rows whose expert range and pair are both intact match the consistent call
+    ref_o = offs_ref.cpu().numpy()
+    pr = bad_perm.cpu().numpy()
+    for e in range(E):
+        for i in range(int(want[e]), int(want[e + 1])):
+            j = i - int(want[e]) + int(ref_o[e])          # the same row of the consistent call
+            if 0 <= pr[i] < P and j < ref_o[e + 1] and int(pr[i]) == int(perm_ref[j]):
+                assert torch.equal(d[i].view(torch.int16), d_ref[j].view(torch.int16)), (e, i)
