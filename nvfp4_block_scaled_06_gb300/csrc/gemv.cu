@@ -227,6 +227,29 @@ __device__ __forceinline__ GemvPlan gemv_plan(const GemvParams &p, int nchunks) 
   return q;
 }
 
+// L2 prefetch of a unit's weights: in-CTA mode (thread 0) the unit's rows are
+// contiguous, all K; the unit that starts a 128-row group also takes the
+// group's swizzled scale atoms.  Global mode (one task per warp) fetches the
+// task's R row pieces of one chunk from lanes 0..R-1.
+template <int R>
+__device__ __forceinline__ void gemv_prefetch(const GemvParams &p, const GemvPlan &q, int32_t unit, int lane) {
+  if (unit >= q.units) return;
+  const int64_t row_bytes = p.K / 2;
+  if (q.in_cta) {
+    if (threadIdx.x != 0) return;
+    const int64_t n0 = (int64_t)unit * q.rbu * R;
+    const int64_t span = (int64_t)q.rbu * R, rows = p.N - n0 < span ? p.N - n0 : span;
+    if (rows <= 0) return;
+    prefetch_l2_bulk(p.w_codes + n0 * row_bytes, (uint32_t)(rows * row_bytes));
+    if ((n0 & 127) == 0) prefetch_l2_bulk(p.w_sf + (n0 >> 7) * p.w_sf_katoms * 512, (uint32_t)(p.w_sf_katoms * 512));
+  } else {
+    const int64_t n = (int64_t)(unit / q.nchunks) * R + lane;
+    const int64_t k0 = (int64_t)(unit % q.nchunks) * (kGemvChunk / 2);
+    const int64_t piece = row_bytes - k0 < kGemvChunk / 2 ? row_bytes - k0 : kGemvChunk / 2;
+    if (lane < R && n < p.N) prefetch_l2_bulk(p.w_codes + n * row_bytes + k0, (uint32_t)piece);
+  }
+}
+
 // resident CTAs per SM the register budget is held to: three for the
 // one-row-of-X two-row tasks, two up to two X rows (at most 128 registers)
 constexpr int gemv_min_ctas(int mx, int r) { return mx == 1 && r == 2 ? 3 : mx <= 2 ? 2 : 1; }
@@ -234,6 +257,14 @@ constexpr int gemv_min_ctas(int mx, int r) { return mx == 1 && r == 2 ? 3 : mx <
 template <int MX, int R>
 __global__ void __launch_bounds__(kGemvThreads, gemv_min_ctas(MX, R)) k_gemv(const GemvParams p, int nchunks, float *partial) {
   griddep_launch_dependents();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const GemvPlan q = gemv_plan<R>(p, nchunks);
+  const int32_t ustep = q.in_cta ? (int32_t)gridDim.x : (int32_t)gridDim.x * kWarps;
+  int32_t u = q.in_cta ? (int32_t)blockIdx.x : (int32_t)blockIdx.x * kWarps + w;
+  // The weight stream starts before the wait on the previous grid: an L2
+  // prefetch of the first unit (a cache hint, safe against that grid's
+  // writes) overlaps that grid's tail.
+  gemv_prefetch<R>(p, q, u, lane);
   griddep_wait();   // inputs may come from the previous kernel in the stream
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[2][kWarps][R][4];   // in-CTA chunk sums, double-buffered
@@ -248,13 +279,9 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_ctas(MX, R)) k_gemv(con
   uint32_t *xs = reinterpret_cast<uint32_t *>(smem);             // MX * K/2 words
   float *sxs = reinterpret_cast<float *>(xs + MX * (K / 2));    // MX * K/16 floats
 
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const GemvPlan q = gemv_plan<R>(p, nchunks);
   // this warp's task in unit u (in-CTA) / task index (global)
   const bool active = !q.in_cta || w < q.rbu * q.nchunks;
   const int32_t my_kc = q.in_cta ? w % q.nchunks : 0, my_rb = q.in_cta ? w / q.nchunks : 0;
-  const int32_t ustep = q.in_cta ? (int32_t)gridDim.x : (int32_t)gridDim.x * kWarps;
-  int32_t u = q.in_cta ? (int32_t)blockIdx.x : (int32_t)blockIdx.x * kWarps + w;
   auto task_of = [&](int32_t unit, int32_t &n0, int32_t &kc) {
     if (q.in_cta) {
       n0 = (unit * q.rbu + my_rb) * R;

@@ -95,6 +95,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_u(uint32_t bar, uint32_t b
 }
 
 // --------------------------------------------------------------------- TMA --
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes % 16 == 0).
+// Only a cache hint: L2 is where all SMs' accesses meet, so a line fetched
+// here before another grid writes it is updated by that write.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
