@@ -62,7 +62,12 @@ typedef enum {
   NVFP4_ERR_WORKSPACE = 4,          /* workspace missing or too small */
   NVFP4_ERR_CUDA = 5,               /* a CUDA runtime call failed */
   NVFP4_ERR_TIMEOUT = 6,            /* a bounded in-kernel wait expired */
-  NVFP4_ERR_UNSUPPORTED_DEVICE = 7  /* not an sm_103 device */
+  NVFP4_ERR_UNSUPPORTED_DEVICE = 7, /* not an sm_103 device */
+  NVFP4_ERR_DEVICE_BOUNDS = 8       /* status word, builds with NVFP4_CHECKED defined only:
+                                       a device-side index check failed (caller routing data
+                                       out of range, or a broken internal invariant); the
+                                       access was skipped.  Other builds skip or clamp such
+                                       caller data without recording it. */
 } nvfp4_status;
 
 typedef enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 } nvfp4_sf_layout;

@@ -12,10 +12,13 @@ import ctypes as C
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libnvfp4.so")
+# NVFP4_CHECKED=1 selects the build with device-side index checks
+# (python -m nvfp4_block_scaled_06_gb300.build --checked).
+CHECKED = os.environ.get("NVFP4_CHECKED", "") not in ("", "0")
+LIB_PATH = os.path.join(HERE, "libnvfp4_checked.so" if CHECKED else "libnvfp4.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, \
-    ERR_TIMEOUT, ERR_UNSUPPORTED_DEVICE = range(8)
+    ERR_TIMEOUT, ERR_UNSUPPORTED_DEVICE, ERR_DEVICE_BOUNDS = range(9)
 SF_LINEAR, SF_SWIZZLED = 0, 1
 PACK_ROW, PACK_COL, PACK_BOTH = 1, 2, 3
 OUT_BF16, OUT_FP32 = 0, 1
@@ -158,7 +161,8 @@ def load(path: str | None = None):
     p = path or LIB_PATH
     if not os.path.exists(p):
         raise RuntimeError(
-            f"libnvfp4.so not found at {p}: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+            f"{os.path.basename(p)} not found at {p}: build it first (python -m nvfp4_block_scaled_06_gb300.build"
+            f"{' --checked' if CHECKED else ''})")
     lib = C.CDLL(p)
     for name in EXPORTS:
         if not hasattr(lib, name):

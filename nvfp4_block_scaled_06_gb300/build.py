@@ -75,6 +75,20 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, jobs: int = 8,
     return lib_out
 
 
+LIB_CHECKED = os.path.join(HERE, "libnvfp4_checked.so")
+
+
+def build_checked(verbose: bool = False) -> str:
+    """The build with device-side index checks (NVFP4_CHECKED): violations are
+    recorded in the status word as NVFP4_ERR_DEVICE_BOUNDS and the access is
+    skipped.  Loaded instead of libnvfp4.so when NVFP4_CHECKED=1."""
+    return build(verbose=verbose, defines=("NVFP4_CHECKED",), lib_path=LIB_CHECKED,
+                 build_dir=BUILD + "_checked")
+
+
 if __name__ == "__main__":  # pragma: no cover
     import sys
-    print(build(verbose=True, ptxas_verbose="-v" in sys.argv))
+    if "--checked" in sys.argv:
+        print(build_checked(verbose=True))
+    else:
+        print(build(verbose=True, ptxas_verbose="-v" in sys.argv))

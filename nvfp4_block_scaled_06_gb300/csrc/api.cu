@@ -527,6 +527,7 @@ nvfp4_status validate_grouped(const nvfp4_grouped_args *a) {
 // grouped W4A4 GEMM with the fused LoRA up-projection, D in grouped row order.
 struct GroupedProducts {
   int64_t E, N, K, prow_max;
+  int64_t out_rows;               // rows of d (the pairs)
   const uint8_t *aq, *asf;        // padded A codes / swizzled scales
   const float *g_a;
   const int32_t *row_map;         // padded row -> row of x_src (-1: padding)
@@ -576,6 +577,7 @@ nvfp4_status run_grouped_products(const GroupedProducts &g, int *status, uint64_
     lp.gnum_mtiles = g.nmt;
     lp.row_map = g.row_map;
     lp.x = static_cast<const __nv_bfloat16 *>(g.x_src);
+    lp.x_rows = g.x_rows;
     lp.status = status;
     lp.timeout_ns = tmo;
     if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);
@@ -601,6 +603,7 @@ nvfp4_status run_grouped_products(const GroupedProducts &g, int *status, uint64_
   p.tiles_n = (int)(g.N / bn);
   p.gtiles = g.gtiles;
   p.gnum_mtiles = g.nmt;
+  p.out_rows = g.out_rows;
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
@@ -632,12 +635,13 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
     r.gtiles = pl.gtiles;
     r.gnum_mtiles = pl.nmt;
     r.offsets_out = a->expert_offsets_out;
+    r.status = status;
     if (cudaError_t e_ = launch_route(r, st); e_ != cudaSuccess) return cuda_status(e_);
   } else {
     // the caller's grouping: padded layout from its offsets, row_map -> token through its perm
     if (cudaError_t e_ = launch_layout_from_offsets(a->offsets_in, (int)a->num_experts, P, pl.prow_max, pl.goffsets,
                                                     pl.poffsets, pl.gtiles, pl.nmt, pl.row_map, a->perm_in,
-                                                    (int)a->top_k, sms, st);
+                                                    (int)a->top_k, sms, st, status);
         e_ != cudaSuccess)
       return cuda_status(e_);
     if (a->perm_out && a->perm_out != a->perm_in &&
@@ -650,7 +654,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   if (a->x_codes) {
     // activations already quantized per token row (linear scales) with x_global_scale
     if (cudaError_t e_ = launch_gather_packed(a->x_codes, a->x_sf, pl.row_map, pl.prow_max, pl.nmt, a->K, pl.xq,
-                                              pl.xsf, sms, st);
+                                              pl.xsf, sms, st, a->num_tokens, status);
         e_ != cudaSuccess)
       return cuda_status(e_);
     GroupedProducts gp;
@@ -658,6 +662,8 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
     gp.N = a->N;
     gp.K = a->K;
     gp.prow_max = pl.prow_max;
+  gp.out_rows = P;
+    gp.out_rows = P;
     gp.aq = pl.xq;
     gp.asf = pl.xsf;
     gp.g_a = a->x_global_scale;
@@ -704,7 +710,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   }
   if (cudaError_t e_ = launch_quant_rows(q, sms, st); e_ != cudaSuccess) return cuda_status(e_);
   if (cudaError_t e_ = launch_gather_packed(pl.xq_tok, pl.xsf_tok, pl.row_map, pl.prow_max, pl.nmt, a->K, pl.xq,
-                                            pl.xsf, sms, st);
+                                            pl.xsf, sms, st, a->num_tokens, status);
       e_ != cudaSuccess)
     return cuda_status(e_);
   GroupedProducts gp;
@@ -712,6 +718,7 @@ nvfp4_status run_grouped(const nvfp4_grouped_args *a, const GroupedPlan &pl, int
   gp.N = a->N;
   gp.K = a->K;
   gp.prow_max = pl.prow_max;
+  gp.out_rows = P;
   gp.aq = pl.xq;
   gp.asf = pl.xsf;
   gp.g_a = a->x_global_scale ? a->x_global_scale : pl.g_x;
@@ -796,7 +803,7 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   const int64_t P = a->num_tokens * a->top_k;
   if (cudaError_t e_ = launch_layout_from_offsets(a->expert_offsets, (int)a->num_experts, P, pl.prow_max,
                                                   pl.goffsets, pl.poffsets, pl.gtiles, pl.nmt, pl.row_map,
-                                                  nullptr, 0, sms, st);
+                                                  nullptr, 0, sms, st, status);
       e_ != cudaSuccess)
     return cuda_status(e_);
   // h is quantized once (one tensor-wide g) straight into the padded layout:
@@ -828,6 +835,7 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   gp.N = a->N;
   gp.K = a->K;
   gp.prow_max = pl.prow_max;
+  gp.out_rows = P;
   gp.aq = pl.hq;
   gp.asf = pl.hsf;
   gp.g_a = a->h_global_scale ? a->h_global_scale : pl.g_h;
@@ -851,7 +859,8 @@ nvfp4_status run_moe_down(const nvfp4_moe_down_args *a, const MoeDownPlan &pl, i
   nvfp4_status s = run_grouped_products(gp, status, tmo, sms, st);
   if (s != NVFP4_OK) return s;
   return cuda_status(launch_moe_combine(pl.d, a->perm, pl.inv, a->route_weights, a->num_tokens,
-                                        (int)a->top_k, a->N, static_cast<__nv_bfloat16 *>(a->y), sms, st));
+                                        (int)a->top_k, a->N, static_cast<__nv_bfloat16 *>(a->y), sms, st,
+                                        status));
 }
 
 // --------------------------------------------------------------------- LoRA --
@@ -1267,6 +1276,7 @@ const char *nvfp4_status_string(nvfp4_status s) {
     case NVFP4_ERR_CUDA: return "CUDA runtime error";
     case NVFP4_ERR_TIMEOUT: return "an in-kernel wait timed out";
     case NVFP4_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103";
+    case NVFP4_ERR_DEVICE_BOUNDS: return "a device-side index check failed";
   }
   return "unknown status";
 }

@@ -67,7 +67,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams &p, int t, int 
   const int j = p.gtiles ? t / p.tiles_n : t % nmt;
   ti.n0 = (int64_t)nt * BN;
   if (p.gtiles) {
-    const GroupTile g = p.gtiles[j];
+    GroupTile g = p.gtiles[j];
+    if (!NVFP4_GUARD(g.expert >= 0 && (int64_t)(g.expert + 1) * p.N <= p.b_sf_row_chunks * 128 && g.a_row0 >= 0 &&
+                         g.a_row0 + kBM <= p.M && g.valid_rows >= 0 && g.valid_rows <= kBM && g.out_row0 >= 0 &&
+                         g.out_row0 + g.valid_rows <= p.out_rows,
+                     p.status)) {
+      g.expert = 0;       // an in-range tile that stores nothing
+      g.a_row0 = 0;
+      g.valid_rows = 0;
+      g.out_row0 = 0;
+    }
     ti.e = g.expert;
     ti.a_row0 = g.a_row0;
     ti.valid_rows = g.valid_rows;
@@ -711,7 +720,10 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
         const uint32_t swz = (uint32_t)((gc ^ (grow & 7)) << 4);
         int32_t srow[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) srow[i] = p.row_map[g_row0 + grow + 16 * i];
+        for (int i = 0; i < 8; ++i) {
+          srow[i] = p.row_map[g_row0 + grow + 16 * i];
+          if (!NVFP4_GUARD(srow[i] < p.x_rows, p.status)) srow[i] = -1;
+        }
         int pend[3];
         int npend = 0;
         for (int st = 0; st < nsteps; ++st) {

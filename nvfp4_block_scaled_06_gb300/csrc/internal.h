@@ -61,9 +61,10 @@ cudaError_t launch_dequant(const uint8_t *codes, const uint8_t *sf, int sf_swz, 
                            int64_t cols, int transpose, __nv_bfloat16 *out, int64_t ldo, int num_sms,
                            cudaStream_t st);
 // Token-row codes + linear scales -> expert-grouped rows + swizzled scales.
+// src_rows: token rows of the source (index checks); status: device status word.
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
                                  int64_t rows, const int32_t *num_mtiles, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
-                                 cudaStream_t st);
+                                 cudaStream_t st, int64_t src_rows, int *status);
 
 // --------------------------------------------------------------------- GEMM --
 // One grouped m-tile: expert, first A row (padded grouped order), valid rows,
@@ -90,6 +91,7 @@ struct GemmParams {
   int tiles_m, tiles_n;
   const GroupTile *gtiles;    // grouped mode: m-tile table
   const int32_t *gnum_mtiles; // grouped mode: number of m-tiles (device)
+  int64_t out_rows;           // grouped mode: rows of D (index checks)
   int ksplit;                 // >1: K split into ranges, fp32 partials [ksplit][M][N]
   float *partial;
   int *status;
@@ -124,6 +126,7 @@ struct LoraDownParams {
   const int32_t *gnum_mtiles;
   const int32_t *row_map;     // grouped: padded row -> token (gather)
   const __nv_bfloat16 *x;     // grouped: token rows of X, leading dimension K
+  int64_t x_rows;             // grouped: token rows of X (index checks)
   uint32_t *amax_part;        // optional: per-CTA max |x| magnitude bits of the X tiles read
   float *t_f32;               // optional: write T in fp32 (unscaled) instead of T'
   int ksplit;                 // with t_f32: K split in ranges, partials [ksplit][M][rank]
@@ -174,6 +177,7 @@ struct RouteParams {
   GroupTile *gtiles;          // [max m-tiles]
   int32_t *gnum_mtiles;
   int32_t *offsets_out;       // optional copy of offsets for the caller
+  int *status;                // device status word (index checks)
 };
 cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 // Padded grouped layout (goffsets = the clamped offsets rebuilt, poffsets,
@@ -182,11 +186,11 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st);
 cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pairs, int64_t padded_rows_max,
                                        int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
                                        int32_t *gnum_mtiles, int32_t *row_map, const int32_t *perm, int top_k,
-                                       int num_sms, cudaStream_t st);
+                                       int num_sms, cudaStream_t st, int *status);
 // y[t] = sum_j w[t][j] d[inverse perm (t*top_k + j)] (bf16 rows, fp32 sums).
 cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int32_t *inv, const float *w,
                                int64_t tokens, int top_k, int64_t N, __nv_bfloat16 *y, int num_sms,
-                               cudaStream_t st);
+                               cudaStream_t st, int *status);
 
 // ------------------------------------------------------------- tensor maps --
 // Encodes a 2-D row-major tensor map; returns false on failure.

@@ -21,6 +21,26 @@ __device__ __forceinline__ void record_timeout(int *status) {
   if (status) atomicExch(status, kStatusTimeout);
 }
 
+// Device-side index checks.  NVFP4_NOTE(cond, status) is a condition the
+// kernels already handle (caller data out of range, skipped or clamped):
+// always evaluated, and in checked builds (-DNVFP4_CHECKED) a false one is
+// also recorded.  NVFP4_GUARD(cond, status) is an internal invariant: checked
+// builds evaluate it, record a violation and skip the access; other builds
+// take it as true.  A violation writes kStatusBounds into the status word
+// unless an earlier error is there; nothing traps.
+constexpr int kStatusBounds = 8;   // == NVFP4_ERR_DEVICE_BOUNDS
+__device__ __forceinline__ bool note_bounds(bool ok, int *status) {
+  if (!ok && status) atomicCAS(status, 0, kStatusBounds);
+  return ok;
+}
+#ifdef NVFP4_CHECKED
+#define NVFP4_NOTE(cond, status) ::nvfp4::note_bounds(static_cast<bool>(cond), (status))
+#define NVFP4_GUARD(cond, status) ::nvfp4::note_bounds(static_cast<bool>(cond), (status))
+#else
+#define NVFP4_NOTE(cond, status) (static_cast<bool>(cond))
+#define NVFP4_GUARD(cond, status) (true)
+#endif
+
 // ---------------------------------------------------------------- mbarrier --
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
     const int64_t r = wi / nch, ch = wi - r * nch;
     int64_t sr = -1;
     if (r < p.dst_rows) sr = p.row_map ? (int64_t)p.row_map[r] : r;
+    if (!NVFP4_GUARD(sr < p.rows, p.status)) sr = -1;
     if (p.row_map && sr < 0) continue;   // unmapped (padding) rows are left untouched
     if (p.t_f32 && r < p.dst_rows && ch == 0) {
       // LoRA hand-off: the down-projection's fp32 row, scaled and rounded once to bf16
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(kQWarps * 32, 1)
   // unit -> (matrix, row, segment, source row); source row < 0: nothing to copy
   auto source_row = [&](int64_t r) -> int64_t {
     if (r >= p.dst_rows) return -1;
-    return p.row_map ? (int64_t)p.row_map[r] : r;
+    const int64_t sr = p.row_map ? (int64_t)p.row_map[r] : r;
+    return NVFP4_GUARD(sr < p.rows, p.status) ? sr : -1;
   };
   struct Cursor {
     int64_t b, r, sg;
@@ -775,7 +777,8 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
                                                        const int32_t *__restrict__ row_map, int64_t rows,
                                                        const int32_t *__restrict__ num_mtiles, int64_t K,
                                                        uint8_t *__restrict__ codes_dst,
-                                                       uint8_t *__restrict__ sf_dst) {
+                                                       uint8_t *__restrict__ sf_dst, int64_t src_rows,
+                                                       int *status) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   const int lane = threadIdx.x & 31;
@@ -794,6 +797,7 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
     for (int i = 0; i < 4; ++i) {
       const int64_t r = r0 + 32 * i;
       sr[i] = r < rows ? (int64_t)row_map[r] : -1;
+      if (!NVFP4_GUARD(sr[i] < src_rows, status)) sr[i] = -1;
     }
     // codes of the four rows, eight 16-byte loads per lane in flight
 #pragma unroll
@@ -839,11 +843,11 @@ __global__ void __launch_bounds__(256) k_gather_packed(const uint8_t *__restrict
 
 cudaError_t launch_gather_packed(const uint8_t *codes_src, const uint8_t *sf_src, const int32_t *row_map,
                                  int64_t rows, const int32_t *num_mtiles, int64_t K, uint8_t *codes_dst, uint8_t *sf_dst, int num_sms,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, int64_t src_rows, int *status) {
   const int64_t quads = ((rows + 127) / 128) * 32;   // one warp per four rows
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((quads + 7) / 8, (int64_t)num_sms * 8));
   return launch_pdl(k_gather_packed, dim3((unsigned)ctas), dim3(256), 0, st, codes_src, sf_src, row_map, rows,
-                    num_mtiles, K, codes_dst, sf_dst);
+                    num_mtiles, K, codes_dst, sf_dst, src_rows, status);
 }
 
 // Zero the swizzled padding of a scale buffer that the tile kernel does not

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(1024) k_route_hist(const RouteParams p) {
   const int64_t i = (int64_t)blockIdx.x * p.chunk + threadIdx.x;
   if (threadIdx.x < p.chunk && i < p.pairs) {
     const int e = p.expert_ids[i];
-    if (e >= 0 && e < p.num_experts) atomicAdd(&sh_hist[e], 1);
+    if (NVFP4_NOTE(e >= 0 && e < p.num_experts, p.status)) atomicAdd(&sh_hist[e], 1);   // others are dropped
   }
   __syncthreads();
   for (int e = threadIdx.x; e < p.num_experts; e += blockDim.x)
@@ -144,9 +144,10 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
       g.a_row0 = poff + 128 * j;
       g.valid_rows = min(128, count - 128 * j);
       g.out_row0 = off + 128 * j;
-      p.gtiles[moff + j] = g;
+      if (NVFP4_GUARD(moff + j < p.padded_rows_max / 128, p.status)) p.gtiles[moff + j] = g;
     }
-    for (int32_t i = count; i < padded; ++i) p.row_map[poff + i] = -1;
+    for (int32_t i = count; i < padded; ++i)
+      if (NVFP4_GUARD(poff + i < p.padded_rows_max, p.status)) p.row_map[poff + i] = -1;
   }
   if (threadIdx.x == 0) {
     p.offsets[p.num_experts] = total;
@@ -191,8 +192,11 @@ __global__ void __launch_bounds__(1024) k_route_scatter(const RouteParams p) {
     int before = 0;
     for (int v = 0; v < w; ++v) before += sh_cnt[v * E + e];
     const int32_t pos = sh_base[e] + before + rank_w;
-    p.perm[pos] = (int32_t)i;
-    p.row_map[p.poffsets[e] + (pos - p.offsets[e])] = (int32_t)(i / p.top_k);
+    const int64_t prow = (int64_t)p.poffsets[e] + (pos - p.offsets[e]);
+    if (NVFP4_GUARD(pos >= 0 && pos < p.pairs && prow >= 0 && prow < p.padded_rows_max, p.status)) {
+      p.perm[pos] = (int32_t)i;
+      p.row_map[prow] = (int32_t)(i / p.top_k);
+    }
   }
 }
 
@@ -217,7 +221,7 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t st) {
 // grouped rows or the padded bound.
 __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restrict__ offsets, int E, int64_t pairs,
                                                          int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
-                                                         int32_t *gnum_mtiles) {
+                                                         int32_t *gnum_mtiles, int64_t max_tiles, int *status) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   __shared__ int32_t scratch[64];
@@ -227,6 +231,8 @@ __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restri
   int32_t count = (int32_t)(diff < 0 ? 0 : diff > pairs ? pairs : diff);
   const int32_t before = block_exclusive_scan_capped(count, (int32_t)pairs, scratch);
   count = min(count, (int32_t)pairs - before);
+  (void)NVFP4_NOTE(!act || (int64_t)count == diff, status);   // the caller's offsets were clamped
+  if (threadIdx.x == 0) (void)NVFP4_NOTE(offsets[0] == 0, status);
   const int32_t padded = (count + 127) & ~127;
   const int32_t mt = padded / 128;
   int32_t ctotal, ptotal, mtotal;
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restri
       g.a_row0 = poff + 128 * j;
       g.valid_rows = min(128, count - 128 * j);
       g.out_row0 = off + 128 * j;
-      gtiles[moff + j] = g;
+      if (NVFP4_GUARD(moff + j < max_tiles, status)) gtiles[moff + j] = g;
     }
   }
   if (threadIdx.x == 0) {
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(1024) k_offsets_layout(const int32_t *__restri
 __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ goffsets,
                                       const int32_t *__restrict__ poffsets, int E, int64_t rows,
                                       const int32_t *__restrict__ perm, int top_k, int64_t pairs,
-                                      int32_t *row_map) {
+                                      int32_t *row_map, int *status) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows;
@@ -276,7 +282,7 @@ __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ goffsets,
         v = (int32_t)(goffsets[lo] + i);
         if (perm) {
           const int32_t pr = perm[v];
-          v = (pr >= 0 && pr < pairs) ? pr / top_k : -1;
+          v = NVFP4_NOTE(pr >= 0 && pr < pairs, status) ? pr / top_k : -1;
         }
       }
     }
@@ -287,13 +293,13 @@ __global__ void k_rowmap_from_offsets(const int32_t *__restrict__ goffsets,
 cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pairs, int64_t padded_rows_max,
                                        int32_t *goffsets, int32_t *poffsets, GroupTile *gtiles,
                                        int32_t *gnum_mtiles, int32_t *row_map, const int32_t *perm, int top_k,
-                                       int num_sms, cudaStream_t st) {
+                                       int num_sms, cudaStream_t st, int *status) {
   cudaError_t e = launch_pdl(k_offsets_layout, dim3(1), dim3(1024), 0, st, offsets, E, pairs, goffsets, poffsets,
-                             gtiles, gnum_mtiles);
+                             gtiles, gnum_mtiles, padded_rows_max / 128, status);
   if (e != cudaSuccess) return e;
   const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((padded_rows_max + 255) / 256, (int64_t)num_sms * 4));
   return launch_pdl(k_rowmap_from_offsets, dim3((unsigned)ctas), dim3(256), 0, st, (const int32_t *)goffsets,
-                    (const int32_t *)poffsets, E, padded_rows_max, perm, top_k, pairs, row_map);
+                    (const int32_t *)poffsets, E, padded_rows_max, perm, top_k, pairs, row_map, status);
 }
 
 // ----------------------------------------------------------------- combine --
@@ -302,13 +308,13 @@ cudaError_t launch_layout_from_offsets(const int32_t *offsets, int E, int64_t pa
 // g(t, j) is the grouped row of pair t*top_k + j (the inverse of perm).
 // perm is the caller's device data: entries outside [0, pairs) are skipped,
 // and inv is first filled with -1 so that a pair no entry names reads nothing.
-__global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, int32_t *inv) {
+__global__ void k_invert_perm(const int32_t *__restrict__ perm, int64_t pairs, int32_t *inv, int *status) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < pairs;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t q = perm[i];
-    if (q >= 0 && q < pairs) inv[q] = (int32_t)i;
+    if (NVFP4_NOTE(q >= 0 && q < pairs, status)) inv[q] = (int32_t)i;
   }
 }
 __global__ void k_fill_i32(int32_t *p, int64_t n, int32_t v) {
@@ -324,7 +330,7 @@ __global__ void k_fill_i32(int32_t *p, int64_t n, int32_t v) {
 __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__restrict__ d,
                                                      const int32_t *__restrict__ inv,
                                                      const float *__restrict__ w, int64_t tokens, int top_k,
-                                                     int64_t N, __nv_bfloat16 *__restrict__ y) {
+                                                     int64_t N, __nv_bfloat16 *__restrict__ y, int *status) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
   constexpr int kMaxK = 8;
@@ -338,7 +344,8 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
       float wj[kMaxK];
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        const int32_t g = j < top_k ? inv[t * top_k + j] : -1;
+        int32_t g = j < top_k ? inv[t * top_k + j] : -1;
+        if (!NVFP4_GUARD(g < tokens * top_k, status)) g = -1;
         rows[j] = g >= 0 ? reinterpret_cast<const uint4 *>(d + (int64_t)g * N) : nullptr;
         wj[j] = g >= 0 ? w[t * top_k + j] : 0.0f;
       }
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
       for (int j = 0; j < top_k; ++j) {
         const int64_t g = inv[t * top_k + j];
-        if (g < 0) continue;
+        if (g < 0 || !NVFP4_GUARD(g < tokens * top_k, status)) continue;
         const float wv = w[t * top_k + j];
         const uint4 q = __ldg(reinterpret_cast<const uint4 *>(d + g * N) + v);
         const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
@@ -398,16 +405,16 @@ __global__ void __launch_bounds__(256) k_moe_combine(const __nv_bfloat16 *__rest
 
 cudaError_t launch_moe_combine(const __nv_bfloat16 *d, const int32_t *perm, int32_t *inv, const float *w,
                                int64_t tokens, int top_k, int64_t N, __nv_bfloat16 *y, int num_sms,
-                               cudaStream_t st) {
+                               cudaStream_t st, int *status) {
   const int64_t pairs = tokens * top_k;
   const int64_t c1 = std::max<int64_t>(1, std::min<int64_t>((pairs + 255) / 256, (int64_t)num_sms * 4));
   cudaError_t e = launch_pdl(k_fill_i32, dim3((unsigned)c1), dim3(256), 0, st, inv, pairs, (int32_t)-1);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_invert_perm, dim3((unsigned)c1), dim3(256), 0, st, perm, pairs, inv);
+  e = launch_pdl(k_invert_perm, dim3((unsigned)c1), dim3(256), 0, st, perm, pairs, inv, status);
   if (e != cudaSuccess) return e;
   const int64_t c2 = std::max<int64_t>(1, std::min<int64_t>((tokens + 7) / 8, (int64_t)num_sms * 8));
   return launch_pdl(k_moe_combine, dim3((unsigned)c2), dim3(256), 0, st, d, (const int32_t *)inv, w, tokens, top_k,
-                    N, y);
+                    N, y, status);
 }
 
 }  // namespace nvfp4
