@@ -48,9 +48,10 @@ PREFILL = dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0)
 L2_BYTES = 129 * 1024 * 1024
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
 # DRAM bytes (read + write) of one GEMM launch on the prefill workload, from
-# one ncu capture of the current kernel; None until the current kernel has
-# been captured.
-GEMM_TRAFFIC_BYTES = None
+# one ncu capture of the current kernel (36.8 MB read + 3.1 MB written; Y is
+# still in L2 when the launch ends); None whenever the kernel has changed
+# since that capture.
+GEMM_TRAFFIC_BYTES = 39.9e6
 
 
 def peaks():
@@ -381,10 +382,10 @@ def run_decode(torch, nv, device, steps, warmup, pk):
     return res
 
 
-def run_grouped(torch, nv, device, steps, warmup, pk):
+def run_grouped(torch, nv, device, steps, warmup, pk, experts=None):
     import ctypes as C
     from synth import torch_case
-    c = torch_case("grouped", seed=0, device=device)
+    c = torch_case("grouped", seed=0, device=device, **({"E": experts} if experts else {}))
     E, N, K, T, topk = c["E"], c["N"], c["K"], c["T"], c["topk"]
     wq = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
     del c["w"]
@@ -459,12 +460,12 @@ def run_dgrad(torch, nv, device, steps, warmup, pk):
     return out
 
 
-def run_moe_down(torch, nv, device, steps, warmup, pk):
+def run_moe_down(torch, nv, device, steps, warmup, pk, experts=None):
     """The routed experts' down-projection W2_e[6144,2048] + gate-weighted combine
     for 4096 tokens x top-8 (the grouped up-projection's successor)."""
     import ctypes as C
     from synth import torch_case
-    c = torch_case("moe_down", seed=0, device=device)
+    c = torch_case("moe_down", seed=0, device=device, **({"E": experts} if experts else {}))
     E, N, K, T, k = c["E"], c["N"], c["K"], c["T"], c["topk"]
     wq = nv.nvfp4_quantize(c["w"], pack="row", sf_layout="swizzled")
     del c["w"]
@@ -584,6 +585,9 @@ def main():
     ap.add_argument("--only", choices=["quantize", "decode", "grouped", "dgrad", "moe_down"],
                     help="run just this secondary workload (for profiling) and print its numbers")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="with --only grouped/moe_down: number of routed experts (default: the "
+                         "workload's 256; fewer keep an ncu capture to a few GB on the device)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -607,7 +611,8 @@ def main():
     if args.only:
         fn = dict(quantize=run_quantize_sweep, decode=run_decode, grouped=run_grouped,
                   dgrad=run_dgrad, moe_down=run_moe_down)[args.only]
-        res = fn(torch, nv, device, args.steps, args.warmup, pk)
+        kw = {"experts": args.experts} if args.only in ("grouped", "moe_down") and args.experts else {}
+        res = fn(torch, nv, device, args.steps, args.warmup, pk, **kw)
         if rank == 0:
             print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup, **res}))
         return
@@ -651,7 +656,8 @@ def main():
                       peak=fp4_peak, unit="TFLOP/s", frac=gemm_tflops / fp4_peak,
                       traffic=GEMM_TRAFFIC_BYTES,
                       traffic_note="dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu "
-                                   "capture of this kernel on this workload (M8192 N2048 K6144)",
+                                   "capture of this kernel on this workload (M8192 N2048 K6144, "
+                                   "cold L2); algorithmic bytes 70.3 MB",
                       peak_note=f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x 6 "
                                 f"(nominal fp4:bf16), of {pk['source']}",
                       timing_note="CUDA events around each GEMM launch in a second run of the same "
