@@ -432,9 +432,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int nvalid = full_chunk ? 32 : (int)(p.N - n);
           if (p.partial) {
             float *dst = p.partial + ((int64_t)ks * p.M + orow) * p.N + n;
+            if (full_chunk && (reinterpret_cast<uintptr_t>(dst) & 31) == 0) {   // whole 32-byte sectors
 #pragma unroll
-            for (int i2 = 0; i2 < 32; ++i2)
-              if (i2 < nvalid) dst[i2] = f[i2];
+              for (int i2 = 0; i2 < 32; i2 += 8)
+                st_global_v8(dst + i2, __float_as_uint(f[i2]), __float_as_uint(f[i2 + 1]),
+                             __float_as_uint(f[i2 + 2]), __float_as_uint(f[i2 + 3]), __float_as_uint(f[i2 + 4]),
+                             __float_as_uint(f[i2 + 5]), __float_as_uint(f[i2 + 6]), __float_as_uint(f[i2 + 7]));
+            } else {
+#pragma unroll
+              for (int i2 = 0; i2 < 32; ++i2)
+                if (i2 < nvalid) dst[i2] = f[i2];
+            }
           } else if (p.out_fp32) {
             float *dst = reinterpret_cast<float *>(p.d) + orow * p.ldd + n;
             if (p.accumulate_d) {
@@ -875,6 +883,41 @@ __global__ void __launch_bounds__(kLoraThreads, 1)
 }
 
 // ----------------------------------------------------------- split-K sum --
+// Four consecutive outputs per thread and pass (N % 4 == 0): the partials of
+// every K range are loaded before they are added, so the loads of a pass are
+// in flight together; sums in K-range order as below.
+__global__ void k_splitk_reduce4(const GemmParams p) {
+  griddep_launch_dependents();
+  griddep_wait();   // inputs may come from the previous kernel in the stream
+  constexpr int kMaxSplit = 16;
+  const int64_t total = p.M * p.N, quads = total / 4;
+  const float4 *part = reinterpret_cast<const float4 *>(p.partial);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < quads;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 v[kMaxSplit];
+#pragma unroll
+    for (int k = 0; k < kMaxSplit; ++k)
+      if (k < p.ksplit) v[k] = part[k * quads + i];
+    float4 s = v[0];
+#pragma unroll
+    for (int k = 1; k < kMaxSplit; ++k)
+      if (k < p.ksplit) {
+        s.x = __fadd_rn(s.x, v[k].x);
+        s.y = __fadd_rn(s.y, v[k].y);
+        s.z = __fadd_rn(s.z, v[k].z);
+        s.w = __fadd_rn(s.w, v[k].w);
+      }
+    const int64_t e = 4 * i, m = e / p.N, n = e - m * p.N;
+    if (p.out_fp32) {
+      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.d) + m * p.ldd + n) = s;
+    } else {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(s.x, s.y), hi = __floats2bfloat162_rn(s.z, s.w);
+      *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.d) + m * p.ldd + n) =
+          make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    }
+  }
+}
+
 __global__ void k_splitk_reduce(const GemmParams p) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
@@ -891,6 +934,15 @@ __global__ void k_splitk_reduce(const GemmParams p) {
 
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st) {
   const int64_t total = p.M * p.N;
+  // the vector form: rows of whole quads, 16-byte partials, aligned output quads
+  const bool quad = p.N % 4 == 0 && p.ldd % 4 == 0 && p.ksplit <= 16 &&
+                    (reinterpret_cast<uintptr_t>(p.partial) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(p.d) & (p.out_fp32 ? 15 : 7)) == 0;
+  if (quad) {
+    const int64_t quads = total / 4;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((quads + 255) / 256, (int64_t)num_sms * 8));
+    return launch_pdl(k_splitk_reduce4, dim3(grid), dim3(256), 0, st, p);
+  }
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 4));
   return launch_pdl(k_splitk_reduce, dim3(grid), dim3(256), 0, st, p);
 }
