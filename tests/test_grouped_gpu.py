@@ -203,3 +203,21 @@ def test_grouped_given_routing_inconsistent():
             j = i - int(want[e]) + int(ref_o[e])          # the same row of the consistent call
             if 0 <= pr[i] < P and j < ref_o[e + 1] and int(pr[i]) == int(perm_ref[j]):
                 assert torch.equal(d[i].view(torch.int16), d_ref[j].view(torch.int16)), (e, i)
+
+
+def test_grouped_single_expert_top1():
+    """Degenerate routing: top-1 with every token on one expert (three m-tiles,
+    the last one ragged) and the other 15 experts empty."""
+    c = make_case("grouped", T=300, E=16, topk=1, N=256, K=512, rank=32)
+    c["expert_ids"] = np.full((300, 1), 5, np.int32)
+    run_case(c, True)
+
+
+def test_grouped_repeated_expert_in_a_token():
+    """top-2 with both slots of every third token on the same expert: two pairs
+    of one token in one expert's rows, kept in pair order."""
+    c = make_case("grouped", T=128, E=8, topk=2, N=256, K=256, rank=32)
+    ids = c["expert_ids"].copy()
+    ids[::3, 1] = ids[::3, 0]
+    c["expert_ids"] = ids
+    run_case(c, False)

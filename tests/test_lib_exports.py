@@ -89,3 +89,36 @@ def test_product_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.replace("the oracle", ""), f
+
+
+def test_grouped_input_forms_validation(clib):
+    """The grouped call's routing and activation forms are checked on the host:
+    exactly one routing form (expert ids + perm_out, or offsets + perm), packed
+    activations with their scales and global scale, bf16 rows with a LoRA, a
+    known output dtype.  Valid forms pass validation (and then fail for the
+    missing device, or the missing workspace, never with INVALID_ARG)."""
+    from nvfp4_block_scaled_06_gb300._binding import ERR_INVALID_ARG, GroupedArgs, OUT_FP32
+
+    def grouped(**kw):
+        base = dict(num_tokens=4, top_k=2, num_experts=8, N=256, K=64, w_codes=4096, w_sf=4096,
+                    w_global_scale=4096, d=4096)
+        base.update(kw)
+        return clib.nvfp4_grouped_gemm(C.byref(GroupedArgs(**base)), None)
+
+    ids = dict(expert_ids=4096, perm_out=4096)
+    given = dict(offsets_in=4096, perm_in=4096)
+    bf16 = dict(x_bf16=4096)
+    packed = dict(x_codes=4096, x_sf=4096, x_global_scale=4096)
+    assert grouped(**bf16) == ERR_INVALID_ARG                                   # no routing
+    assert grouped(**ids, **given, **bf16) == ERR_INVALID_ARG                   # both routings
+    assert grouped(expert_ids=4096, **bf16) == ERR_INVALID_ARG                  # ids without perm_out
+    assert grouped(**ids, offsets_in=4096, **bf16) == ERR_INVALID_ARG           # ids + half of given
+    assert grouped(offsets_in=4096, **bf16) == ERR_INVALID_ARG                  # offsets without perm
+    assert grouped(**ids) == ERR_INVALID_ARG                                    # no activations
+    assert grouped(**ids, x_codes=4096, x_global_scale=4096) == ERR_INVALID_ARG  # codes without scales
+    assert grouped(**ids, x_codes=4096, x_sf=4096) == ERR_INVALID_ARG           # packed without g_x
+    assert grouped(**ids, **packed, lora_a=4096, lora_b=4096, rank=64) == ERR_INVALID_ARG  # LoRA needs bf16 X
+    assert grouped(**ids, **bf16, out_dtype=7) == ERR_INVALID_ARG                # unknown output dtype
+    for form in (dict(**ids, **bf16), dict(**given, **packed), dict(**ids, **packed, x_bf16=4096,
+                 lora_a=4096, lora_b=4096, rank=64), dict(**given, **bf16, out_dtype=OUT_FP32)):
+        assert grouped(**form) != ERR_INVALID_ARG, form

@@ -131,3 +131,10 @@ def test_moe_down_full_size_sampled():
     assert bad.size == 0, (f"{bad.shape[0]} of {err.size} outside tolerance; first {bad[:3].tolist()} "
                            f"err {err[tuple(bad[0])]:.4g} tol {tol[tuple(bad[0])]:.4g}")
     assert len(tokens) >= 10 and counts[heavy[0]] > 1000 and len(single) >= 1
+
+
+def test_moe_down_single_expert_top1():
+    """Degenerate routing: top-1, every token on one expert, 15 experts empty."""
+    c = make_case("moe_down", T=300, E=16, topk=1, N=256, K=512, rank=32)
+    c["expert_ids"] = np.full((300, 1), 3, np.int32)
+    run_case(c, True)
