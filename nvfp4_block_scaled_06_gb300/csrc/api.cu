@@ -195,6 +195,21 @@ bool map2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t in
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The pair kernel's bf16 output leaves through tensor stores of 32 x 32 boxes
+// (64-byte swizzle) when D's base and pitch allow a tensor map; otherwise its
+// epilogue threads store their rows directly.
+void map_pair_d(GemmMaps *maps, GemmParams *p) {
+  maps->has_d = false;
+  p->store_tma = 0;
+  if (p->out_fp32 || p->ksplit > 1 || p->M < 32 || p->N < 32) return;
+  if ((reinterpret_cast<uintptr_t>(p->d) & 15) != 0 || (p->ldd * 2) % 16 != 0) return;
+  if (!make_map_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->d, p->N, p->M, p->ldd * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B))
+    return;
+  maps->has_d = true;
+  p->store_tma = 1;
+}
+
 int pick_bn(int64_t M, int64_t N, int sms) {
   if (N <= 128) return 128;
   const int64_t t256 = ceil_div(M, 128) * ceil_div(N, 256);
@@ -435,7 +450,10 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
-  if (pl.pair) p.tiles_n = (int)ceil_div(a->N, 256);
+  if (pl.pair) {
+    p.tiles_n = (int)ceil_div(a->N, 256);
+    map_pair_d(&maps, &p);
+  }
   if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = pl.pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess && pl.ksplit > 1) e = launch_splitk_reduce(p, sms, st);
@@ -982,6 +1000,7 @@ nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, i
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
+  if (pair) map_pair_d(&maps, &p);
   if (cudaError_t e_ = mark(prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess) e = mark(prof_end, st);

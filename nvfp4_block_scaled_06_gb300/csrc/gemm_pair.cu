@@ -55,7 +55,10 @@ constexpr int kPSfaBytes = 4 * 512;            // 128 A rows x 16 scales (four 1
 constexpr int kPSfbBytes = 2 * 4 * 512;        // 256 B rows x 16 scales (two 128-row chunks)
 constexpr int kPStageBytes = kPABytes + kPBBytes + kPSfaBytes + kPSfbBytes;
 constexpr int kPBarBytes = 256;
-constexpr int kPSmemBytes = kPairStages * kPStageBytes + kPBarBytes + 1024;
+// epilogue staging for the bf16 output's tensor stores: per epilogue warp two
+// 32 x 32 bf16 boxes (2 KB each), 1024-aligned
+constexpr int kPStgBytes = 4 * 2 * 2048;
+constexpr int kPSmemBytes = kPairStages * kPStageBytes + kPBarBytes + 1024 + kPStgBytes + 1024;
 // TMEM columns of one stage's scales: 4 per K step for A, then 8 per K step
 // for B.  The MMA of K step j reads the A scale of row r from lane r, column
 // base + 4j + r/32, so lane quarter q needs only column base + 4j + q (one
@@ -108,7 +111,7 @@ __device__ __forceinline__ void pair_abort(volatile int *abort_flag, int *status
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     k_gemm_fp4_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmLB,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   constexpr int S = kPairStages;
 #ifdef NVFP4_WAIT_STATS
   const long long kernel_t0 = clock64();
@@ -121,6 +124,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint8_t *sSFA = sB + S * kPBBytes;
   uint8_t *sSFB = sSFA + S * kPSfaBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sSFB + S * kPSfbBytes);
+  uint8_t *stg = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bars) + kPBarBytes + 1023) &
+                                             ~uintptr_t(1023));
   // full (the leader's copy): both CTAs' A and B tiles landed -- the peer's
   // tile loads complete on the leader's barrier; sf_full: this CTA's scales
   // landed (small copies, so the scale warps fill tensor memory while the
@@ -391,6 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
+    int sbuf = 0;   // this warp's staging buffer for the next box
     const float alpha = acc_scale_of(p.g_a ? *p.g_a : 1.0f, p.g_b ? *p.g_b : 1.0f);
     for (int u = pair; u < num_tiles; u += npairs) {
       const PairTile t = pair_tile(p, u, tiles_m2);
@@ -418,6 +424,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_l);
+        }
+        if (p.store_tma) {
+          // bf16 through shared memory: row `lane` of a 32 x 32 box, its four
+          // 16-byte chunks at their 64-byte-swizzle positions (conflict-free),
+          // then one tensor store per box; rows and columns outside D are not
+          // written by the store
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int64_t n = t.n0 + (half * 4 + c) * 32;
+            if (n >= p.N) break;
+            uint32_t w[16];
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][2 * i2]), alpha),
+                                                              __fmul_rn(__uint_as_float(v[c][2 * i2 + 1]), alpha));
+              w[i2] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+            if (lane == 0) bulk_wait_group_read<1>();   // the store issued from this buffer two boxes ago has read it
+            __syncwarp();
+            const uint32_t buf = smem_u32(stg) + (uint32_t)(q * 4096 + sbuf * 2048);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              sts128(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2],
+                     w[4 * k + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmD, buf, (int32_t)n, (int32_t)(t.m0 + 128 * rank + 32 * q));
+              bulk_commit_group();
+            }
+            sbuf ^= 1;
+          }
+          continue;
         }
         if (!row_ok) continue;
 #pragma unroll
@@ -469,6 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       }
       acc_phase ^= 1;
     }
+    // every tensor store of this warp has written D before the CTA exits
+    if (p.store_tma && lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
   __syncthreads();
 #ifdef NVFP4_WAIT_STATS
@@ -513,8 +555,10 @@ cudaError_t launch_gemm_fp4_pair(const GemmParams &p, const GemmMaps &m, int num
   const int64_t tiles = ((p.M + 255) / 256) * (int64_t)p.tiles_n;
   int64_t pairs = std::min<int64_t>(tiles, resident_pairs(num_sms));
   if (pairs <= 0) return cudaSuccess;
+  GemmParams q = p;
+  q.store_tma = p.store_tma && m.has_d;
   return launch_pdl(k_gemm_fp4_pair, dim3((unsigned)(2 * pairs)), dim3(kPairThreads), kPSmemBytes, st, m.a, m.b, m.t,
-                    m.lb, p);
+                    m.lb, m.has_d ? m.d : m.a, q);
 }
 
 }  // namespace nvfp4

@@ -97,10 +97,13 @@ struct GemmParams {
   int *status;
   uint64_t timeout_ns;
   int stall_probe;            // test hook: first wait on a barrier nothing arrives at
+  int store_tma;              // pair kernel, bf16 output: D leaves through GemmMaps::d
 };
 
 struct GemmMaps {
   CUtensorMap a, b, t, lb;
+  CUtensorMap d;   // pair kernel, bf16 output: D [M][ldd] in 32 x 32 boxes, 64-byte swizzle
+  bool has_d = false;
 };
 
 cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, int num_sms,
