@@ -127,10 +127,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint8_t *stg = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(bars) + kPBarBytes + 1023) &
                                              ~uintptr_t(1023));
   // full (the leader's copy): both CTAs' A and B tiles landed -- the peer's
-  // tile loads complete on the leader's barrier; sf_full: this CTA's scales
+  // tile loads complete on the leader's barrier -- and both CTAs' scale warps
+  // have written the stage's scales into tensor memory; sf_full: this CTA's scales
   // landed (small copies, so the scale warps fill tensor memory while the
   // tiles are still in flight)
-  uint64_t *full = bars, *empty = bars + S, *sfready = bars + 2 * S, *sf_full = bars + 3 * S;
+  uint64_t *full = bars, *empty = bars + S, *sf_full = bars + 3 * S;
   uint64_t *acc_full = bars + 4 * S, *acc_empty = acc_full + 1, *drain = acc_full + 2;
   uint64_t *never = acc_full + 3;          // test hook: a barrier nothing arrives at
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 4);
@@ -140,9 +141,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const uint32_t rank = cluster_ctarank();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 2);            // the leader's A and B producers (bytes of both CTAs)
+      // the leader's A and B producers (with the bytes of both CTAs) and the
+      // scale warps of both CTAs: the MMA thread waits on one barrier a stage
+      mbar_init(&full[s], 2 + 2 * 4);
       mbar_init(&empty[s], 1);
-      mbar_init(&sfready[s], 2 * 4);     // the scale warps of both CTAs (leader's copy used)
       mbar_init(&sf_full[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -177,7 +179,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int a_sf_chunks = (int)((p.M + 127) / 128);
   // the leader's barriers as cluster addresses (for the peer: its remote copy)
-  const uint32_t sfready_l = mapa_shared(smem_u32(sfready), 0);
   const uint32_t full_l = mapa_shared(smem_u32(full), 0);
   const uint32_t acc_empty_l = mapa_shared(smem_u32(acc_empty), 0);
 
@@ -260,10 +261,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint32_t idesc = idesc_nvfp4(256, 256);
       const uint32_t idesc_l = idesc_bf16(256, 256);
       const uint64_t adesc0 = sdesc_k_sw128(sA), bdesc0 = sdesc_k_sw128(sB);
-      const uint32_t sfr_base = smem_u32(sfready), empty_base = smem_u32(empty);
+      const uint32_t empty_base = smem_u32(empty);
       const uint32_t full_base = smem_u32(full);
       const uint32_t accf = smem_u32(acc_full), acce = smem_u32(acc_empty);
       const int last_nk = p.num_kt ? p.nk64 - (p.num_kt - 1) * 4 : 0;
+      const int nsteps = p.num_kt + p.lora_steps;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -271,6 +273,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         pair_abort(abort_flag, p.status);   // expected: the expiry path under test
         ok = false;
       }
+      // The issuing thread, not the tensor pipe, sets the pace: each MMA
+      // instruction and each iteration's waits, commit and loop control cost
+      // it tens to hundreds of cycles.  So one iteration takes two stages:
+      // both stages' barriers are waited first (one barrier per stage: the
+      // tiles and the scales), then the eight MMAs go out back to back with
+      // a commit after each stage's four, and no flag is read per stage.
+      auto issue_stage = [&](int st, int i, uint32_t &accumulate) {
+        const uint64_t adesc = adesc0 + (uint64_t)((st * kPABytes) >> 4);
+        const uint64_t bdesc = bdesc0 + (uint64_t)((st * kPBBytes) >> 4);
+        if (i < p.num_kt) {
+          const int nk = i == p.num_kt - 1 ? last_nk : 4;
+          const uint32_t sfa_col = tmem + 256 + st * kPSfCols;
+          const uint32_t sfb_col = sfa_col + kPSfaCols;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < nk) {
+              tc_mma_nvfp4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col + 4 * j, sfb_col + 8 * j,
+                                accumulate);
+              accumulate = 1;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_mma_bf16_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_l, accumulate);
+            accumulate = 1;
+          }
+        }
+        tc_commit_pair_mc(empty_base + 8 * st, 3);   // frees the stage in both CTAs
+      };
       for (int u = pair; ok && u < num_tiles; u += npairs) {
         PSTAT_T0();
         const bool got_acc = !*abort_flag && mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns);
@@ -281,13 +313,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         uint32_t accumulate = 0;
-        const int nsteps = p.num_kt + p.lora_steps;
-        for (int i = 0; i < nsteps; ++i) {
-          // this stage's operands have landed in both CTAs and both CTAs'
-          // scales are in tensor memory
+        for (int i = 0; i < nsteps; i += 2) {
+          const int stage1 = stage + 1 == S ? 0 : stage + 1;
+          const uint32_t phase1 = stage + 1 == S ? phase ^ 1 : phase;
+          const bool two = i + 1 < nsteps;
           PSTAT_T0();
-          const bool got = !*abort_flag && mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns) &&
-                           mbar_wait_u(sfr_base + 8 * stage, phase, p.timeout_ns);
+          const bool got = mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns) &&
+                           (!two || mbar_wait_u(full_base + 8 * stage1, phase1, p.timeout_ns));
           PSTAT_ADD(p, rank, 1);
           if (!got) {
             pair_abort(abort_flag, p.status);
@@ -295,31 +327,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = adesc0 + (uint64_t)((stage * kPABytes) >> 4);
-          const uint64_t bdesc = bdesc0 + (uint64_t)((stage * kPBBytes) >> 4);
-          if (i < p.num_kt) {
-            const int nk = i == p.num_kt - 1 ? last_nk : 4;
-            const uint32_t sfa_col = tmem + 256 + stage * kPSfCols;
-            const uint32_t sfb_col = sfa_col + kPSfaCols;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (j < nk) {
-                tc_mma_nvfp4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col + 4 * j, sfb_col + 8 * j,
-                                  accumulate);
-                accumulate = 1;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              tc_mma_bf16_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc_l, accumulate);
-              accumulate = 1;
-            }
-          }
-          tc_commit_pair_mc(empty_base + 8 * stage, 3);   // frees the stage in both CTAs
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+          issue_stage(stage, i, accumulate);
+          stage = stage1;
+          phase = phase1;
+          if (two) {
+            issue_stage(stage, i + 1, accumulate);
+            phase = stage + 1 == S ? phase ^ 1 : phase;
+            stage = stage + 1 == S ? 0 : stage + 1;
           }
         }
         if (!ok) break;
@@ -380,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           break;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(sfready_l + 8 * stage);
+        if (lane == 0) mbar_arrive_cluster(full_l + 8 * stage);
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
