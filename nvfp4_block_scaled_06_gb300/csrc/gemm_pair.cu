@@ -303,6 +303,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_commit_pair_mc(empty_base + 8 * st, 3);   // frees the stage in both CTAs
       };
+      // one stage with all four K steps of FP4 (the first MMA accumulates
+      // when `acc_first` is set)
+      auto issue_full = [&](int st, uint32_t acc_first) {
+        const uint64_t adesc = adesc0 + (uint64_t)((st * kPABytes) >> 4);
+        const uint64_t bdesc = bdesc0 + (uint64_t)((st * kPBBytes) >> 4);
+        const uint32_t sfa_col = tmem + 256 + st * kPSfCols;
+        const uint32_t sfb_col = sfa_col + kPSfaCols;
+        tc_mma_nvfp4_pair(tmem, adesc, bdesc, idesc, sfa_col, sfb_col, acc_first);
+#pragma unroll
+        for (int j = 1; j < 4; ++j)
+          tc_mma_nvfp4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, idesc, sfa_col + 4 * j, sfb_col + 8 * j, 1u);
+        tc_commit_pair_mc(empty_base + 8 * st, 3);   // frees the stage in both CTAs
+      };
+      const int nfull = p.num_kt - (last_nk < 4 ? 1 : 0);
       for (int u = pair; ok && u < num_tiles; u += npairs) {
         PSTAT_T0();
         const bool got_acc = !*abort_flag && mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns);
@@ -313,7 +327,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         uint32_t accumulate = 0;
-        for (int i = 0; i < nsteps; i += 2) {
+        // pairs of full FP4 stages (all four K steps present), then the rest
+        // (a partial last FP4 stage, the LoRA stages, bf16-only products) in
+        // pairs of any kind
+        int i = 0;
+        for (; i + 2 <= nfull; i += 2) {
+          const int stage1 = stage + 1 == S ? 0 : stage + 1;
+          const uint32_t phase1 = stage + 1 == S ? phase ^ 1 : phase;
+          PSTAT_T0();
+          const bool got = mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns) &&
+                           mbar_wait_u(full_base + 8 * stage1, phase1, p.timeout_ns);
+          PSTAT_ADD(p, rank, 1);
+          if (!got) {
+            pair_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_full(stage, accumulate);
+          issue_full(stage1, 1);
+          accumulate = 1;
+          phase = stage1 + 1 == S ? phase1 ^ 1 : phase1;
+          stage = stage1 + 1 == S ? 0 : stage1 + 1;
+        }
+        for (; ok && i < nsteps; i += 2) {
           const int stage1 = stage + 1 == S ? 0 : stage + 1;
           const uint32_t phase1 = stage + 1 == S ? phase ^ 1 : phase;
           const bool two = i + 1 < nsteps;
