@@ -55,9 +55,9 @@ constexpr int kPSfaBytes = 4 * 512;            // 128 A rows x 16 scales (four 1
 constexpr int kPSfbBytes = 2 * 4 * 512;        // 256 B rows x 16 scales (two 128-row chunks)
 constexpr int kPStageBytes = kPABytes + kPBBytes + kPSfaBytes + kPSfbBytes;
 constexpr int kPBarBytes = 256;
-// epilogue staging for the bf16 output's tensor stores: per epilogue warp two
+// epilogue staging for the bf16 output's tensor stores: per epilogue warp four
 // 32 x 32 bf16 boxes (2 KB each), 1024-aligned
-constexpr int kPStgBytes = 4 * 2 * 2048;
+constexpr int kPStgBytes = 4 * 4 * 2048;
 constexpr int kPSmemBytes = kPairStages * kPStageBytes + kPBarBytes + 1024 + kPStgBytes + 1024;
 // TMEM columns of one stage's scales: 4 per K step for A, then 8 per K step
 // for B.  The MMA of K step j reads the A scale of row r from lane r, column
@@ -447,7 +447,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
-    int sbuf = 0;   // this warp's staging buffer for the next box
     const float alpha = acc_scale_of(p.g_a ? *p.g_a : 1.0f, p.g_b ? *p.g_b : 1.0f);
     for (int u = pair; u < num_tiles; u += npairs) {
       const PairTile t = pair_tile(p, u, tiles_m2);
@@ -477,35 +476,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0) mbar_arrive_cluster(acc_empty_l);
         }
         if (p.store_tma) {
-          // bf16 through shared memory: row `lane` of a 32 x 32 box, its four
-          // 16-byte chunks at their 64-byte-swizzle positions (conflict-free),
-          // then one tensor store per box; rows and columns outside D are not
-          // written by the store
+          // bf16 through shared memory: this warp's four 32 x 32 boxes take
+          // the half's four column chunks (row `lane` of each, its 16-byte
+          // pieces at their 64-byte-swizzle positions: conflict-free), then
+          // one fence and one lane issues the four tensor stores, which leave
+          // out rows and columns outside D.  Half 0 goes out before half 1 is
+          // loaded, so the accumulator is released after one pass of stores.
+          if (lane == 0) bulk_wait_group_read<0>();   // the boxes' previous stores have read them
+          __syncwarp();
+          const uint32_t box0 = smem_u32(stg) + (uint32_t)(q * 4 * 2048);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int64_t n = t.n0 + (half * 4 + c) * 32;
-            if (n >= p.N) break;
-            uint32_t w[16];
+            if (t.n0 + (half * 4 + c) * 32 < p.N) {
+              uint32_t w[16];
 #pragma unroll
-            for (int i2 = 0; i2 < 16; ++i2) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][2 * i2]), alpha),
-                                                              __fmul_rn(__uint_as_float(v[c][2 * i2 + 1]), alpha));
-              w[i2] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-            if (lane == 0) bulk_wait_group_read<1>();   // the store issued from this buffer two boxes ago has read it
-            __syncwarp();
-            const uint32_t buf = smem_u32(stg) + (uint32_t)(q * 4096 + sbuf * 2048);
+              for (int i2 = 0; i2 < 16; ++i2) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[c][2 * i2]), alpha),
+                                                                __fmul_rn(__uint_as_float(v[c][2 * i2 + 1]), alpha));
+                w[i2] = *reinterpret_cast<const uint32_t *>(&h2);
+              }
+              const uint32_t row = box0 + (uint32_t)(c * 2048 + lane * 64);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              sts128(buf + lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2],
-                     w[4 * k + 3]);
-            fence_proxy_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmD, buf, (int32_t)n, (int32_t)(t.m0 + 128 * rank + 32 * q));
-              bulk_commit_group();
+              for (int k = 0; k < 4; ++k)
+                sts128(row + ((k ^ ((lane >> 1) & 3)) << 4), w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
             }
-            sbuf ^= 1;
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int64_t n = t.n0 + (half * 4 + c) * 32;
+              if (n < p.N) tma_store_2d(&tmD, box0 + (uint32_t)(c * 2048), (int32_t)n, (int32_t)(t.m0 + 128 * rank + 32 * q));
+            }
+            bulk_commit_group();
           }
           continue;
         }
