@@ -335,8 +335,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const int stage1 = stage + 1 == S ? 0 : stage + 1;
           const uint32_t phase1 = stage + 1 == S ? phase ^ 1 : phase;
           PSTAT_T0();
-          const bool got = mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns) &&
-                           mbar_wait_u(full_base + 8 * stage1, phase1, p.timeout_ns);
+          bool got = mbar_wait_u(full_base + 8 * stage, phase, p.timeout_ns);
           PSTAT_ADD(p, rank, 1);
           if (!got) {
             pair_abort(abort_flag, p.status);
@@ -345,8 +344,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           tc_fence_after();
           issue_full(stage, accumulate);
-          issue_full(stage1, 1);
           accumulate = 1;
+          // the second stage's wait comes after the first stage's MMAs: the
+          // stage it needs was freed by MMAs issued four stages back
+          got = mbar_wait_u(full_base + 8 * stage1, phase1, p.timeout_ns);
+          if (!got) {
+            phase = phase1;
+            stage = stage1;
+            pair_abort(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_full(stage1, 1);
           phase = stage1 + 1 == S ? phase1 ^ 1 : phase1;
           stage = stage1 + 1 == S ? 0 : stage1 + 1;
         }
