@@ -588,6 +588,141 @@ __device__ __forceinline__ void store_blocks4(uint8_t *dst, const uint64_t (&cd)
   }
 }
 
+// Destinations of one matrix's packings (row: [rows][cols/2] codes; column:
+// [cols][rows/2]) and their scale layouts.
+struct TileOut {
+  uint8_t *codes_r, *sf_r, *codes_c, *sf_c;
+  int32_t rows, cols, nblk_r, sfc_pad_r, nblk_c, sfc_pad_c;
+  bool do_row, do_col;
+};
+
+__device__ __forceinline__ TileOut tile_out(const QuantParams &p, int64_t b) {
+  TileOut o;
+  o.rows = (int32_t)p.rows;
+  o.cols = (int32_t)p.cols;
+  o.do_row = p.codes_row != nullptr;
+  o.do_col = p.codes_col != nullptr;
+  o.nblk_r = o.cols / 16;
+  o.sfc_pad_r = (o.nblk_r + 3) & ~3;
+  o.nblk_c = o.rows / 16;
+  o.sfc_pad_c = (o.nblk_c + 3) & ~3;
+  o.codes_r = o.do_row ? p.codes_row + b * p.codes_row_bstride : nullptr;
+  o.sf_r = o.do_row ? p.sf_row + b * p.sf_row_bstride : nullptr;
+  o.codes_c = o.do_col ? p.codes_col + b * p.codes_col_bstride : nullptr;
+  o.sf_c = o.do_col ? p.sf_col + b * p.sf_col_bstride : nullptr;
+  return o;
+}
+
+// Both packings of one staged [kTR][kTC] bf16 tile whose first element is
+// (r0, c0).  Thread t has the row role (tile row t / 4, 64-column quarter
+// t % 4) and the column role (column pair t / 2, 32-row half t % 2).
+__device__ __forceinline__ void pack_tile(const QuantParams &p, const BlockScale &s, const uint32_t *tile,
+                                          int32_t r0, int32_t c0, const TileOut &o, int t) {
+  const int32_t rows = o.rows, cols = o.cols;
+  const int rr = t >> 2, qd = t & 3;          // row role: tile row, 64-column quarter
+  const int cp = t >> 1, rh = t & 1;          // column role: column pair, 32-row half
+  if (o.do_row) {
+    const int32_t gr = r0 + rr, gq = c0 + 64 * qd;   // this thread's row and first column
+    if (gr < rows) {
+      // the 16-byte pairs are read in an order rotated by the quarter, so
+      // that the four quarters of a row hit different bank groups: w-block
+      // m holds block (m + qd) % 4 of the quarter
+      uint32_t w[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = (k + 2 * qd) & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr * (kTC / 2) + 32 * qd + 4 * c]);
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+      }
+      const int nvalid = min(4, (cols - gq) / 16);
+      uint64_t cm[4];
+      uint32_t sm[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t(&wb)[8] = *reinterpret_cast<const uint32_t(*)[8]>(&w[8 * m]);
+        sm[m] = 0;
+        cm[m] = ((m + qd) & 3) < nvalid ? quant16_abs(wb, s, sm[m]) : 0ull;
+      }
+      // back to block order j = 0..3 (w-block (j - qd) % 4)
+      uint64_t cd[4];
+      uint32_t sbw = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int m0 = (j - qd) & 3;
+        cd[j] = m0 == 0 ? cm[0] : m0 == 1 ? cm[1] : m0 == 2 ? cm[2] : cm[3];
+        sbw |= (m0 == 0 ? sm[0] : m0 == 1 ? sm[1] : m0 == 2 ? sm[2] : sm[3]) << (8 * j);
+      }
+      store_blocks4(o.codes_r + (int64_t)gr * (cols / 2) + gq / 2, cd, nvalid);
+      const int32_t blk = gq / 16;
+      if (p.sf_swizzled) {
+        if (blk < o.sfc_pad_r) *reinterpret_cast<uint32_t *>(o.sf_r + sf_swz_offset(gr, blk, o.sfc_pad_r)) = sbw;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nvalid) o.sf_r[(int64_t)gr * o.nblk_r + blk + j] = (uint8_t)(sbw >> (8 * j));
+      }
+    }
+  }
+  if (o.do_col) {
+    // rows 32*rh .. 32*rh+31 of columns 2cp, 2cp+1: blocks 2rh, 2rh+1 of each
+    uint64_t cda[2], cdb[2];
+    uint32_t sba[2], sbb[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int rb = 2 * rh + h2;               // 16-row block of the tile
+      uint32_t ca[8], cb[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w0 = tile[(16 * rb + 2 * i) * (kTC / 2) + cp];
+        const uint32_t w1 = tile[(16 * rb + 2 * i + 1) * (kTC / 2) + cp];
+        ca[i] = __byte_perm(w0, w1, 0x5410);   // column 2cp: rows 2i, 2i+1
+        cb[i] = __byte_perm(w0, w1, 0x7632);   // column 2cp+1
+      }
+      const bool bin = r0 + 16 * rb < rows;
+      sba[h2] = sbb[h2] = 0;
+      cda[h2] = (bin && c0 + 2 * cp < cols) ? quant16_abs(ca, s, sba[h2]) : 0ull;
+      cdb[h2] = (bin && c0 + 2 * cp + 1 < cols) ? quant16_abs(cb, s, sbb[h2]) : 0ull;
+    }
+    // lane rh = 0 keeps column 2cp and receives its blocks 2, 3; lane rh = 1
+    // keeps column 2cp+1 and receives its blocks 0, 1
+    uint64_t keep[2], give[2];
+    uint32_t skeep[2], sgive[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      keep[h2] = rh ? cdb[h2] : cda[h2];
+      give[h2] = rh ? cda[h2] : cdb[h2];
+      skeep[h2] = rh ? sbb[h2] : sba[h2];
+      sgive[h2] = rh ? sba[h2] : sbb[h2];
+    }
+    uint64_t got2[2];
+    uint32_t sgot[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)give[h2], 1);
+      const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(give[h2] >> 32), 1);
+      got2[h2] = ((uint64_t)hi << 32) | lo;
+      sgot[h2] = __shfl_xor_sync(0xffffffffu, sgive[h2], 1);
+    }
+    const int32_t oc = c0 + 2 * cp + rh;        // this thread's output row (= input column)
+    if (oc < cols) {
+      const uint64_t cd[4] = {rh ? got2[0] : keep[0], rh ? got2[1] : keep[1], rh ? keep[0] : got2[0],
+                              rh ? keep[1] : got2[1]};
+      const uint32_t sbw = (rh ? sgot[0] : skeep[0]) | ((rh ? sgot[1] : skeep[1]) << 8) |
+                           ((rh ? skeep[0] : sgot[0]) << 16) | ((rh ? skeep[1] : sgot[1]) << 24);
+      const int nvalid = min(4, (rows - r0) / 16);
+      store_blocks4(o.codes_c + (int64_t)oc * (rows / 2) + r0 / 2, cd, nvalid);
+      const int32_t blk = r0 / 16;              // first of the tile's 4 column blocks
+      if (p.sf_swizzled) {
+        if (blk < o.sfc_pad_c) *reinterpret_cast<uint32_t *>(o.sf_c + sf_swz_offset(oc, blk, o.sfc_pad_c)) = sbw;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < nvalid) o.sf_c[(int64_t)oc * o.nblk_c + blk + j] = (uint8_t)(sbw >> (8 * j));
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const __grid_constant__ CUtensorMap tm) {
   griddep_launch_dependents();
   griddep_wait();   // inputs may come from the previous kernel in the stream
@@ -616,15 +751,7 @@ __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const 
   const int32_t rows = (int32_t)p.rows, cols = (int32_t)p.cols;
   const int32_t tiles_r = (rows + kTR - 1) / kTR, tiles_c = (cols + kTC - 1) / kTC;
   const int32_t ntiles = tiles_r * tiles_c;
-  const bool do_row = p.codes_row != nullptr, do_col = p.codes_col != nullptr;
-  const int32_t nblk_r = cols / 16, sfc_pad_r = (nblk_r + 3) & ~3;
-  const int32_t nblk_c = rows / 16, sfc_pad_c = (nblk_c + 3) & ~3;
-  uint8_t *codes_r = do_row ? p.codes_row + (int64_t)b * p.codes_row_bstride : nullptr;
-  uint8_t *sf_r = do_row ? p.sf_row + (int64_t)b * p.sf_row_bstride : nullptr;
-  uint8_t *codes_c = do_col ? p.codes_col + (int64_t)b * p.codes_col_bstride : nullptr;
-  uint8_t *sf_c = do_col ? p.sf_col + (int64_t)b * p.sf_col_bstride : nullptr;
-  const int rr = t >> 2, qd = t & 3;          // row role: tile row, 64-column quarter
-  const int cp = t >> 1, rh = t & 1;          // column role: column pair, 32-row half
+  const TileOut o = tile_out(p, b);
 
   // tile it of this CTA -> buffer it % 2 (thread 0)
   int32_t issued = 0;
@@ -653,106 +780,7 @@ __global__ void __launch_bounds__(256) k_quant_tiles(const QuantParams p, const 
     const uint32_t *tile = reinterpret_cast<const uint32_t *>(qts + buf * kTileBytes);   // [kTR][kTC/2] words
     const int32_t tr = tix / tiles_c;
     const int32_t r0 = tr * kTR, c0 = (tix - tr * tiles_c) * kTC;
-    if (do_row) {
-      const int32_t gr = r0 + rr, gq = c0 + 64 * qd;   // this thread's row and first column
-      if (gr < rows) {
-        // the 16-byte pairs are read in an order rotated by the quarter, so
-        // that the four quarters of a row hit different bank groups: w-block
-        // m holds block (m + qd) % 4 of the quarter
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int c = (k + 2 * qd) & 7;
-          const uint4 v = *reinterpret_cast<const uint4 *>(&tile[rr * (kTC / 2) + 32 * qd + 4 * c]);
-          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-        }
-        const int nvalid = min(4, (cols - gq) / 16);
-        uint64_t cm[4];
-        uint32_t sm[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t(&wb)[8] = *reinterpret_cast<const uint32_t(*)[8]>(&w[8 * m]);
-          sm[m] = 0;
-          cm[m] = ((m + qd) & 3) < nvalid ? quant16_abs(wb, s, sm[m]) : 0ull;
-        }
-        // back to block order j = 0..3 (w-block (j - qd) % 4)
-        uint64_t cd[4];
-        uint32_t sbw = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int m0 = (j - qd) & 3;
-          cd[j] = m0 == 0 ? cm[0] : m0 == 1 ? cm[1] : m0 == 2 ? cm[2] : cm[3];
-          sbw |= (m0 == 0 ? sm[0] : m0 == 1 ? sm[1] : m0 == 2 ? sm[2] : sm[3]) << (8 * j);
-        }
-        store_blocks4(codes_r + (int64_t)gr * (cols / 2) + gq / 2, cd, nvalid);
-        const int32_t blk = gq / 16;
-        if (p.sf_swizzled) {
-          if (blk < sfc_pad_r) *reinterpret_cast<uint32_t *>(sf_r + sf_swz_offset(gr, blk, sfc_pad_r)) = sbw;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < nvalid) sf_r[(int64_t)gr * nblk_r + blk + j] = (uint8_t)(sbw >> (8 * j));
-        }
-      }
-    }
-    if (do_col) {
-      // rows 32*rh .. 32*rh+31 of columns 2cp, 2cp+1: blocks 2rh, 2rh+1 of each
-      uint64_t cda[2], cdb[2];
-      uint32_t sba[2], sbb[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int rb = 2 * rh + h2;               // 16-row block of the tile
-        uint32_t ca[8], cb[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w0 = tile[(16 * rb + 2 * i) * (kTC / 2) + cp];
-          const uint32_t w1 = tile[(16 * rb + 2 * i + 1) * (kTC / 2) + cp];
-          ca[i] = __byte_perm(w0, w1, 0x5410);   // column 2cp: rows 2i, 2i+1
-          cb[i] = __byte_perm(w0, w1, 0x7632);   // column 2cp+1
-        }
-        const bool bin = r0 + 16 * rb < rows;
-        sba[h2] = sbb[h2] = 0;
-        cda[h2] = (bin && c0 + 2 * cp < cols) ? quant16_abs(ca, s, sba[h2]) : 0ull;
-        cdb[h2] = (bin && c0 + 2 * cp + 1 < cols) ? quant16_abs(cb, s, sbb[h2]) : 0ull;
-      }
-      // lane rh = 0 keeps column 2cp and receives its blocks 2, 3; lane rh = 1
-      // keeps column 2cp+1 and receives its blocks 0, 1
-      uint64_t keep[2], give[2];
-      uint32_t skeep[2], sgive[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        keep[h2] = rh ? cdb[h2] : cda[h2];
-        give[h2] = rh ? cda[h2] : cdb[h2];
-        skeep[h2] = rh ? sbb[h2] : sba[h2];
-        sgive[h2] = rh ? sba[h2] : sbb[h2];
-      }
-      uint64_t got2[2];
-      uint32_t sgot[2];
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)give[h2], 1);
-        const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(give[h2] >> 32), 1);
-        got2[h2] = ((uint64_t)hi << 32) | lo;
-        sgot[h2] = __shfl_xor_sync(0xffffffffu, sgive[h2], 1);
-      }
-      const int32_t oc = c0 + 2 * cp + rh;        // this thread's output row (= input column)
-      if (oc < cols) {
-        const uint64_t cd[4] = {rh ? got2[0] : keep[0], rh ? got2[1] : keep[1], rh ? keep[0] : got2[0],
-                                rh ? keep[1] : got2[1]};
-        const uint32_t sbw = (rh ? sgot[0] : skeep[0]) | ((rh ? sgot[1] : skeep[1]) << 8) |
-                             ((rh ? skeep[0] : sgot[0]) << 16) | ((rh ? skeep[1] : sgot[1]) << 24);
-        const int nvalid = min(4, (rows - r0) / 16);
-        store_blocks4(codes_c + (int64_t)oc * (rows / 2) + r0 / 2, cd, nvalid);
-        const int32_t blk = r0 / 16;              // first of the tile's 4 column blocks
-        if (p.sf_swizzled) {
-          if (blk < sfc_pad_c) *reinterpret_cast<uint32_t *>(sf_c + sf_swz_offset(oc, blk, sfc_pad_c)) = sbw;
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < nvalid) sf_c[(int64_t)oc * nblk_c + blk + j] = (uint8_t)(sbw >> (8 * j));
-        }
-      }
-    }
+    pack_tile(p, s, tile, r0, c0, o, t);
     __syncthreads();   // every read of this buffer is done
     if (t == 0) issue(it + 2);
   }
@@ -907,26 +935,18 @@ cudaError_t launch_quant_rows(const QuantParams &p, int num_sms, cudaStream_t st
   return launch_pdl(k_quant_rows<false>, grid, dim3(256), 0, st, p);
 }
 
-cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
-  // the source as [batch][rows][cols] bf16, one 256 x 64 x 1 box per tile
-  CUtensorMap tm;
+// The source as [batch][rows][cols] bf16, one kTC x kTR x 1 box per tile.
+static bool tiles_map(const QuantParams &p, CUtensorMap *tm) {
   const uint64_t dims[3] = {(uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)p.batch};
   const uint64_t bstride = p.batch > 1 ? (uint64_t)p.bstride : (uint64_t)p.rows * (uint64_t)p.ld;
   const uint64_t strides[2] = {(uint64_t)p.ld * 2, bstride * 2};
   const uint32_t box[3] = {kTC, kTR, 1};
-  if (!make_map_3d(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.src, dims, strides, box))
-    return cudaErrorInvalidValue;
-  if (cudaError_t e = ensure_dynamic_smem((const void *)k_quant_tiles, 2 * kTileBytes); e != cudaSuccess) return e;
-  const int64_t tiles = ((p.rows + kTR - 1) / kTR) * ((p.cols + kTC - 1) / kTC);
-  int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 2 * kTileBytes);
-  per_sm = std::max(per_sm, 1);
-  // one wave of resident CTAs, shared by the matrices of the batch
-  int64_t ctas = std::min<int64_t>(tiles, std::max<int64_t>(1, (int64_t)num_sms * per_sm / std::max<int64_t>(1, p.batch)));
-  dim3 grid((unsigned)ctas, (unsigned)p.batch);
-  cudaError_t e = launch_pdl(k_quant_tiles, grid, dim3(256), 2 * kTileBytes, st, p, tm);
-  if (e != cudaSuccess || !p.sf_swizzled) return e;
-  // rows beyond the matrix inside the last 128-row atom
+  return make_map_3d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.src, dims, strides, box);
+}
+
+// Swizzled scales: rows beyond the matrix inside the last 128-row atom.
+static cudaError_t zero_pad_rows(const QuantParams &p, cudaStream_t st) {
+  if (!p.sf_swizzled) return cudaSuccess;
   if (p.codes_row && (p.rows % 128) != 0) {
     if (cudaError_t e2 = launch_pdl(k_zero_sf_pad_rows, dim3(4, (unsigned)p.batch), dim3(256), 0, st, p.sf_row,
                                     p.sf_row_bstride, p.rows, p.cols / 16);
@@ -940,6 +960,22 @@ cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t s
       return e2;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_quant_tiles(const QuantParams &p, int num_sms, cudaStream_t st) {
+  CUtensorMap tm;
+  if (!tiles_map(p, &tm)) return cudaErrorInvalidValue;
+  if (cudaError_t e = ensure_dynamic_smem((const void *)k_quant_tiles, 2 * kTileBytes); e != cudaSuccess) return e;
+  const int64_t tiles = ((p.rows + kTR - 1) / kTR) * ((p.cols + kTC - 1) / kTC);
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quant_tiles, 256, 2 * kTileBytes);
+  per_sm = std::max(per_sm, 1);
+  // one wave of resident CTAs, shared by the matrices of the batch
+  int64_t ctas = std::min<int64_t>(tiles, std::max<int64_t>(1, (int64_t)num_sms * per_sm / std::max<int64_t>(1, p.batch)));
+  dim3 grid((unsigned)ctas, (unsigned)p.batch);
+  cudaError_t e = launch_pdl(k_quant_tiles, grid, dim3(256), 2 * kTileBytes, st, p, tm);
+  if (e != cudaSuccess) return e;
+  return zero_pad_rows(p, st);
 }
 
 }  // namespace nvfp4

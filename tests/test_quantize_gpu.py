@@ -53,6 +53,24 @@ def test_expert_weights_batched_both(layout):
     check_quantize(w, "both", layout)
 
 
+@pytest.mark.parametrize("pack", ["col", "both"])
+def test_batched_dynamic_every_matrix(pack):
+    """A batch with dynamic scales and the column packing: every matrix's g,
+    codes and scales against the oracle.  Ragged tiles in both dimensions, a
+    different scale per matrix and the outlier of matrix b in a different tile
+    region each time, so that a maximum taken over the wrong matrix or a
+    missed region changes g."""
+    E, R, C = 9, 208, 1040
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((E, R, C)).astype(np.float32)
+    for b in range(E):
+        x[b] *= 0.05 * (b + 1)
+        x[b, (37 * b) % R, (211 * b + 5) % C] = 40.0 * (b + 2) * (-1) ** b
+    bits = f32_to_bf16_bits(x)
+    check_quantize(bits, pack, "swizzled")
+    check_quantize(bits, pack, "linear")
+
+
 @pytest.mark.parametrize("shape", [(16, 16), (1, 16), (300, 208), (144, 80), (48, 1040)])
 @pytest.mark.parametrize("pack", ["row", "both"])
 def test_ragged_shapes(shape, pack):
