@@ -71,6 +71,35 @@ def test_batched_dynamic_every_matrix(pack):
     check_quantize(bits, pack, "linear")
 
 
+@pytest.mark.parametrize("pack", ["row", "both"])
+def test_block_maxima_at_e4m3_rounding_ties(pack):
+    """Block maxima on every E4M3 value, on every midpoint between two
+    neighbours (exact ties of the scale's round-to-nearest-even), and one bf16
+    step either side of each midpoint.  The tensor maximum 448 gives
+    g = fl(448/2688) = fl(1/6) and fl(6 g) = 1 exactly, so each block's
+    quotient bamax / (6 g) is bamax itself and the ties are exact: the scale
+    codes near rounding boundaries, where a fast approximate quotient cannot
+    decide, are checked bit for bit against the oracle."""
+    v = o.E4M3_VALUES.astype(np.float64)
+    mids = (v[1:] + v[:-1]) / 2                      # exact in bf16 (four significant bits)
+    mb = f32_to_bf16_bits(mids.astype(np.float32)).astype(np.int64)
+    tb = np.concatenate([f32_to_bf16_bits(v[1:].astype(np.float32)).astype(np.int64), mb, mb - 1, mb + 1])
+    tvals = o.bf16_to_f32(tb.astype(np.uint16)).astype(np.float64)
+    nblk = len(tvals) + 1
+    cols = 512
+    rows = (nblk * 16 + cols - 1) // cols
+    rows = (rows + 15) // 16 * 16
+    rng = np.random.default_rng(5)
+    x = np.zeros(rows * cols, np.float64)
+    x[0] = 448.0                                     # block 0: the tensor maximum
+    for i, tv in enumerate(tvals):
+        blk = x[(i + 1) * 16:(i + 2) * 16]
+        blk[:] = rng.uniform(-1.0, 1.0, 16) * tv * 0.9
+        blk[rng.integers(16)] = tv * (1 if i % 2 else -1)
+    bits = f32_to_bf16_bits(x.reshape(rows, cols).astype(np.float32))
+    check_quantize(bits, pack, "linear")
+
+
 @pytest.mark.parametrize("shape", [(16, 16), (1, 16), (300, 208), (144, 80), (48, 1040)])
 @pytest.mark.parametrize("pack", ["row", "both"])
 def test_ragged_shapes(shape, pack):
