@@ -547,9 +547,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // stages in flight per thread; the A tiles still come by TMA.
 constexpr int kLoraStages = 6;
 constexpr int kLoraThreads = 192;
-// with the amax scan, warps 6..9 scan each stage's second X sub-tile (warps
-// 2..5 the first), so that the scan keeps up with the copies
-constexpr int kLoraScanThreads = 320;
 constexpr int kGatherThreads = 128;   // warps 2..5 gather X rows in grouped mode
 
 // A stage holds two 64-wide K sub-tiles: [X0 | X1 | A0 | A1], X tiles 128 rows x 128 B.
@@ -566,7 +563,7 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(int n) {
   return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256;
 }
 
-__global__ void __launch_bounds__(kLoraScanThreads, 1)
+__global__ void __launch_bounds__(kLoraThreads, 1)
     k_lora_down(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
                 const LoraDownParams p, int stages) {
   extern __shared__ uint8_t smem_raw[];
@@ -587,7 +584,7 @@ __global__ void __launch_bounds__(kLoraScanThreads, 1)
     for (int s = 0; s < stages; ++s) {
       // grouped: the producer's arrival + one per gathering thread
       mbar_init(&full[s], p.row_map ? 1 + kGatherThreads : 1);
-      mbar_init(&empty[s], scan ? 9 : 1);
+      mbar_init(&empty[s], scan ? 5 : 1);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
@@ -707,46 +704,6 @@ __global__ void __launch_bounds__(kLoraScanThreads, 1)
       tc_commit(drain);
       mbar_wait(drain, 0, kDrainNs);
     }
-  } else if (warp >= 6) {
-    // amax scan of every stage's second X sub-tile (rows as warps 2..5)
-    const int r = (warp & 3) * 32 + lane;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t m2 = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < num_tiles; u += gridDim.x) {
-      const int ks = u % ksplit;
-      const int kb = ks * k64_per, ke = min(p.num_k64, kb + k64_per);
-      const int nsteps = (ke - kb + kLoraSub - 1) / kLoraSub;
-      for (int st = 0; st < nsteps; ++st) {
-        if (!__all_sync(0xffffffffu, !*abort_flag && mbar_wait(&full[stage], phase, p.timeout_ns))) {
-          if (lane == 0) signal_abort(abort_flag, p.status);
-          ok = false;
-          break;
-        }
-        if (kb + st * kLoraSub + 1 < ke) {
-          const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + x_sub + r * 128);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 v = row[i ^ (r & 7)];   // conflict-free order on the swizzled rows
-            m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-            m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        if (++stage == stages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) atomicMax(amax_smem, m);
   } else {
     const int q = warp & 3;
     const int r = q * 32 + lane;
@@ -825,7 +782,7 @@ __global__ void __launch_bounds__(kLoraScanThreads, 1)
             break;
           }
           const int nsub = min(kLoraSub, ke - (kb + st * kLoraSub));
-          for (int j = 0; j < nsub && j < 1; ++j) {   // sub-tile 0 (warps 6..9: sub-tile 1)
+          for (int j = 0; j < nsub; ++j) {
             const uint4 *row = reinterpret_cast<const uint4 *>(base + stage * sbytes + j * x_sub + r * 128);
             // The tile is 128-byte swizzled (16-byte chunk c of row r sits at
             // c ^ (r & 7)); visiting chunks in the order i ^ (r & 7) makes the
@@ -1023,8 +980,7 @@ cudaError_t launch_lora_down(const LoraDownParams &p, const LoraDownMaps &m, int
   int grid = num_sms;
   if (!p.gtiles) grid = std::min(p.tiles_m * std::max(1, p.ksplit), num_sms);
   if (grid <= 0) return cudaSuccess;
-  const int threads = p.amax_part ? kLoraScanThreads : kLoraThreads;
-  return launch_pdl(k_lora_down, dim3(grid), dim3(threads), smem, st, m.x, m.a, p, stages);
+  return launch_pdl(k_lora_down, dim3(grid), dim3(kLoraThreads), smem, st, m.x, m.a, p, stages);
 }
 
 }  // namespace nvfp4
