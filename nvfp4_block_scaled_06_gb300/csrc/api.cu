@@ -196,12 +196,14 @@ bool map2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t in
 }
 
 // The pair kernel's bf16 output leaves through tensor stores of 32 x 32 boxes
-// (64-byte swizzle) when D's base and pitch allow a tensor map; otherwise its
-// epilogue threads store their rows directly.
+// (64-byte swizzle) when D's base and pitch allow a tensor map and its rows
+// end on a 16-byte boundary (a store clips the last box of a row only at 16
+// bytes: with N % 8 != 0 it would write up to 7 columns past N); otherwise
+// the epilogue threads store their rows directly.
 void map_pair_d(GemmMaps *maps, GemmParams *p) {
   maps->has_d = false;
   p->store_tma = 0;
-  if (p->out_fp32 || p->ksplit > 1 || p->M < 32 || p->N < 32) return;
+  if (p->out_fp32 || p->ksplit > 1 || p->M < 32 || p->N < 32 || p->N % 8 != 0) return;
   if ((reinterpret_cast<uintptr_t>(p->d) & 15) != 0 || (p->ldd * 2) % 16 != 0) return;
   if (!make_map_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p->d, p->N, p->M, p->ldd * 2, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B))

@@ -58,6 +58,27 @@ def test_ragged_gemm(M, N, K, out_dtype):
     assert_gemm_close(y, y_or, S, what=f"gemm {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(260, 333, 512), (512, 96, 256), (384, 1030, 768)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_pair_gemm_ragged_columns_and_padded_output(M, N, K, out_dtype):
+    """The CTA-pair GEMM (M >= 256) with N not a multiple of the 32-column
+    store boxes, written into an output whose rows are wider than N: every
+    element of the product within tolerance, the padding columns untouched."""
+    rng = np.random.default_rng(M * 7 + N)
+    xb = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wb = f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    xc, xs, xg = quant_dev(xb)
+    wc, ws, wg = quant_dev(wb)
+    pad = (8 - N % 8) % 8 + 8                      # row pitch a multiple of 8 elements
+    full = torch.full((M, N + pad), 7.0, dtype=out_dtype, device="cuda")
+    out = full[:, :N]
+    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg, out_dtype=out_dtype, out=out)
+    torch.cuda.synchronize()
+    y_or, S, _ = oracle_linear(xb, wb)
+    assert_gemm_close(y, y_or, S, what=f"pair gemm {M}x{N}x{K}")
+    assert torch.all(full[:, N:] == 7.0), "padding columns written"
+
+
 def test_bf16_input_dynamic_matches_packed_path():
     c = make_case("prefill", M=384, N=512, K=1024)
     wc, ws, wg = quant_dev(c["w"])
