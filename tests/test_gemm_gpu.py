@@ -79,6 +79,33 @@ def test_pair_gemm_ragged_columns_and_padded_output(M, N, K, out_dtype):
     assert torch.all(full[:, N:] == 7.0), "padding columns written"
 
 
+@pytest.mark.parametrize("M,N,K,static", [(1, 333, 2048, True), (3, 1030, 20480, True), (8, 333, 512, False),
+                                          (64, 1030, 4096, False), (32, 333, 16384, True)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_padded_output_rows_every_path(M, N, K, static, out_dtype):
+    """Outputs with rows wider than N on the other GEMM paths (CUDA-core GEMV
+    with one or several chunk passes, the 1-SM tcgen05 GEMM with and without
+    split K): the product within tolerance, the padding columns untouched."""
+    c = make_case("decode_q_b_proj", M=M, N=N, K=K)
+    wc, ws, wg = quant_dev(c["w"])
+    pad = (8 - N % 8) % 8 + 8
+    full = torch.full((M, N + pad), 7.0, dtype=out_dtype, device="cuda")
+    if static:
+        sx = 16.0 / 2688.0
+        gx = torch.tensor([sx], dtype=torch.float32, device="cuda")
+        nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx, out_dtype=out_dtype,
+                      out=full[:, :N])
+        y_or, S, _ = oracle_linear(c["x"], c["w"], xg=np.float32(sx))
+    else:
+        xc, xs, xg = quant_dev(c["x"])
+        nv.nvfp4_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg, out_dtype=out_dtype,
+                      out=full[:, :N])
+        y_or, S, _ = oracle_linear(c["x"], c["w"])
+    torch.cuda.synchronize()
+    assert_gemm_close(full[:, :N], y_or, S, what=f"padded {M}x{N}x{K}")
+    assert torch.all(full[:, N:] == 7.0), "padding columns written"
+
+
 def test_bf16_input_dynamic_matches_packed_path():
     c = make_case("prefill", M=384, N=512, K=1024)
     wc, ws, wg = quant_dev(c["w"])
