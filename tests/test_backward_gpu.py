@@ -129,3 +129,73 @@ def test_wgrad_static_scales():
     a = o.quantize_colwise(dy, gdy)
     b = o.quantize_colwise(x, gx)
     assert_gemm_close(dw, o.linear_fp64(a, b), o.error_scale(a, b), what="wgrad static")
+
+
+def _padded(rows, cols, pad, dtype, fill=7.0):
+    full = torch.full((rows, cols + pad), fill, dtype=dtype, device="cuda")
+    return full, full[:, :cols]
+
+
+def _strided_bf16(bits, pad):
+    """A device bf16 view of `bits` whose rows are `pad` elements wider (the
+    extra columns hold large values the call must not read)."""
+    R, C = bits.shape
+    big = np.full((R, C + pad), 0x4480, np.uint16)              # bf16 1024.0
+    big[:, :C] = bits
+    return dev_bf16(big)[:, :C]
+
+
+@pytest.mark.parametrize("transpose", [False, True])
+def test_dequantize_into_padded_rows(transpose):
+    R, C = 300, 192
+    rng = np.random.default_rng(77)
+    w = f32_to_bf16_bits((rng.standard_normal((R, C)) * 0.05).astype(np.float32))
+    codes, sf, g = o.quantize(w)
+    c, s, gg = upload_packed(codes, sf, g)
+    orows, ocols = (C, R) if transpose else (R, C)
+    full, out = _padded(orows, ocols, 8, torch.bfloat16)
+    nv.nvfp4_dequantize(c, s, gg, R, C, transpose=transpose, out=out)
+    torch.cuda.synchronize()
+    want = o.dequantize_bf16(codes, sf, g)
+    assert_bits_equal(host_bits(out.contiguous()), want.T if transpose else want, "padded dequant")
+    assert torch.all(full[:, ocols:] == 7.0), "padding columns written"
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("mode", ["bf16", "fp4"])
+def test_dgrad_strided_dy_padded_dx(mode, out_dtype):
+    """dY with rows wider than N (the extra columns must not be read) and dX
+    written into rows wider than K (the padding must not be written)."""
+    M, N, K = 300, 256, 640
+    c = make_case("dgrad", M=M, N=N, K=K)
+    dy = _strided_bf16(c["dy"], 16)
+    full, out = _padded(M, K, 8, out_dtype)
+    if mode == "bf16":
+        codes, sf, g = o.quantize(c["w"])
+        nv.nvfp4_dgrad(dy, N, K, w=upload_packed(codes, sf, g), out_dtype=out_dtype, out=out)
+        y_or, S = dgrad_oracle_bf16(c["dy"], codes, sf, g)
+    else:
+        col = nv.nvfp4_quantize(dev_bf16(c["w"]), pack="col", sf_layout="swizzled")
+        nv.nvfp4_dgrad(dy, N, K, wcol=(col["codes_col"][0], col["sf_col"][0], col["global_scale"]),
+                       out_dtype=out_dtype, out=out)
+        dyq = o.quantize(c["dy"])
+        wq = o.quantize_colwise(c["w"])
+        y_or, S = o.linear_fp64(dyq, wq), o.error_scale(dyq, wq)
+    torch.cuda.synchronize()
+    assert_gemm_close(out, y_or, S, what=f"dgrad {mode} strided")
+    assert torch.all(full[:, K:] == 7.0), "padding columns written"
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_wgrad_strided_inputs_padded_dw(out_dtype):
+    M, N, K = 256, 208, 640
+    rng = np.random.default_rng(91)
+    dyb = f32_to_bf16_bits((rng.standard_normal((M, N)) * 0.01).astype(np.float32))
+    xb = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    full, out = _padded(N, K, 8, out_dtype)
+    nv.nvfp4_wgrad(_strided_bf16(dyb, 24), _strided_bf16(xb, 16), out_dtype=out_dtype, out=out)
+    torch.cuda.synchronize()
+    a = o.quantize_colwise(dyb)
+    b = o.quantize_colwise(xb)
+    assert_gemm_close(out, o.linear_fp64(a, b), o.error_scale(a, b), what="wgrad strided")
+    assert torch.all(full[:, K:] == 7.0), "padding columns written"

@@ -71,6 +71,35 @@ def test_batched_dynamic_every_matrix(pack):
     check_quantize(bits, pack, "linear")
 
 
+@pytest.mark.parametrize("pack", ["row", "col", "both"])
+def test_strided_batched_input(pack):
+    """Input rows wider than the matrix and matrices further apart than their
+    rows (a view into a larger buffer whose extra elements are large: a read
+    of them would change g and the codes), dynamic scales, every matrix
+    against the oracle."""
+    E, R, C = 3, 208, 1040
+    rng = np.random.default_rng(23)
+    bits = f32_to_bf16_bits((rng.standard_normal((E, R, C)) * 0.1).astype(np.float32))
+    big = np.full((E, R + 2, C + 16), 0x4480, np.uint16)          # bf16 1024.0 outside the view
+    big[:, :R, :C] = bits
+    x = dev_bf16(big)[:, :R, :C]
+    out = nv.nvfp4_quantize(x, pack=pack, sf_layout="swizzled")
+    torch.cuda.synchronize()
+    g_gpu = out["global_scale"].cpu().numpy().reshape(-1)
+    for b in range(E):
+        if pack in ("row", "both"):
+            c, s_, g = oracle_pack(bits[b], None, "swizzled")
+            assert g_gpu[b] == g, (b, g_gpu[b], g)
+            assert_bits_equal(u8(out["codes_row"][b]), c, f"codes_row[{b}]")
+            assert_bits_equal(u8(out["sf_row"][b]), s_, f"sf_row[{b}]")
+        if pack in ("col", "both"):
+            gg = o.global_scale(bits[b])
+            assert g_gpu[b] == gg, (b, g_gpu[b], gg)
+            c, s_, _ = oracle_pack(np.ascontiguousarray(bits[b].T), gg, "swizzled")
+            assert_bits_equal(u8(out["codes_col"][b]), c, f"codes_col[{b}]")
+            assert_bits_equal(u8(out["sf_col"][b]), s_, f"sf_col[{b}]")
+
+
 @pytest.mark.parametrize("pack", ["row", "both"])
 def test_block_maxima_at_e4m3_rounding_ties(pack):
     """Block maxima on every E4M3 value, on every midpoint between two
