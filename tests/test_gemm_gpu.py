@@ -230,6 +230,34 @@ def test_lora_epilogue_in_place_and_norm(ydtype):
     assert abs(float(norm) - want) <= 2e-2 * want
 
 
+@pytest.mark.parametrize("ydtype", [torch.bfloat16, torch.float32])
+def test_lora_epilogue_strided_x_padded_y(ydtype):
+    """The standalone LoRA epilogue with X rows wider than K (extra elements
+    large: a read of them would change T) and Y rows wider than N (the padding
+    must stay as it was)."""
+    M, N, K, r = 260, 333, 512, 32
+    c = make_case("prefill", M=M, N=N, K=K, rank=r)
+    big = np.full((M, K + 16), 0x4480, np.uint16)
+    big[:, :K] = c["x"]
+    x = dev_bf16(big)[:, :K]
+    rng = np.random.default_rng(19)
+    pad = (8 - N % 8) % 8 + 8
+    full = torch.full((M, N + pad), 7.0, dtype=ydtype, device="cuda")
+    full[:, :N] = torch.from_numpy(rng.standard_normal((M, N)).astype(np.float32)).to("cuda", ydtype)
+    y = full[:, :N]
+    ybase = y.double().cpu().numpy()
+    nv.nvfp4_lora_epilogue(y, x, dev_bf16(c["lora_a"]), dev_bf16(c["lora_b"]), 64.0)
+    torch.cuda.synchronize()
+    d, _ = o.lora_delta_fp64(c["x"], c["lora_a"], c["lora_b"], 64.0)
+    term = lora_bf16_term(c["x"], c["lora_a"], c["lora_b"], 64.0)
+    got = y.double().cpu().numpy()
+    tol = term + 2e-5 * np.abs(d) + 1e-30
+    if ydtype == torch.bfloat16:
+        tol = tol + o.bf16_ulp(np.abs(ybase + d) + 1e-30)
+    assert np.all(np.abs(got - (ybase + d)) <= tol)
+    assert torch.all(full[:, N:] == 7.0), "padding columns written"
+
+
 def test_timeout_path_reports_and_recovers():
     """A zero wait budget makes in-kernel waits expire: the call must report
     NVFP4_ERR_TIMEOUT through the status word and leave the context usable."""
