@@ -14,27 +14,28 @@
 // on two SMs: each SM supplies its own 128 A rows and half of the B tile and
 // the instruction reads the other half from the peer's shared memory, so each
 // SM loads 4 KB of A, 4 KB of B and 1.5 KB of scales per 128 cycles (~74
-// B/cycle), and a stage is 38 KB instead of 54 KB (five stages in flight
-// instead of four).  Measured on the 8192 x 2048 x 6144 product it runs a few
-// percent faster than the 1-SM kernel: both are paced by the per-stage
-// hand-offs between the roles (~1100-1400 cycles per 512-cycle stage), not by
-// the tensor pipe or the loads (removing either changes the time by < 10%).
+// B/cycle), and a stage is 38.9 KB instead of 54 KB (five stages in flight
+// instead of four).  In steady state the stage copies arrive at ~56 B/cycle
+// per SM, close to what bulk copies from L2 reach with every SM loading: that
+// bandwidth, not the tensor pipe, bounds the kernel (~700 cycles a stage).
 //
 // A persistent kernel on clusters of two CTAs, one per SM, 384 threads each:
 //   warps 0, 10, 11  producers (both CTAs), one thread each: its 128 A rows,
 //               its 128-row half of B, and the scales of its A rows and of all
 //               256 B rows (one issuing warp per stream: a single warp issuing
 //               16 KB tile loads was measured at ~24 B/cycle per SM).
-//   warp 1      leader CTA only: one thread waits until both CTAs' tiles
-//               have landed (the peer's loads complete on the leader's
-//               barrier) and both CTAs' scales are in TMEM, then issues the pair MMAs
-//               (kind::mxf4nvf4 scale_vec::4X, M=256, N=256, K=64) and the
-//               LoRA kind::f16 steps; each commit arrives on the barriers of
-//               both CTAs (multicast).
+//   warp 1      leader CTA only: one thread waits on one barrier per stage --
+//               both CTAs' tiles landed (the peer's loads complete on the
+//               leader's barrier) and both CTAs' scale warps arrived -- then
+//               issues the pair MMAs (kind::mxf4nvf4 scale_vec::4X, M=256,
+//               N=256, K=64), two stages per loop iteration, and the LoRA
+//               kind::f16 steps; each commit arrives on the barriers of both
+//               CTAs (multicast).
 //   warps 2..5  scales -> own tensor memory (tcgen05.st), then arrive on the
-//               leader's "scales ready" barrier (remote arrive for the peer).
+//               leader's stage barrier (remote arrive for the peer).
 //   warps 6..9  epilogue: drain own 128 x 256 accumulator, arrive on the
-//               leader's "accumulator free" barrier, scale, convert, store.
+//               leader's "accumulator free" barrier, scale, convert, store
+//               (bf16 through shared-memory boxes and tensor stores).
 // Every wait is bounded; on expiry a CTA records a timeout, drains its own
 // copies (and, in the leader, its MMAs) and leaves its loops; the peer's waits
 // then expire too.  Both CTAs meet at a cluster barrier before freeing TMEM.
@@ -88,7 +89,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmParams &p, int u, int ti
 // Optional wait statistics (compile with -DNVFP4_WAIT_STATS): cycles each role
 // of each CTA of the pair spends in waits, summed over pairs into 64-bit
 // counters at byte 64 of the workspace (the status word's reserved block):
-// [8 * rank + role], roles 0 producer (stage free), 1 MMA (scales ready),
+// [8 * rank + role], roles 0 producer (stage free), 1 MMA (stage ready),
 // 2 MMA (accumulator free), 3 scale warp (stage full), 4 epilogue (accumulator
 // full), 5 kernel cycles, 6 CTAs.  Off in normal builds.
 #ifdef NVFP4_WAIT_STATS
@@ -399,7 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // scales: lane i of every quarter gets line i of each
     // 128x4 atom (rows i, i+32, i+64, i+96 of the chunk), 4 columns per atom --
     // every quarter holds all 256 B rows.  Then one arrive on the leader's
-    // "scales ready" barrier.
+    // stage barrier.
     const int q = warp & 3;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + 256;
     int stage = 0;
