@@ -285,7 +285,10 @@ nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
     }
   }
   if (a->lora_a) pl->t = c.take<__nv_bfloat16>((size_t)a->M * a->rank * 2);
-  if (a->lora_a && a->a_bf16 && !a->a_global_scale && !a->lora_x) {
+  // with X quantized in the call, the LoRA-down pass goes first (it reads X
+  // from HBM, and takes the amax when the scale is dynamic) and the packing
+  // pass reads X from L2 after it
+  if (a->lora_a && a->a_bf16 && !a->lora_x) {
     pl->lsplit = lora_split_for(a->K);
     pl->t32 = c.take<float>((size_t)pl->lsplit * a->M * a->rank * 4);
   }
@@ -396,9 +399,10 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
     q.status = status;
     q.timeout_ns = tmo;
     if (pl.t32) {
-      // one pass over X forms T = X A^T (fp32) and the amax partials; the
-      // packing pass then derives g, quantizes X and rounds T' = bf16(T s)
-      lp.amax_part = pl.aq_amax;
+      // one pass over X forms T = X A^T (fp32) and, for a dynamic scale, the
+      // amax partials; the packing pass then derives g (or takes the static
+      // one), quantizes X and rounds T' = bf16(T s)
+      lp.amax_part = a->a_global_scale ? nullptr : pl.aq_amax;
       lp.t_f32 = pl.t32;
       lp.ksplit = pl.lsplit;
       if (cudaError_t e_ = launch_lora_down(lp, lm, sms, st); e_ != cudaSuccess) return cuda_status(e_);

@@ -129,6 +129,22 @@ def test_prefill_lora_small(rank, out_dtype):
     assert_gemm_close(y, y_or, S, term, what=f"lora r{rank}")
 
 
+@pytest.mark.parametrize("M", [320, 96])
+def test_prefill_lora_static_input_scale(M):
+    """The prefill linear with a static input scale (no maximum pass: X is
+    packed first and the LoRA-down pass reads it on its own) on the CTA-pair
+    path (M = 320) and the 1-SM path (M = 96)."""
+    N, K, r = 512, 1024, 64
+    c = make_case("prefill", M=M, N=N, K=K, rank=r)
+    wc, ws, wg = quant_dev(c["w"])
+    sx = np.float32(16.0 / 2688.0)
+    gx = torch.tensor([float(sx)], dtype=torch.float32, device="cuda")
+    lora = dict(a=dev_bf16(c["lora_a"]), b=dev_bf16(c["lora_b"]), alpha=128.0)
+    y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx, lora=lora)
+    y_or, S, term = oracle_linear(c["x"], c["w"], (c["lora_a"], c["lora_b"], 128.0), xg=sx)
+    assert_gemm_close(y, y_or, S, term, what=f"static-scale lora M{M}")
+
+
 def test_prefill_full_size_sampled_rows():
     """X[8192,6144], W[2048,6144], LoRA r64 alpha 128, bf16 out: 96 sampled rows."""
     c = make_case("prefill")
