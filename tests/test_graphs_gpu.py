@@ -111,3 +111,34 @@ def test_graph_grouped_routing_and_lora():
     _same(perm, perm2, "grouped perm")
     _same(offs, offs2, "grouped offsets")
     _same(d, d2, "grouped D")
+
+
+def test_concurrent_streams_match_serial():
+    """Two calls on two streams at once (the persistent kernels share the
+    SMs; none of them waits on another grid): each result bit-identical to
+    the same call run alone."""
+    M, N, K, r = 512, 1024, 2048, 64
+    c = make_case("prefill", M=M, N=N, K=K, rank=r)
+    wq = nv.nvfp4_quantize(dev_bf16(c["w"]), pack="row", sf_layout="swizzled")
+    x = dev_bf16(c["x"])
+    lora = dict(a=dev_bf16(c["lora_a"]), b=dev_bf16(c["lora_b"]), alpha=128.0)
+    rng = np.random.default_rng(6)
+    w2 = dev_bf16(_bits(rng, (4, 512, 1536), 0.05))
+    call1, y = nv.prepare_gemm(wq["codes_row"], wq["sf_row"], wq["global_scale"], N, K, a_bf16=x, lora=lora)
+    call2, q = nv.prepare_quantize(w2, pack="both", sf_layout="swizzled")
+    call1()
+    call2()
+    torch.cuda.synchronize()
+    y_alone = y.clone()
+    q_alone = {k: v.clone() for k, v in q.items() if k != "workspace"}
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        s1.wait_stream(torch.cuda.current_stream())
+        s2.wait_stream(torch.cuda.current_stream())
+        for _ in range(4):
+            call1(s1)
+            call2(s2)
+        torch.cuda.synchronize()
+        _same(y, y_alone, "gemm on a concurrent stream")
+        for k, v in q_alone.items():
+            _same(q[k], v, f"quantize on a concurrent stream: {k}")
