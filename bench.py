@@ -48,10 +48,9 @@ PREFILL = dict(M=8192, N=2048, K=6144, rank=64, alpha=128.0)
 L2_BYTES = 129 * 1024 * 1024
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense fp4 : bf16 tensor ratio
 # DRAM bytes (read + write) of one GEMM launch on the prefill workload, from
-# one ncu capture of the current kernel (36.8 MB read + 3.1 MB written; Y is
-# still in L2 when the launch ends); None whenever the kernel has changed
+# one ncu capture of the current kernel; None whenever the kernel has changed
 # since that capture.
-GEMM_TRAFFIC_BYTES = 39.9e6
+GEMM_TRAFFIC_BYTES = None
 
 
 def peaks():
@@ -681,9 +680,11 @@ def main():
         roofline=dict(bound="tensor", kernel="k_gemm_fp4_pair", achieved=gemm_tflops,
                       peak=fp4_peak, unit="TFLOP/s", frac=gemm_tflops / fp4_peak,
                       traffic=GEMM_TRAFFIC_BYTES,
-                      traffic_note="dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu "
-                                   "capture of this kernel on this workload (M8192 N2048 K6144, "
-                                   "cold L2); algorithmic bytes 70.3 MB",
+                      traffic_note=("dram__bytes_read.sum + dram__bytes_write.sum per launch, one ncu "
+                                    "capture of this kernel on this workload (M8192 N2048 K6144, "
+                                    "cold L2); algorithmic bytes 70.3 MB" if GEMM_TRAFFIC_BYTES else
+                                    "null: no ncu capture of the kernel as it stands; algorithmic "
+                                    "bytes 70.3 MB"),
                       peak_note=f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x 6 "
                                 f"(nominal fp4:bf16), of {pk['source']}",
                       timing_note="CUDA events around each GEMM launch in a second run of the same "

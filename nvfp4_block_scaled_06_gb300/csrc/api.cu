@@ -459,6 +459,11 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   if (pl.pair) {
     p.tiles_n = (int)ceil_div(a->N, 256);
     map_pair_d(&maps, &p);
+    // 64-row B boxes for the half units of a short last round
+    maps.has_half = map2d(&maps.bh, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, 64) &&
+                    (!a->lora_a || map2d(&maps.lbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N,
+                                         a->rank * 2, 64, 64));
+    if (!a->lora_a) maps.lbh = maps.bh;
   }
   if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = pl.pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
@@ -1006,7 +1011,12 @@ nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, i
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
-  if (pair) map_pair_d(&maps, &p);
+  if (pair) {
+    map_pair_d(&maps, &p);
+    // 64-row B boxes for the half units of a short last round
+    maps.has_half = map2d(&maps.lbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, Kc, Nout, ldb * 2, 64, 64);
+    maps.bh = maps.lbh;
+  }
   if (cudaError_t e_ = mark(prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
   cudaError_t e = pair ? launch_gemm_fp4_pair(p, maps, sms, st) : launch_gemm_fp4(p, maps, bn, sms, st);
   if (e == cudaSuccess) e = mark(prof_end, st);

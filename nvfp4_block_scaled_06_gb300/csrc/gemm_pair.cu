@@ -75,14 +75,44 @@ static_assert(256 + kPairStages * kPSfCols <= kPTmemCols, "TMEM budget");
 static_assert(kPSmemBytes <= 232448, "shared memory budget");
 
 struct PairTile {
-  int64_t m0, n0;      // first row of the pair tile's A (256 rows) and B (256 rows)
+  int64_t m0, n0;      // first row of the unit's A (256 rows) and B (256 or 128 rows)
+  bool half;           // a 256 x 128 unit: one half of a tail tile
 };
 
-__device__ __forceinline__ PairTile pair_tile(const GemmParams &p, int u, int tiles_m2) {
+// The work units of a launch.  256 x 256 tiles, n-tile major (the pairs
+// running together share B tiles; A stays in L2), dealt round-robin to the
+// pairs.  When the tiles leave a last round that fills at most half of the
+// pairs (and the host allows it), each tile of that round is dealt as two
+// 256 x 128 units instead, so that the last round takes about half a tile's
+// time on twice as many pairs.  Every role derives the same schedule from
+// the grid size.
+struct PairSchedule {
+  int tiles_m2;        // 256-row tiles along M
+  int split_from;      // units before this are whole tiles
+  int num_units;
+};
+
+__device__ __forceinline__ PairSchedule pair_schedule(const GemmParams &p, int npairs) {
+  PairSchedule s;
+  s.tiles_m2 = (int)((p.M + 255) / 256);
+  const int tiles = s.tiles_m2 * p.tiles_n;
+  const int tail = tiles % npairs;
+  const bool split = p.pair_half_tail && tail > 0 && 2 * tail <= npairs;
+  s.split_from = split ? tiles - tail : tiles;
+  s.num_units = split ? tiles + tail : tiles;
+  return s;
+}
+
+__device__ __forceinline__ PairTile pair_tile(const PairSchedule &s, int u) {
   PairTile t;
-  // n-tile major: the pairs running together share B tiles; A stays in L2
-  t.n0 = (int64_t)(u / tiles_m2) * 256;
-  t.m0 = (int64_t)(u % tiles_m2) * 256;
+  int v = u, sub = 0;
+  t.half = u >= s.split_from;
+  if (t.half) {
+    v = s.split_from + ((u - s.split_from) >> 1);
+    sub = (u - s.split_from) & 1;
+  }
+  t.n0 = (int64_t)(v / s.tiles_m2) * 256 + 128 * sub;
+  t.m0 = (int64_t)(v % s.tiles_m2) * 256;
   return t;
 }
 
@@ -112,6 +142,7 @@ __device__ __forceinline__ void pair_abort(volatile int *abort_flag, int *status
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     k_gemm_fp4_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmT, const __grid_constant__ CUtensorMap tmLB,
+                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmLBh,
                     const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   constexpr int S = kPairStages;
 #ifdef NVFP4_WAIT_STATS
@@ -162,6 +193,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       tma_prefetch_desc(&tmT);
       tma_prefetch_desc(&tmLB);
     }
+    if (p.pair_half_tail) {
+      tma_prefetch_desc(&tmBh);
+      if (p.lora_steps) tma_prefetch_desc(&tmLBh);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kPTmemCols);
@@ -175,9 +210,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   griddep_launch_dependents();
   griddep_wait();      // inputs of this kernel come from the previous one in the stream
 
-  const int tiles_m2 = (int)((p.M + 255) / 256);
-  const int num_tiles = tiles_m2 * p.tiles_n;
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const PairSchedule sched = pair_schedule(p, npairs);
+  const int num_units = sched.num_units;
   const int a_sf_chunks = (int)((p.M + 127) / 128);
   // the leader's barriers as cluster addresses (for the peer: its remote copy)
   const uint32_t full_l = mapa_shared(smem_u32(full), 0);
@@ -197,12 +232,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_par = 0;
     bool ok = true;
-    for (int u = pair; ok && u < num_tiles; u += npairs) {
-      const PairTile t = pair_tile(p, u, tiles_m2);
-      const int a_row = (int)(t.m0 + 128 * rank), b_row = (int)(t.n0 + 128 * rank);
+    for (int u = pair; ok && u < num_units; u += npairs) {
+      const PairTile t = pair_tile(sched, u);
+      // a half unit's B is 128 rows: 64 in each CTA
+      const int a_row = (int)(t.m0 + 128 * rank), b_row = (int)(t.n0 + (t.half ? 64 : 128) * rank);
+      const uint32_t b_bytes = t.half ? kPBBytes / 2 : kPBBytes;
       const bool sfa_ok = (a_row >> 7) < a_sf_chunks;           // rows past the padded scales: codes are 0
       const int64_t chunk0 = t.n0 >> 7;
-      const int chunks = chunk0 + 1 < p.b_sf_row_chunks ? 2 : 1;  // B scale chunks present
+      const int chunks = !t.half && chunk0 + 1 < p.b_sf_row_chunks ? 2 : 1;  // B scale chunks read
       const uint8_t *sfa_src = p.a_sf + 512 * ((int64_t)(a_row >> 7) * p.a_sf_katoms);
       const uint8_t *sfb_src = p.b_sf + 512 * (chunk0 * p.b_sf_katoms);
       const int64_t sfb_chunk_stride = 512 * p.b_sf_katoms;
@@ -219,12 +256,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const uint32_t fb = full_base + 8 * stage, sfbar = sff_base + 8 * stage;
         if (role < 2) {
           // the leader expects both CTAs' tiles; the peer's land on the leader's barrier
-          const CUtensorMap *tm = role == 0 ? (i < p.num_kt ? &tmA : &tmT) : (i < p.num_kt ? &tmB : &tmLB);
+          const CUtensorMap *tm = role == 0 ? (i < p.num_kt ? &tmA : &tmT)
+                                            : t.half ? (i < p.num_kt ? &tmBh : &tmLBh)
+                                                     : (i < p.num_kt ? &tmB : &tmLB);
           const uint32_t dst = role == 0 ? a_base + stage * kPABytes : b_base + stage * kPBBytes;
           const int c0 = i < p.num_kt ? i * 128 : (i - p.num_kt) * 64;
           const int c1 = role == 0 ? a_row : b_row;
           if (rank == 0) {
-            mbar_arrive_expect_tx_u(fb, 2 * (role == 0 ? kPABytes : kPBBytes));
+            mbar_arrive_expect_tx_u(fb, 2 * (role == 0 ? (uint32_t)kPABytes : b_bytes));
             tma_load_2d_u(dst, tm, fb, c0, c1);
           } else {
             tma_load_2d_pair_u(dst, tm, full_l + 8 * stage, c0, c1);
@@ -259,8 +298,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------- MMA issue (leader only) --
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = idesc_nvfp4(256, 256);
-      const uint32_t idesc_l = idesc_bf16(256, 256);
+      uint32_t idesc = idesc_nvfp4(256, 256);
+      uint32_t idesc_l = idesc_bf16(256, 256);
       const uint64_t adesc0 = sdesc_k_sw128(sA), bdesc0 = sdesc_k_sw128(sB);
       const uint32_t empty_base = smem_u32(empty);
       const uint32_t full_base = smem_u32(full);
@@ -318,7 +357,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         tc_commit_pair_mc(empty_base + 8 * st, 3);   // frees the stage in both CTAs
       };
       const int nfull = p.num_kt - (last_nk < 4 ? 1 : 0);
-      for (int u = pair; ok && u < num_tiles; u += npairs) {
+      for (int u = pair; ok && u < num_units; u += npairs) {
+        // a half unit: N = 128 (64 B rows in each CTA, one chunk of B scales)
+        const bool half_unit = u >= sched.split_from;
+        idesc = idesc_nvfp4(256, half_unit ? 128 : 256);
+        idesc_l = idesc_bf16(256, half_unit ? 128 : 256);
         PSTAT_T0();
         const bool got_acc = !*abort_flag && mbar_wait_u(acce, acc_phase ^ 1, p.timeout_ns);
         PSTAT_ADD(p, rank, 2);
@@ -406,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int u = pair; ok && u < num_tiles; u += npairs) {
+    for (int u = pair; ok && u < num_units; u += npairs) {
       const int nsteps = p.num_kt + p.lora_steps;
       for (int i = 0; i < nsteps; ++i) {
         PSTAT_T0();
@@ -452,15 +495,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ epilogue --
     // Warp w drains lane quarter w % 4 of this CTA's accumulator: each thread
-    // owns one row, loads it in two halves of 128 columns and releases the
-    // accumulator after the second half's loads, so that the next tile's MMAs
-    // overlap the remaining stores.
+    // owns one row, loads it in two halves of 128 columns (a half unit: one)
+    // and releases the accumulator after the last half's loads, so that the
+    // next unit's MMAs overlap the remaining stores.
     const int q = warp & 3;
     const int r = q * 32 + lane;
     uint32_t acc_phase = 0;
     const float alpha = acc_scale_of(p.g_a ? *p.g_a : 1.0f, p.g_b ? *p.g_b : 1.0f);
-    for (int u = pair; u < num_tiles; u += npairs) {
-      const PairTile t = pair_tile(p, u, tiles_m2);
+    for (int u = pair; u < num_units; u += npairs) {
+      const PairTile t = pair_tile(sched, u);
+      const int halves = t.half ? 1 : 2;
       // warp-uniform outcome: tcgen05.ld below is a warp-collective instruction
       PSTAT_T0();
       const bool got_full =
@@ -474,14 +518,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const int64_t orow = t.m0 + 128 * rank + r;
       const bool row_ok = orow < p.M;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < halves; ++half) {
         uint32_t v[4][32];
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(q * 32) << 16) + (half * 4 + c) * 32, v[c]);
         tmem_ld_wait();
-        if (half == 1) {
+        if (half == halves - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_l);
@@ -619,12 +663,19 @@ static int resident_pairs(int num_sms) {
 cudaError_t launch_gemm_fp4_pair(const GemmParams &p, const GemmMaps &m, int num_sms, cudaStream_t st) {
   if (cudaError_t e = ensure_dynamic_smem((const void *)k_gemm_fp4_pair, kPSmemBytes); e != cudaSuccess) return e;
   const int64_t tiles = ((p.M + 255) / 256) * (int64_t)p.tiles_n;
-  int64_t pairs = std::min<int64_t>(tiles, resident_pairs(num_sms));
-  if (pairs <= 0) return cudaSuccess;
+  const int64_t resident = resident_pairs(num_sms);
   GemmParams q = p;
   q.store_tma = p.store_tma && m.has_d;
+  // half units need the 64-row B maps, and every half of the last n-tile
+  // must hold a column of D (so that its B scale chunk exists)
+  q.pair_half_tail = m.has_half && p.N - (int64_t)(p.tiles_n - 1) * 256 > 128;
+  // fewer tiles than pairs: as many pairs as tiles, or twice as many (every
+  // tile dealt as two half units) when they fit
+  int64_t pairs = std::min<int64_t>(tiles, resident);
+  if (q.pair_half_tail && tiles < resident && 2 * tiles <= resident) pairs = 2 * tiles;
+  if (pairs <= 0) return cudaSuccess;
   return launch_pdl(k_gemm_fp4_pair, dim3((unsigned)(2 * pairs)), dim3(kPairThreads), kPSmemBytes, st, m.a, m.b, m.t,
-                    m.lb, m.has_d ? m.d : m.a, q);
+                    m.lb, m.has_half ? m.bh : m.b, m.has_half ? m.lbh : m.lb, m.has_d ? m.d : m.a, q);
 }
 
 }  // namespace nvfp4

@@ -98,19 +98,23 @@ struct GemmParams {
   uint64_t timeout_ns;
   int stall_probe;            // test hook: first wait on a barrier nothing arrives at
   int store_tma;              // pair kernel, bf16 output: D leaves through GemmMaps::d
+  int pair_half_tail;         // pair kernel: a last round of at most half the pairs runs as 256 x 128 units
 };
 
 struct GemmMaps {
   CUtensorMap a, b, t, lb;
   CUtensorMap d;   // pair kernel, bf16 output: D [M][ldd] in 32 x 32 boxes, 64-byte swizzle
+  CUtensorMap bh, lbh;   // pair kernel: b and lb with 64-row boxes (the 256 x 128 units)
   bool has_d = false;
+  bool has_half = false;
 };
 
 cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, int num_sms,
                             cudaStream_t st);
 // The dense product on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2):
 // p.tiles_n = ceil(N / 256); maps.b and maps.lb with 128-row boxes (each CTA
-// loads its half of the B tile); no grouped tiles, split-K or accumulation.
+// loads its half of the B tile), maps.bh and maps.lbh (has_half) the same
+// with 64-row boxes; no grouped tiles, split-K or accumulation.
 cudaError_t launch_gemm_fp4_pair(const GemmParams &p, const GemmMaps &maps, int num_sms, cudaStream_t st);
 // Sums split-K partials in order: D = sum_s partial[s] (bf16 or fp32 out).
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st);

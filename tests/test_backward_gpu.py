@@ -58,7 +58,8 @@ def dgrad_oracle_bf16(dy_bits, codes, sf, g):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (300, 256, 640), (1, 128, 128), (129, 1024, 256)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (300, 256, 640), (1, 128, 128), (129, 1024, 256),
+                                   (2560, 256, 2048)])
 def test_dgrad_dequant_bf16(M, N, K, out_dtype):
     c = make_case("dgrad", M=M, N=N, K=K)
     codes, sf, g = o.quantize(c["w"])

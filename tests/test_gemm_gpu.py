@@ -79,6 +79,33 @@ def test_pair_gemm_ragged_columns_and_padded_output(M, N, K, out_dtype):
     assert torch.all(full[:, N:] == 7.0), "padding columns written"
 
 
+@pytest.mark.parametrize("M,N,K,rank", [(2560, 2048, 512, 0), (4864, 1536, 256, 64), (5120, 968, 512, 32),
+                                         (1024, 1792, 512, 64), (2304, 864, 256, 0)])
+def test_pair_gemm_half_width_last_round(M, N, K, rank):
+    """The CTA-pair schedule whose last round of 256 x 256 tiles fills at most
+    half of the pairs deals those tiles as 256 x 128 halves (with 76 resident
+    pairs: 80 tiles leave 4, 114 leave 38; 32 tiles all run as 64 halves; a
+    last n-tile of 200 columns splits into 128 + 72, one of 96 columns keeps
+    whole tiles): every element of Y within tolerance, with and without the
+    LoRA steps, whatever the number of resident pairs."""
+    rng = np.random.default_rng(M + 3 * N + K)
+    xb = f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    wb = f32_to_bf16_bits((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    wc, ws, wg = quant_dev(wb)
+    if rank:
+        la = f32_to_bf16_bits((rng.standard_normal((rank, K)) * 0.02).astype(np.float32))
+        lb = f32_to_bf16_bits((rng.standard_normal((N, rank)) * 0.02).astype(np.float32))
+        lora = dict(a=dev_bf16(la), b=dev_bf16(lb), alpha=128.0)
+        y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(xb), lora=lora)
+        y_or, S, term = oracle_linear(xb, wb, (la, lb, 128.0))
+    else:
+        xc, xs, xg = quant_dev(xb)
+        y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg)
+        y_or, S, term = oracle_linear(xb, wb)
+    torch.cuda.synchronize()
+    assert_gemm_close(y, y_or, S, term, what=f"half-width last round {M}x{N}x{K} r{rank}")
+
+
 @pytest.mark.parametrize("M,N,K,static", [(1, 333, 2048, True), (3, 1030, 20480, True), (8, 333, 512, False),
                                           (64, 1030, 4096, False), (32, 333, 16384, True)])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
