@@ -225,6 +225,28 @@ def test_decode_chunked_rows(M, N, K):
         assert_gemm_close(y, y_or, S, what=f"decode M{M} N{N} K{K}")
 
 
+@pytest.mark.parametrize("M,N,K,static", [(8, 1024, 2048, True), (8, 768, 16384, True), (40, 512, 1024, False),
+                                          (300, 512, 512, False)])
+def test_in_call_x_padding_rows_ignored(M, N, K, static):
+    """X quantized in the call is packed into the workspace with its rows
+    padded to 128, and the GEMM's A tiles span the padding: whatever those
+    rows' codes hold (the workspace is filled with 0xFF, code -6 in every
+    nibble, before each call), their zero block scales keep them out of every
+    stored row of Y.  Small M on the 1-SM kernel (with and without split K)
+    and a ragged last row tile on the CTA-pair kernel."""
+    c = make_case("decode_q_b_proj", M=M, N=N, K=K)
+    wc, ws, wg = quant_dev(c["w"])
+    sx = np.float32(16.0 / 2688.0)
+    gx = torch.tensor([float(sx)], dtype=torch.float32, device="cuda") if static else None
+    call, y = nv.prepare_gemm(wc, ws, wg, N, K, a_bf16=dev_bf16(c["x"]), a_global_scale=gx)
+    for _ in range(2):
+        call.workspace[256:].fill_(0xFF)
+        call()
+        torch.cuda.synchronize()
+        y_or, S, _ = oracle_linear(c["x"], c["w"], xg=sx if static else None)
+        assert_gemm_close(y, y_or, S, what=f"padded-row X M{M} N{N} K{K}")
+
+
 @pytest.mark.parametrize("name", ["decode_q_b_proj", "decode_o_proj"])
 def test_decode_full_weights_sampled(name):
     """The decode projections at their real shapes and M = 1, 8, 32: the GEMV
