@@ -467,7 +467,7 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   if (pl.pair) {
     p.tiles_n = (int)ceil_div(a->N, 256);
     map_pair_d(&maps, &p);
-    // 64-row B boxes for the half units of a short last round
+    // 64-row B boxes for the half units of a short last wave
     maps.has_half = map2d(&maps.bh, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, 64) &&
                     (!a->lora_a || map2d(&maps.lbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->lora_b, a->rank, a->N,
                                          a->rank * 2, 64, 64));
@@ -1021,7 +1021,7 @@ nvfp4_status run_bf16_gemm(int64_t M, int64_t Nout, int64_t Kc, const void *A, i
   p.stall_probe = tmo == 0;
   if (pair) {
     map_pair_d(&maps, &p);
-    // 64-row B boxes for the half units of a short last round
+    // 64-row B boxes for the half units of a short last wave
     maps.has_half = map2d(&maps.lbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, Kc, Nout, ldb * 2, 64, 64);
     maps.bh = maps.lbh;
   }

@@ -81,9 +81,9 @@ struct PairTile {
 
 // The work units of a launch.  256 x 256 tiles, n-tile major (the pairs
 // running together share B tiles; A stays in L2), dealt round-robin to the
-// pairs.  When the tiles leave a last round that fills at most half of the
-// pairs (and the host allows it), each tile of that round is dealt as two
-// 256 x 128 units instead, so that the last round takes about half a tile's
+// pairs.  When the tiles leave a last wave that fills at most half of the
+// pairs (and the host allows it), each tile of that wave is dealt as two
+// 256 x 128 units instead, so that the last wave takes about half a tile's
 // time on twice as many pairs.  Every role derives the same schedule from
 // the grid size.
 struct PairSchedule {

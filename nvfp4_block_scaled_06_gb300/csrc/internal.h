@@ -98,7 +98,7 @@ struct GemmParams {
   uint64_t timeout_ns;
   int stall_probe;            // test hook: first wait on a barrier nothing arrives at
   int store_tma;              // pair kernel, bf16 output: D leaves through GemmMaps::d
-  int pair_half_tail;         // pair kernel: a last round of at most half the pairs runs as 256 x 128 units
+  int pair_half_tail;         // pair kernel: a last wave of at most half the pairs runs as 256 x 128 units
 };
 
 struct GemmMaps {

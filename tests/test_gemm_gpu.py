@@ -81,8 +81,8 @@ def test_pair_gemm_ragged_columns_and_padded_output(M, N, K, out_dtype):
 
 @pytest.mark.parametrize("M,N,K,rank", [(2560, 2048, 512, 0), (4864, 1536, 256, 64), (5120, 968, 512, 32),
                                          (1024, 1792, 512, 64), (2304, 864, 256, 0)])
-def test_pair_gemm_half_width_last_round(M, N, K, rank):
-    """The CTA-pair schedule whose last round of 256 x 256 tiles fills at most
+def test_pair_gemm_half_width_last_wave(M, N, K, rank):
+    """The CTA-pair schedule whose last wave of 256 x 256 tiles fills at most
     half of the pairs deals those tiles as 256 x 128 halves (with 76 resident
     pairs: 80 tiles leave 4, 114 leave 38; 32 tiles all run as 64 halves; a
     last n-tile of 200 columns splits into 128 + 72, one of 96 columns keeps
@@ -103,7 +103,7 @@ def test_pair_gemm_half_width_last_round(M, N, K, rank):
         y = nv.nvfp4_gemm(wc, ws, wg, N, K, a_codes=xc, a_sf=xs, a_global_scale=xg)
         y_or, S, term = oracle_linear(xb, wb)
     torch.cuda.synchronize()
-    assert_gemm_close(y, y_or, S, term, what=f"half-width last round {M}x{N}x{K} r{rank}")
+    assert_gemm_close(y, y_or, S, term, what=f"half-width last wave {M}x{N}x{K} r{rank}")
 
 
 @pytest.mark.parametrize("M,N,K,static", [(1, 333, 2048, True), (3, 1030, 20480, True), (8, 333, 512, False),
