@@ -56,7 +56,8 @@ typedef struct CUstream_st *nvfp4_stream;   /* == cudaStream_t */
 
 typedef enum {
   NVFP4_OK = 0,
-  NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, non-positive size */
+  NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, bad enum, non-positive size (an empty
+                                       operand: nothing is launched or written) */
   NVFP4_ERR_UNSUPPORTED_SHAPE = 2,  /* size outside what the kernels take */
   NVFP4_ERR_ALIGNMENT = 3,          /* pointer or leading dimension misaligned */
   NVFP4_ERR_WORKSPACE = 4,          /* workspace missing or too small */

@@ -122,3 +122,45 @@ def test_grouped_input_forms_validation(clib):
     for form in (dict(**ids, **bf16), dict(**given, **packed), dict(**ids, **packed, x_bf16=4096,
                  lora_a=4096, lora_b=4096, rank=64), dict(**given, **bf16, out_dtype=OUT_FP32)):
         assert grouped(**form) != ERR_INVALID_ARG, form
+
+
+def test_empty_operands_rejected_before_any_launch(clib):
+    """An empty operand (a zero size) is NVFP4_ERR_INVALID_ARG on every entry
+    point, decided on the host before anything is launched or written; the
+    same arguments with the size restored pass that check (they then fail for
+    the missing workspace or device, never with INVALID_ARG)."""
+    from nvfp4_block_scaled_06_gb300._binding import (ERR_INVALID_ARG, DequantArgs, DgradArgs, GemmArgs,
+                                                       GroupedArgs, LoraArgs, MoeDownArgs, QuantArgs, WgradArgs)
+    P = 4096                                       # a 16-byte aligned stand-in pointer (never dereferenced)
+    cases = [
+        (clib.nvfp4_quantize, QuantArgs, dict(src=P, batch=1, rows=32, cols=64, ld=64, pack=1, sf_layout=1,
+                                              global_scale_out=P, codes_row=P, sf_row=P),
+         ("batch", "rows", "cols")),
+        (clib.nvfp4_gemm, GemmArgs, dict(M=8, N=8, K=64, a_codes=P, a_sf=P, a_global_scale=P, b_codes=P,
+                                         b_sf=P, b_global_scale=P, d=P, ldd=8),
+         ("M", "N", "K")),
+        (clib.nvfp4_grouped_gemm, GroupedArgs, dict(num_tokens=4, top_k=2, num_experts=8, N=256, K=64,
+                                                    expert_ids=P, x_bf16=P, w_codes=P, w_sf=P,
+                                                    w_global_scale=P, d=P, perm_out=P),
+         ("num_tokens", "top_k", "num_experts", "N", "K")),
+        (clib.nvfp4_lora_epilogue, LoraArgs, dict(M=4, N=8, K=64, x=P, ldx=64, lora_a=P, lora_b=P, rank=64,
+                                                  alpha=128.0, y_dtype=0, y=P, ldy=8),
+         ("M", "N", "K")),
+        (clib.nvfp4_dequantize, DequantArgs, dict(codes=P, sf=P, sf_layout=1, global_scale=P, rows=32, cols=64,
+                                                  out=P, ldo=64),
+         ("rows", "cols")),
+        (clib.nvfp4_dgrad, DgradArgs, dict(M=8, N=64, K=64, mode=0, dy=P, lddy=64, w_codes=P, w_sf=P,
+                                           w_global_scale=P, dx=P, lddx=64),
+         ("M", "N", "K")),
+        (clib.nvfp4_wgrad, WgradArgs, dict(M=32, N=16, K=16, dy=P, lddy=16, x=P, ldx=16, dw=P, lddw=16),
+         ("M", "N", "K")),
+        (clib.nvfp4_moe_down_combine, MoeDownArgs, dict(num_tokens=4, top_k=2, num_experts=8, N=256, K=64,
+                                                        h=P, perm=P, expert_offsets=P, route_weights=P,
+                                                        w_codes=P, w_sf=P, w_global_scale=P, y=P),
+         ("num_tokens", "top_k", "num_experts", "N", "K")),
+    ]
+    for fn, cls, base, sizes in cases:
+        assert fn(C.byref(cls(**base)), None) != ERR_INVALID_ARG, (fn.__name__, "baseline")
+        for name in sizes:
+            args = cls(**dict(base, **{name: 0}))
+            assert fn(C.byref(args), None) == ERR_INVALID_ARG, (fn.__name__, name)
