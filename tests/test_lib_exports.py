@@ -164,3 +164,47 @@ def test_empty_operands_rejected_before_any_launch(clib):
         for name in sizes:
             args = cls(**dict(base, **{name: 0}))
             assert fn(C.byref(args), None) == ERR_INVALID_ARG, (fn.__name__, name)
+
+
+def test_size_limits_on_the_host(clib):
+    """The largest sizes each entry point takes (indices stay within the
+    kernels' 32-bit fields) pass the host checks; one step past them is
+    NVFP4_ERR_UNSUPPORTED_SHAPE, decided before any launch."""
+    from nvfp4_block_scaled_06_gb300._binding import (ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, GemmArgs,
+                                                       GroupedArgs, QuantArgs)
+    P = 4096
+    bad = (ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE)
+
+    def gemm(**kw):
+        base = dict(M=8, N=8, K=64, a_codes=P, a_sf=P, a_global_scale=P, b_codes=P, b_sf=P,
+                    b_global_scale=P, d=P, ldd=8)
+        base.update(kw)
+        base["ldd"] = max(base["ldd"], base["N"] + (-base["N"]) % 8)
+        return clib.nvfp4_gemm(C.byref(GemmArgs(**base)), None)
+
+    top = (1 << 31) - 256
+    assert gemm(M=top) not in bad and gemm(M=top + 1) == ERR_UNSUPPORTED_SHAPE
+    assert gemm(N=top) not in bad and gemm(N=top + 8) == ERR_UNSUPPORTED_SHAPE
+    assert gemm(K=1 << 24) not in bad and gemm(K=(1 << 24) + 32) == ERR_UNSUPPORTED_SHAPE
+
+    def quant(**kw):
+        base = dict(src=P, batch=1, rows=32, cols=64, ld=64, pack=1, sf_layout=1, global_scale_out=P,
+                    codes_row=P, sf_row=P, codes_col=P, sf_col=P)
+        base.update(kw)
+        base["ld"] = max(base["ld"], base["cols"])
+        return clib.nvfp4_quantize(C.byref(QuantArgs(**base)), None)
+
+    assert quant(rows=1 << 31) not in bad and quant(rows=(1 << 31) + 16) == ERR_UNSUPPORTED_SHAPE
+    # the column packing indexes rows and columns in 32 bits
+    assert quant(pack=3, rows=(1 << 30) - 16) not in bad and quant(pack=3, rows=1 << 30) == ERR_UNSUPPORTED_SHAPE
+
+    def grouped(**kw):
+        base = dict(num_tokens=4, top_k=2, num_experts=8, N=256, K=64, expert_ids=P, x_bf16=P, w_codes=P,
+                    w_sf=P, w_global_scale=P, d=P, perm_out=P)
+        base.update(kw)
+        return clib.nvfp4_grouped_gemm(C.byref(GroupedArgs(**base)), None)
+
+    assert grouped(num_experts=1024) not in bad and grouped(num_experts=1025) == ERR_UNSUPPORTED_SHAPE
+    assert grouped(top_k=8, num_experts=8) not in bad and grouped(top_k=9, num_experts=8) == ERR_UNSUPPORTED_SHAPE
+    assert grouped(num_tokens=1 << 27, top_k=8) not in bad
+    assert grouped(num_tokens=(1 << 27) + 1, top_k=8) == ERR_UNSUPPORTED_SHAPE
