@@ -16,8 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "gemv.cu", "route.cu", "static_scratch.cu",
-           "dequant.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemv.cu", "route.cu",
+           "static_scratch.cu", "dequant.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -233,8 +233,23 @@ struct GemmPlan {
   int lsplit = 1;
   int bn = 256, ksplit = 1;
   bool pair = false;            // dense product on CTA pairs (256 x 256 tiles)
+  bool skinny = false;          // a few rows, weights as the MMA's A operand
   float *partial = nullptr;     // split-K partials [ksplit][M][N]
 };
+
+// A few activation rows quantized in the call (decode) take the operand-swapped
+// kernel: the weights fill the 128-row side of the MMA, the rows (<= 32) its
+// N = 32 side, and a stage carries 24 KB instead of 36 KB.
+bool use_skinny(const nvfp4_gemm_args *a) { return a->M <= 32 && a->a_bf16 && !a->lora_a; }
+
+// K ranges for the operand-swapped kernel: enough units (128-feature tiles x
+// K ranges) to occupy the SMs, at least four 256-wide K tiles per range.
+int pick_skinny_ksplit(int64_t N, int64_t K, int sms) {
+  const int64_t tiles = ceil_div(N, 128), nkt = ceil_div(K, 256);
+  int64_t ks = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(sms / tiles, nkt / 4), 16));
+  const int64_t per = ceil_div(nkt, ks);   // every K range non-empty
+  return (int)ceil_div(nkt, per);
+}
 
 // The pair kernel serves every dense product with at least one full 256-row
 // pair tile and no K split (the small-M decode products keep the 1-SM kernel,
@@ -297,8 +312,10 @@ nvfp4_status plan_gemm(const nvfp4_gemm_args *a, GemmPlan *pl) {
   }
   const int sms = plan_sms();
   pl->bn = pick_bn(a->M, a->N, sms);
-  pl->ksplit = pick_ksplit(a->M, a->N, a->K, pl->bn, sms, a->lora_a != nullptr);
-  pl->pair = use_pair(a->M, pl->ksplit);
+  pl->skinny = use_skinny(a);
+  pl->ksplit = pl->skinny ? pick_skinny_ksplit(a->N, a->K, sms)
+                          : pick_ksplit(a->M, a->N, a->K, pl->bn, sms, a->lora_a != nullptr);
+  pl->pair = !pl->skinny && use_pair(a->M, pl->ksplit);
   if (pl->ksplit > 1) pl->partial = c.take<float>((size_t)pl->ksplit * a->M * a->N * 4);
   pl->ws = c.off;
   return NVFP4_OK;
@@ -464,6 +481,20 @@ nvfp4_status run_gemm(const nvfp4_gemm_args *a, const GemmPlan &pl, int sms, cud
   p.status = status;
   p.timeout_ns = tmo;
   p.stall_probe = tmo == 0;
+  if (pl.skinny) {
+    // the activation rows as the MMA's B operand: boxes of 32 rows of the
+    // 128-row padded buffer; the weights keep their 128-row boxes
+    CUtensorMap mx;
+    if (!map2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, a->K / 2, a_rows, a->K / 2, 128, 32) ||
+        !map2d(&maps.b, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->b_codes, a->K / 2, a->N, a->K / 2, 128, 128))
+      return NVFP4_ERR_CUDA;
+    p.tiles_n = (int)ceil_div(a->N, 128);
+    if (cudaError_t e_ = mark(a->prof_begin, st); e_ != cudaSuccess) return cuda_status(e_);
+    cudaError_t e = launch_gemm_fp4_skinny(p, mx, maps.b, sms, st);
+    if (e == cudaSuccess && pl.ksplit > 1) e = launch_splitk_reduce(p, sms, st);
+    if (e == cudaSuccess) e = mark(a->prof_end, st);
+    return cuda_status(e);
+  }
   if (pl.pair) {
     p.tiles_n = (int)ceil_div(a->N, 256);
     map_pair_d(&maps, &p);

@@ -116,6 +116,12 @@ cudaError_t launch_gemm_fp4(const GemmParams &p, const GemmMaps &maps, int bn, i
 // loads its half of the B tile), maps.bh and maps.lbh (has_half) the same
 // with 64-row boxes; no grouped tiles, split-K or accumulation.
 cudaError_t launch_gemm_fp4_pair(const GemmParams &p, const GemmMaps &maps, int num_sms, cudaStream_t st);
+// The product for M <= 32 activation rows with the operands swapped (weights
+// as the MMA's 128-row A side): x = activation codes in 32-row boxes of a
+// buffer padded to 128 rows, w = weight codes in 128-row boxes; p.tiles_n =
+// ceil(N / 128); split-K partials as k_gemm_fp4's.
+cudaError_t launch_gemm_fp4_skinny(const GemmParams &p, const CUtensorMap &x, const CUtensorMap &w, int num_sms,
+                                   cudaStream_t st);
 // Sums split-K partials in order: D = sum_s partial[s] (bf16 or fp32 out).
 cudaError_t launch_splitk_reduce(const GemmParams &p, int num_sms, cudaStream_t st);
 

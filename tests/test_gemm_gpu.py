@@ -226,14 +226,16 @@ def test_decode_chunked_rows(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,static", [(8, 1024, 2048, True), (8, 768, 16384, True), (40, 512, 1024, False),
-                                          (300, 512, 512, False)])
+                                          (300, 512, 512, False), (8, 200, 3072, True), (24, 968, 2560, False)])
 def test_in_call_x_padding_rows_ignored(M, N, K, static):
     """X quantized in the call is packed into the workspace with its rows
-    padded to 128, and the GEMM's A tiles span the padding: whatever those
+    padded to 128, and the GEMM's tiles span the padding: whatever those
     rows' codes hold (the workspace is filled with 0xFF, code -6 in every
     nibble, before each call), their zero block scales keep them out of every
-    stored row of Y.  Small M on the 1-SM kernel (with and without split K)
-    and a ragged last row tile on the CTA-pair kernel."""
+    stored row of Y.  M <= 32 on the operand-swapped kernel (K ranges summed
+    in clusters of 2 and 3, ragged N, or by the split-K pass for 16 ranges),
+    M = 40 on the 1-SM kernel and a ragged last row tile on the CTA-pair
+    kernel."""
     c = make_case("decode_q_b_proj", M=M, N=N, K=K)
     wc, ws, wg = quant_dev(c["w"])
     sx = np.float32(16.0 / 2688.0)
