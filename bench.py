@@ -399,7 +399,7 @@ def run_decode(torch, nv, device, steps, warmup, pk):
                 ms=ms, ms_instrumented=ms_prof, kernel_ms=kms,
                 weight_gbs=wbytes / (ms * 1e-3) / 1e9, frac_call=alg / (ms * 1e-3) / 1e9 / pk["hbm"],
                 kernel_gbs=alg / (kms * 1e-3) / 1e9, frac=alg / (kms * 1e-3) / 1e9 / pk["hbm"],
-                path="cuda-core GEMV" if M <= 4 else "tcgen05 GEMM")
+                path="cuda-core GEMV" if M <= 4 else "tcgen05 GEMM, weights as the 128-row operand")
         del wqs, c
         torch.cuda.empty_cache()
     return res
