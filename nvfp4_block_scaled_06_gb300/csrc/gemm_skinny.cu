@@ -104,7 +104,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_launch_dependents();
-  griddep_wait();   // inputs of this kernel come from the previous one in the stream
+  // Inputs of this kernel come from the previous one in the stream (the
+  // activation packing), which lets this grid start only after every kernel
+  // before it has completed: the producer issues the weight tiles of its
+  // first stages before its wait, every other thread waits here.
+  if (warp != 0) griddep_wait();
 
   const int ksplit = p.ksplit > 1 ? p.ksplit : 1;
   const int num_units = p.tiles_n * ksplit;          // (128-feature tile, K range)
@@ -120,13 +124,32 @@ __global__ void __launch_bounds__(kSkThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_par = 0;
       bool ok = true;
+      // the first unit's first stages (all free at entry): weights before the wait
+      int pre = 0;
+      if ((int)blockIdx.x < num_units) {
+        const int nt = blockIdx.x / ksplit;
+        const int kt0 = (blockIdx.x % ksplit) * kt_per, kt1 = min(p.num_kt, kt0 + kt_per);
+        pre = min(S, kt1 - kt0);
+        const uint8_t *sfw_src = p.b_sf + 512 * ((int64_t)nt * p.b_sf_katoms + (int64_t)kt0 * 4);
+        for (int i = 0; i < pre; ++i) {
+          const int kt = kt0 + i;
+          const uint32_t fb = full_base + 8 * i;
+          const uint32_t sfb = (uint32_t)((kt == p.num_kt - 1 ? last_nk : 4) * 512);
+          mbar_arrive_expect_tx_u(fb, kSkABytes + kSkBBytes + 2 * sfb);
+          tma_load_2d_u(w_base + i * kSkABytes, &tmW, fb, kt * 128, nt * 128);
+          bulk_load_u(sfw_base + i * kSkSfBytes, sfw_src, sfb, fb);
+          sfw_src += 2048;
+        }
+      }
+      griddep_wait();
       for (int u = blockIdx.x; ok && u < num_units; u += gridDim.x) {
         const int nt = u / ksplit;
         const int kt0 = (u % ksplit) * kt_per, kt1 = min(p.num_kt, kt0 + kt_per);
         const uint8_t *sfw_src = p.b_sf + 512 * ((int64_t)nt * p.b_sf_katoms + (int64_t)kt0 * 4);
         const uint8_t *sfx_src = p.a_sf + 512 * ((int64_t)kt0 * 4);   // the rows' one 128-row chunk
         for (int kt = kt0; kt < kt1; ++kt) {
-          const bool got = !*abort_flag && mbar_wait_u(empty_base + 8 * stage, phase ^ 1, p.timeout_ns);
+          const bool early = u == (int)blockIdx.x && kt - kt0 < pre;   // weights already in flight
+          const bool got = early || (!*abort_flag && mbar_wait_u(empty_base + 8 * stage, phase ^ 1, p.timeout_ns));
           if (!got) {
             sk_abort(abort_flag, p.status);
             ok = false;
@@ -134,10 +157,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           }
           const uint32_t fb = full_base + 8 * stage;
           const uint32_t sfb = (uint32_t)((kt == p.num_kt - 1 ? last_nk : 4) * 512);
-          mbar_arrive_expect_tx_u(fb, kSkABytes + kSkBBytes + 2 * sfb);
-          tma_load_2d_u(w_base + stage * kSkABytes, &tmW, fb, kt * 128, nt * 128);
+          if (!early) {
+            mbar_arrive_expect_tx_u(fb, kSkABytes + kSkBBytes + 2 * sfb);
+            tma_load_2d_u(w_base + stage * kSkABytes, &tmW, fb, kt * 128, nt * 128);
+            bulk_load_u(sfw_base + stage * kSkSfBytes, sfw_src, sfb, fb);
+          }
           tma_load_2d_u(x_base + stage * kSkBBytes, &tmX, fb, kt * 128, 0);
-          bulk_load_u(sfw_base + stage * kSkSfBytes, sfw_src, sfb, fb);
           bulk_load_u(sfx_base + stage * kSkSfBytes, sfx_src, sfb, fb);
           sfw_src += 2048;
           sfx_src += 2048;

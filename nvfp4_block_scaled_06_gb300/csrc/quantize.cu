@@ -222,8 +222,12 @@ __global__ void __launch_bounds__(256) k_amax_partial(QuantParams p) {
 // written (zeros outside the matrix).
 template <bool kV8>
 __global__ void __launch_bounds__(256) k_quant_rows(QuantParams p) {
-  griddep_launch_dependents();
+  // The wait comes first: a kernel launched after this one starts only once
+  // every earlier kernel of the stream has completed, so it may read data
+  // that this kernel does not write (the operand-swapped GEMM streams its
+  // weights) before its own wait.
   griddep_wait();   // inputs may come from the previous kernel in the stream
+  griddep_launch_dependents();
   __shared__ uint32_t scratch[32];
   __shared__ float senc_tab[128];
   const int b = blockIdx.y;
