@@ -158,7 +158,11 @@ nvfp4_status nvfp4_quantize_noalloc(const nvfp4_quant_args *args, nvfp4_stream s
  *     a_global_scale device scalar), or bf16 a_bf16 [M][lda] quantized inside
  *     the call into the workspace (a_global_scale = static input_scale, or
  *     NULL for the dynamic amax rule); with a_bf16 the decode path for M <= 4
- *     is a CUDA-core GEMV that quantizes X on the fly (static scale only).
+ *     is a CUDA-core GEMV that quantizes X on the fly (static scale only),
+ *     and other products of M <= 32 rows without LoRA run with the operands
+ *     swapped (the weights as the MMA's 128-row side).  The results are the
+ *     same product within the tolerance of the header; which path runs
+ *     depends only on M, the scale form and the LoRA.
  *   B (weights) [N][K]: b_codes [N][K/2], b_sf swizzled, b_global_scale.
  *   D [M][ldd] bf16 or fp32, written (not accumulated).
  *   LoRA (lora_a != NULL): D += (alpha/rank) * (X A^T) B^T with X = the bf16
