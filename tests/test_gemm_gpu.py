@@ -226,7 +226,8 @@ def test_decode_chunked_rows(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K,static", [(8, 1024, 2048, True), (8, 768, 16384, True), (40, 512, 1024, False),
-                                          (300, 512, 512, False), (8, 200, 3072, True), (24, 968, 2560, False)])
+                                          (300, 512, 512, False), (8, 200, 3072, True), (24, 968, 2560, False),
+                                          (2, 520, 4096, False)])
 def test_in_call_x_padding_rows_ignored(M, N, K, static):
     """X quantized in the call is packed into the workspace with its rows
     padded to 128, and the GEMM's tiles span the padding: whatever those

@@ -75,6 +75,29 @@ def test_graph_decode_gemv_static_scale():
     _same(y, want, "decode replay")
 
 
+def test_graph_decode_operand_swapped_split_k():
+    """M = 8 rows with a static scale on a long K: the operand-swapped tcgen05
+    GEMM (weights issued before its wait on the activation packing) and the
+    split-K pass, captured and replayed on new rows."""
+    M, N, K = 8, 768, 16384
+    c = make_case("decode_o_proj", M=M, N=N, K=K)
+    wq = nv.nvfp4_quantize(dev_bf16(c["w"]), pack="row", sf_layout="swizzled")
+    gx = torch.tensor([16.0 / 2688.0], dtype=torch.float32, device="cuda")
+    x = dev_bf16(c["x"])
+    call, y = nv.prepare_gemm(wq["codes_row"], wq["sf_row"], wq["global_scale"], N, K, a_bf16=x,
+                              a_global_scale=gx)
+    g = _capture(call)
+    rng = np.random.default_rng(5)
+    for step in range(2):
+        x.copy_(dev_bf16(_bits(rng, (M, K), 0.5 + step)))
+        g.replay()
+        torch.cuda.synchronize()
+        want = nv.nvfp4_gemm(wq["codes_row"], wq["sf_row"], wq["global_scale"], N, K, a_bf16=x.clone(),
+                             a_global_scale=gx)
+        torch.cuda.synchronize()
+        _same(y, want, f"operand-swapped replay {step}")
+
+
 def test_graph_quantize_batched_both():
     E, R, C = 3, 256, 768
     rng = np.random.default_rng(3)
