@@ -104,8 +104,12 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
   const bool few = p.nchunks <= 32;
   int32_t hv[32];
   if (act && few) {
+    // unconditional loads (the last chunk repeated, its value masked): all
+    // 32 are in flight together
 #pragma unroll
-    for (int j = 0; j < 32; ++j) hv[j] = j < p.nchunks ? p.hist[(int64_t)j * p.num_experts + e] : 0;
+    for (int j = 0; j < 32; ++j) hv[j] = p.hist[(int64_t)min(j, p.nchunks - 1) * p.num_experts + e];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) hv[j] = j < p.nchunks ? hv[j] : 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) count += hv[j];
   } else if (act) {
@@ -133,21 +137,36 @@ __global__ void __launch_bounds__(1024) k_route_scan(const RouteParams p) {
       b += hv[j];
     }
   }
+  __shared__ int32_t s_cnt[1024], s_off[1024], s_poff[1024], s_moff[1024];
   if (act) {
     p.counts[e] = count;
     p.offsets[e] = off;
     p.poffsets[e] = poff;
     if (p.offsets_out) p.offsets_out[e] = off;
-    for (int j = 0; j < mt; ++j) {
-      GroupTile g;
-      g.expert = e;
-      g.a_row0 = poff + 128 * j;
-      g.valid_rows = min(128, count - 128 * j);
-      g.out_row0 = off + 128 * j;
-      if (NVFP4_GUARD(moff + j < p.padded_rows_max / 128, p.status)) p.gtiles[moff + j] = g;
+    s_cnt[e] = count;
+    s_off[e] = off;
+    s_poff[e] = poff;
+    s_moff[e] = moff;
+  }
+  __syncthreads();
+  // one warp per expert: its m-tile entries and its padding rows (up to 127)
+  // written by the 32 lanes
+  {
+    const int lane = threadIdx.x & 31;
+    for (int x = threadIdx.x >> 5; x < p.num_experts; x += blockDim.x >> 5) {
+      const int32_t cnt = s_cnt[x], of = s_off[x], pf = s_poff[x], mo = s_moff[x];
+      const int32_t pad = (cnt + 127) & ~127;
+      for (int j = lane; j < pad / 128; j += 32) {
+        GroupTile g;
+        g.expert = x;
+        g.a_row0 = pf + 128 * j;
+        g.valid_rows = min(128, cnt - 128 * j);
+        g.out_row0 = of + 128 * j;
+        if (NVFP4_GUARD(mo + j < p.padded_rows_max / 128, p.status)) p.gtiles[mo + j] = g;
+      }
+      for (int32_t i = cnt + lane; i < pad; i += 32)
+        if (NVFP4_GUARD(pf + i < p.padded_rows_max, p.status)) p.row_map[pf + i] = -1;
     }
-    for (int32_t i = count; i < padded; ++i)
-      if (NVFP4_GUARD(poff + i < p.padded_rows_max, p.status)) p.row_map[poff + i] = -1;
   }
   if (threadIdx.x == 0) {
     p.offsets[p.num_experts] = total;
